@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark: distance-bound smoothing of the n = 16384 lattice globule (fp32).
+
+One step = one complete bs_smooth_bounds call (blocked three-phase
+Floyd-Warshall, all 128 block rounds) on a fresh copy of the bound pair that
+is already resident in HBM.  Metric: cell-updates/s = n^3 / time per step,
+and its fraction of the FP32 ALU peak (6 ALU ops per cell update:
+U add + min, L two subtractions + two maxima; peak = SMs x 128 lanes x
+max SM clock).
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead
+(bounded samples of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "bound-smoothing cell-updates/s (n³/time) and % of GB300 FP32 ALU peak"
+UNIT = "cell-updates/s"
+OPS_PER_CELL = 6
+FP32_LANES_PER_SM = 128
+WORKLOADS = {
+    "globule16384": dict(config=4, desc="lattice globule n=16384, fp32 U+L, blocked"),
+    "globule4096": dict(config=2, desc="lattice globule n=4096, fp32 U+L, blocked"),
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d.get("hbm_gbs", 6800.0), sm_max_mhz=d.get("sm_max_mhz", 2070.0),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, sm_max_mhz=2070.0, source="fallback")
+
+
+def kernel_hash():
+    """Hash of the CUDA sources: ties a committed ncu traffic figure to the code."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "blocked_floyd_warshall_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(n):
+    """DRAM bytes per phase-3 launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "phase3_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    per_cell_k = d.get("dram_bytes_per_cell_k")
+    if per_cell_k is None:
+        return None
+    fb = 128
+    return per_cell_k * float(n - fb) ** 2 * fb
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = os.path.join("/tmp", "bs_clocks_%d.csv" % os.getpid())
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        with open(self.out) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(self.NAMES, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.out)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_smi_id(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[torch.cuda.current_device()] if vis else torch.cuda.current_device()
+
+
+# ------------------------------------------------------------------ distributed
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ oracle leg
+
+
+def oracle_rate(U0, L0, seconds, max_rounds=None):
+    """Time the CPU oracle on rounds 0..R-1 of the workload until `seconds`
+    elapse; returns (cell-updates/s, rounds, threads)."""
+    import oracle
+    oracle.build()
+    U = U0.copy()
+    L = L0.copy()
+    n = U.shape[0]
+    rounds, t0 = 0, time.perf_counter()
+    chunk = 4
+    while True:
+        k1 = min(n, rounds + chunk)
+        oracle.smooth(U, L, k_begin=rounds, k_end=k1, inplace=True)
+        rounds = k1
+        el = time.perf_counter() - t0
+        if el >= seconds or rounds >= n or (max_rounds and rounds >= max_rounds):
+            break
+    return rounds * float(n) * n / el, rounds, oracle.threads(), el
+
+
+# ------------------------------------------------------------------ main
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    from workloads import make_config, to_f32
+    wl = WORKLOADS[args.workload]
+    m = make_config(wl["config"])
+    U0, L0 = to_f32(m["U"]), to_f32(m["L"])
+    n = m["n"]
+    times, rates = [], []
+    per_step = args.ref_rounds
+    for s in range(args.warmup + args.steps):
+        rate, rounds, thr, el = oracle_rate(U0, L0, seconds=1e9, max_rounds=per_step)
+        if s >= args.warmup:
+            times.append(el)
+            rates.append(rate)
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl["desc"], "n": n, "batch": 1},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                         "sample": "each step: rounds 0..%d of the n=%d workload "
+                                   "(%d x n^2 cell updates)" % (per_step - 1, n, per_step)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="globule16384")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU-oracle sample length for cpu_baseline")
+    ap.add_argument("--ref-rounds", type=int, default=48,
+                    help="oracle rounds per step for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import torch
+    import blocked_floyd_warshall_gb300 as bsm
+    from workloads import make_config, to_f32
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    bsm.build()
+    bsm.library()
+
+    wl = WORKLOADS[args.workload]
+    m = make_config(wl["config"])
+    n = m["n"]
+    U0, L0 = to_f32(m["U"]), to_f32(m["L"])
+    dU0 = torch.from_numpy(U0).cuda()
+    dL0 = torch.from_numpy(L0).cuda()
+    stream = torch.cuda.current_stream()
+    ncopies = min(args.steps, 32)
+    copies = [(dU0.clone(), dL0.clone()) for _ in range(ncopies)]
+    wU, wL = dU0.clone(), dL0.clone()
+
+    # warm-up on a scratch copy
+    for _ in range(args.warmup):
+        wU.copy_(dU0)
+        wL.copy_(dL0)
+        bsm.bs_smooth_bounds(wU, wL)
+    torch.cuda.synchronize()
+
+    # timed region: K steps, each on its own resident copy
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = bsm.bs_launch_count()
+    with ClockSampler(gpu_smi_id(torch)) as clk:
+        bsm.bs_profile_begin()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            U, L = copies[s % ncopies]
+            ev[s][0].record(stream)
+            bsm.bs_smooth_bounds(U, L)
+            ev[s][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        prof = bsm.bs_profile_end()
+    launches = bsm.bs_launch_count() - launches0
+    total_ms = t_start.elapsed_time(t_end)
+    if ws > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    cells = float(n) ** 3
+    value = ws * args.steps * cells / (total_ms * 1e-3)
+
+    # parity of the timed output: the stored result is the fixed point, so one
+    # more smoothing must leave it unchanged and the flags must be zero
+    U, L = copies[0]
+    assert bsm.bs_check_feasible(U, L) == 0
+
+    peaks = load_peaks()
+    fmax = peaks["sm_max_mhz"] * 1e6
+    alu_peak_ops = sms * FP32_LANES_PER_SM * fmax            # ALU ops/s
+    p3 = prof["phase3"]
+    fb = 128
+    p3_ops_per_launch = float(n - fb) ** 2 * fb * OPS_PER_CELL
+    p3_avg_s = p3["ms"] * 1e-3 / max(1, p3["launches"])
+    p3_achieved = p3_ops_per_launch / p3_avg_s if p3["launches"] else None
+    traffic = committed_traffic(n)
+    clocks = clk.summary()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl["desc"], "n": n, "batch": 1, "mode": "blocked",
+                   "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": "inputs larger than L2: each step smooths its own resident "
+                         "2 x %d MiB copy" % (n * n * 4 >> 20)},
+        "fp32_alu_frac": value / ws * OPS_PER_CELL / alu_peak_ops,
+        "fp32_alu_peak_basis": "%d SMs x %d lanes x %.0f MHz (%s max SM clock)" % (
+            sms, FP32_LANES_PER_SM, peaks["sm_max_mhz"], peaks["source"]),
+        "step_ms": {"median": statistics.median(step_ms), "best": min(step_ms)},
+        "roofline": {
+            "kernel": "k_phase3 (bulk tile update)", "bound": "alu",
+            "achieved": p3_achieved / 1e12 if p3_achieved else None,
+            "peak": alu_peak_ops / 1e12, "unit": "Tops/s",
+            "frac": (p3_achieved / alu_peak_ops) if p3_achieved else None,
+            "traffic": traffic,
+            "ops_per_launch": p3_ops_per_launch,
+            "avg_launch_ms": p3_avg_s * 1e3,
+            "launches": p3["launches"],
+            "share_of_step": p3["ms"] / max(1e-9, sum(prof[k]["ms"] for k in bsm.PHASES)),
+            "peak_basis": "SMs x 128 FP32 lanes x max SM clock, 6 ALU ops per cell update (%s)"
+                          % peaks["source"],
+        },
+        "phases_ms_per_step": {k: prof[k]["ms"] / args.steps for k in bsm.PHASES},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_leg(torch, bsm, U0, L0, args, ws)
+    if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:
+        rate, rounds, thr, el = oracle_rate(U0, L0, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": "rounds 0..%d of the n=%d workload (%d x n^2 cell updates, %.1f s)"
+                      % (rounds - 1, n, rounds, el)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def e2e_leg(torch, bsm, U0, L0, args, ws):
+    """Same metric through the public call with host buffers: each step copies
+    the pinned inputs to the device, smooths, and reads both results back."""
+    n = U0.shape[0]
+    hU = torch.from_numpy(U0).pin_memory()
+    hL = torch.from_numpy(L0).pin_memory()
+    oU = torch.empty_like(hU).pin_memory()
+    oL = torch.empty_like(hL).pin_memory()
+    dU = torch.empty(hU.shape, dtype=hU.dtype, device="cuda")
+    dL = torch.empty(hL.shape, dtype=hL.dtype, device="cuda")
+    steps = max(1, min(args.steps, 3))
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        dU.copy_(hU, non_blocking=True)
+        dL.copy_(hL, non_blocking=True)
+        bsm.bs_smooth_bounds(dU, dL)
+        oU.copy_(dU, non_blocking=True)
+        oL.copy_(dL, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    nbytes = 2 * n * n * 4
+    return {"value": ws * steps * float(n) ** 3 / (ms * 1e-3), "unit": UNIT,
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

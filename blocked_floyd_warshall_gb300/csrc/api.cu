@@ -1,0 +1,284 @@
+// C ABI of libbsmooth: argument checks, dispatch to the kernels, the small
+// per-device buffer used by the feasibility count and the input check, launch
+// counting and the optional per-phase event profile.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/bsmooth.h"
+#include "bs_internal.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;                   // kernel attributes set
+    unsigned long long* scratch = nullptr;  // [0] count, [1] validation flags
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<long long> g_launches{0};
+
+// ---- profiling ------------------------------------------------------------
+
+struct ProfRec {
+    cudaEvent_t a, b;
+    int phase;
+};
+constexpr size_t kMaxProf = 1u << 16;
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+bool g_prof_overflow = false;
+std::vector<ProfRec> g_prof;
+thread_local cudaEvent_t t_pending = nullptr;
+
+cudaError_t device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        e = bs::blocked_setup(false);
+        if (e == cudaSuccess) e = bs::blocked_setup(true);
+        if (e != cudaSuccess) return e;
+        d.ready = true;
+    }
+    *out = &d;
+    return cudaSuccess;
+}
+
+cudaError_t device_scratch(unsigned long long** out) {
+    DeviceState* d = nullptr;
+    cudaError_t e = device_state(&d);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!d->scratch) {
+        e = cudaMalloc(reinterpret_cast<void**>(&d->scratch), 2 * sizeof(unsigned long long));
+        if (e != cudaSuccess) {
+            d->scratch = nullptr;
+            return e;
+        }
+    }
+    *out = d->scratch;
+    return cudaSuccess;
+}
+
+bs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BS_OK : BS_ERR_CUDA; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common argument checks.  Returns BS_OK and fills `m`, or an error.
+bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
+                     long long bstride, int batch, int mode, bs::Mats* m) {
+    const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE;
+    if (mode & ~known) return BS_ERR_ARG;
+    if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
+    if (n < 0 || batch < 0) return BS_ERR_ARG;
+    if (n > 0 && ld < n) return BS_ERR_ARG;
+    if (n > 0 && batch > 0) {
+        if (!U || (bounds && !L)) return BS_ERR_ARG;
+        if (bounds && U == L) return BS_ERR_ARG;
+        const long long span = (long long)(n - 1) * ld + n;
+        if (batch > 1 && bstride < span) return BS_ERR_ARG;
+        if (!aligned(U, 4) || (bounds && !aligned(L, 4))) return BS_ERR_ALIGN;
+    }
+    m->U = const_cast<void*>(U);
+    m->L = bounds ? const_cast<void*>(L) : nullptr;
+    m->n = n;
+    m->ld = ld;
+    m->bstride = batch > 1 ? bstride : 0;
+    m->batch = batch;
+    m->vec = (ld % 4 == 0) && aligned(U, 16) && (!bounds || aligned(L, 16)) &&
+             (batch <= 1 || bstride % 4 == 0);
+    return BS_OK;
+}
+
+bs_status validate(const bs::Mats& m, bool is_int, cudaStream_t s) {
+    unsigned long long* scr = nullptr;
+    cudaError_t e = device_scratch(&scr);
+    if (e != cudaSuccess) return BS_ERR_CUDA;
+    unsigned int* flags = reinterpret_cast<unsigned int*>(scr + 1);
+    e = cudaMemsetAsync(flags, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess) e = bs::launch_validate(is_int, m, flags, s);
+    unsigned int h = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, flags, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return BS_ERR_CUDA;
+    if (h & (bs::VF_DIAG | bs::VF_NEG | bs::VF_NAN | bs::VF_LINF)) return BS_ERR_INPUT;
+    if (h & bs::VF_RANGE) return BS_ERR_RANGE;
+    return BS_OK;
+}
+
+bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride, int batch,
+                 cudaStream_t s, int mode) {
+    bs::Mats m;
+    bs_status st = check_args(U, L, bounds, n, ld, bstride, batch, mode, &m);
+    if (st != BS_OK) return st;
+    const bool perk = (mode & BS_PERK) != 0;
+    const bool literal = bounds && (mode & BS_RULE_LITERAL) != 0;
+    if (literal && !perk) return BS_ERR_ARG;
+    if (n == 0 || batch == 0) return BS_OK;
+    const bool is_int = (mode & BS_DTYPE_MASK) == BS_INT32_Q10;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != cudaSuccess) return BS_ERR_CUDA;
+    if (mode & BS_VALIDATE) {
+        st = validate(m, is_int, s);
+        if (st != BS_OK) return st;
+    }
+    cudaError_t e = cudaSuccess;
+    if (perk) {
+        for (int k = 0; k < n && e == cudaSuccess; ++k) {
+            e = bs::launch_round(is_int, m, k, literal, s);
+            if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
+        }
+    } else {
+        const int nb = (n + bs::FB - 1) / bs::FB;
+        for (int K = 0; K < nb && e == cudaSuccess; ++K) {
+            e = bs::launch_phase1(is_int, m, K, s);
+            if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K, s);
+            if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, s);
+        }
+    }
+    return cuda_status(e);
+}
+
+}  // namespace
+
+// ---- launch bookkeeping used by the kernel translation units ---------------
+
+namespace bs {
+
+void before_launch(cudaStream_t s, int) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    t_pending = nullptr;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    if (g_prof.size() >= kMaxProf) {
+        g_prof_overflow = true;
+        return;
+    }
+    cudaEvent_t a;
+    if (cudaEventCreate(&a) != cudaSuccess) return;
+    cudaEventRecord(a, s);
+    t_pending = a;
+}
+
+void after_launch(cudaStream_t s, int phase) {
+    if (!t_pending) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEvent_t b;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+        cudaEventDestroy(t_pending);
+        t_pending = nullptr;
+        return;
+    }
+    cudaEventRecord(b, s);
+    g_prof.push_back(ProfRec{t_pending, b, phase});
+    t_pending = nullptr;
+}
+
+}  // namespace bs
+
+// ---- the C ABI -------------------------------------------------------------
+
+extern "C" {
+
+bs_status bs_smooth_upper(void* U, int n, int ld, bs_stream_t stream, int mode) {
+    // rule bits have no meaning for the upper bound alone
+    return smooth(U, nullptr, false, n, ld, 0, 1, stream, mode & ~BS_RULE_LITERAL);
+}
+
+bs_status bs_smooth_bounds(void* U, void* L, int n, int ld, bs_stream_t stream, int mode) {
+    return smooth(U, L, true, n, ld, 0, 1, stream, mode);
+}
+
+bs_status bs_smooth_bounds_batched(void* U, void* L, int n, int ld, long long batch_stride,
+                                   int batch, bs_stream_t stream, int mode) {
+    return smooth(U, L, true, n, ld, batch_stride, batch, stream, mode);
+}
+
+bs_status bs_check_feasible(const void* U, const void* L, int n, int ld, bs_stream_t stream,
+                            int mode, long long* out_count, unsigned char* mask) {
+    if (!out_count) return BS_ERR_ARG;
+    bs::Mats m;
+    bs_status st = check_args(U, L, true, n, ld, 0, 1, mode & BS_DTYPE_MASK, &m);
+    if (st != BS_OK) return st;
+    if (n == 0) {
+        *out_count = 0;
+        return BS_OK;
+    }
+    const bool is_int = (mode & BS_DTYPE_MASK) == BS_INT32_Q10;
+    unsigned long long* scr = nullptr;
+    cudaError_t e = device_scratch(&scr);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scr, 0, sizeof(unsigned long long), stream);
+    if (e == cudaSuccess) e = bs::launch_feasible(is_int, m, mask, scr, stream);
+    unsigned long long h = 0;
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&h, scr, sizeof h, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return BS_ERR_CUDA;
+    *out_count = (long long)h;
+    return BS_OK;
+}
+
+const char* bs_strerror(bs_status status) {
+    switch (status) {
+        case BS_OK: return "success";
+        case BS_ERR_ARG: return "invalid argument (n, ld, batch, stride, pointer or mode bits)";
+        case BS_ERR_ALIGN: return "matrix pointer not aligned to its element size";
+        case BS_ERR_RANGE: return "int32 bound outside [0, 2^30)";
+        case BS_ERR_CUDA: return "CUDA launch or call failed";
+        case BS_ERR_TIMEOUT: return "bounded device wait ran out";
+        case BS_ERR_INPUT: return "input violates preconditions (diagonal, sign, NaN, infinite lower bound)";
+    }
+    return "unknown status";
+}
+
+long long bs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+bs_status bs_profile_begin(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& r : g_prof) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    g_prof.clear();
+    g_prof_overflow = false;
+    g_prof_on = true;
+    return BS_OK;
+}
+
+bs_status bs_profile_end(bs_profile* out) {
+    std::vector<ProfRec> recs;
+    bool overflow;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        g_prof_on = false;
+        recs.swap(g_prof);
+        overflow = g_prof_overflow;
+    }
+    bs_profile p{};
+    cudaError_t first = cudaSuccess;
+    for (auto& r : recs) {
+        float ms = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+        if (e == cudaSuccess && r.phase >= 0 && r.phase < 4) {
+            p.ms[r.phase] += ms;
+            p.launches[r.phase] += 1;
+        } else if (first == cudaSuccess) {
+            first = e;
+        }
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    p.overflow = overflow ? 1 : 0;
+    if (out) *out = p;
+    return cuda_status(first);
+}
+
+}  // extern "C"

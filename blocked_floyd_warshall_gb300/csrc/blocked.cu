@@ -1,0 +1,392 @@
+// Three-phase blocked Floyd-Warshall over the bound pair (U, L).
+//
+// The matrix is cut into FB x FB tiles; block round K processes the middle
+// atoms k of tile-row K in order, in three launches:
+//   phase 1: tile (K,K), k serially, one CTA;
+//   phase 2: row panel (K,J) and column panel (I,K), k serially, against the
+//            finished diagonal tile;
+//   phase 3: every other tile (I,J), against the finished panels.  Its
+//            operands are final, so the k order inside the block is free and U
+//            and L are updated together in one pass.
+//
+// Rules (GPU Gems 2 ch. 43, section 2): U[i,j] = min(U[i,j], U[i,k] + U[k,j]);
+// L[i,j] = max(L[i,j], L[k,j] - U[i,k], Lcol[i] - U[k,j]), with the upper
+// bound tightened first.  Lcol[i] is L[i,k] raised to max(L[i,k], L[k,k] -
+// U[i,k]) wherever column k is still being formed (phase 1, column panel);
+// phase-2 row panels and phase 3 read finished column values where that raise
+// is already contained.  The result is the fixed point of the triangle
+// inequalities, the same as the round-by-round schedule (exactly in int32; in
+// fp32 exactly for values on the 1/1024 grid below 2^14).
+//
+// Inside phases 1 and 2 each step k is round-synchronous: every thread keeps
+// its cells in registers, row k / column k are published to a shared vector
+// double-buffered by k parity, one barrier per step.
+#include "bs_tile.cuh"
+
+namespace bs {
+
+namespace {
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- phase 1
+
+template <class T, bool HAS_L>
+__global__ void __launch_bounds__(NT, 1)
+k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
+    using E = El<T>;
+    __shared__ T sRU[2][FB], sRL[2][FB], sCU[2][FB], sCL[2][FB];
+    const size_t off = (size_t)blockIdx.z * (size_t)bstride;
+    U += off;
+    if (HAS_L) L += off;
+    const int o = K * FB;
+    const int m = min(FB, n - o);
+    T* Ut = U + (size_t)o * ld + o;
+    T* Lt = HAS_L ? L + (size_t)o * ld + o : nullptr;
+
+    T u[TM][TN], l[TM][TN];
+    load_tile(u, Ut, ld, m, m, vec, E::upad());
+    if (HAS_L) load_tile(l, Lt, ld, m, m, vec, E::lpad());
+    publish_row<T, HAS_L>(u, l, 0, sRU[0], sRL[0]);
+    publish_col<T, HAS_L>(u, l, 0, sCU[0], sCL[0]);
+    __syncthreads();
+
+    const int r0 = mt_row0();
+    for (int k = 0; k < m; ++k) {
+        const int b = k & 1;
+        T a[TM], al[TM], bb[TN], bl[TN];
+#pragma unroll
+        for (int r = 0; r < TM; ++r) {
+            a[r] = sCU[b][r0 + r];
+            al[r] = HAS_L ? sCL[b][r0 + r] : T(0);
+        }
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            bb[c] = sRU[b][mt_col(c)];
+            bl[c] = HAS_L ? sRL[b][mt_col(c)] : T(0);
+        }
+        if (HAS_L) {
+            const T lkk = sRL[b][k];
+#pragma unroll
+            for (int r = 0; r < TM; ++r) al[r] = E::mx(al[r], E::sub(lkk, a[r]));
+        }
+        fw_update<T, HAS_L>(u, l, a, al, bb, bl);
+        if (k + 1 < m) {
+            publish_row<T, HAS_L>(u, l, k + 1, sRU[b ^ 1], sRL[b ^ 1]);
+            publish_col<T, HAS_L>(u, l, k + 1, sCU[b ^ 1], sCL[b ^ 1]);
+        }
+        __syncthreads();
+    }
+    store_tile(u, Ut, ld, m, m, vec);
+    if (HAS_L) store_tile(l, Lt, ld, m, m, vec);
+}
+
+// ---------------------------------------------------------------- phase 2
+
+constexpr int DPAD = 1;   // diagonal tile row stride FB + DPAD in shared memory
+
+template <class T, bool HAS_L>
+__global__ void __launch_bounds__(NT, 1)
+k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
+    using E = El<T>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* dU = reinterpret_cast<T*>(smem_raw);
+    T* dL = dU + FB * (FB + DPAD);
+    __shared__ T sU[2][FB], sL[2][FB];
+
+    const size_t off = (size_t)blockIdx.z * (size_t)bstride;
+    U += off;
+    if (HAS_L) L += off;
+    const int o = K * FB;
+    const int mk = min(FB, n - o);
+    const int P = (int)blockIdx.x + ((int)blockIdx.x >= K);
+    const int op = P * FB;
+    const int mp = min(FB, n - op);
+    const bool row_panel = blockIdx.y == 0;
+
+    // the finished diagonal tile, padded
+    for (int e = threadIdx.x; e < FB * FB; e += NT) {
+        const int i = e / FB, j = e % FB;
+        const bool in = i < mk && j < mk;
+        dU[i * (FB + DPAD) + j] = in ? U[(size_t)(o + i) * ld + o + j] : E::upad();
+        if (HAS_L) dL[i * (FB + DPAD) + j] = in ? L[(size_t)(o + i) * ld + o + j] : E::lpad();
+    }
+
+    const int r0 = mt_row0();
+    T u[TM][TN], l[TM][TN];
+    if (row_panel) {
+        // tile (K, P): rows of block K, columns of block P
+        T* Ut = U + (size_t)o * ld + op;
+        T* Lt = HAS_L ? L + (size_t)o * ld + op : nullptr;
+        load_tile(u, Ut, ld, mk, mp, vec, E::upad());
+        if (HAS_L) load_tile(l, Lt, ld, mk, mp, vec, E::lpad());
+        publish_row<T, HAS_L>(u, l, 0, sU[0], sL[0]);
+        __syncthreads();
+        for (int k = 0; k < mk; ++k) {
+            const int b = k & 1;
+            T a[TM], al[TM], bb[TN], bl[TN];
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                a[r] = dU[(r0 + r) * (FB + DPAD) + k];
+                al[r] = HAS_L ? dL[(r0 + r) * (FB + DPAD) + k] : T(0);
+            }
+#pragma unroll
+            for (int c = 0; c < TN; ++c) {
+                bb[c] = sU[b][mt_col(c)];
+                bl[c] = HAS_L ? sL[b][mt_col(c)] : T(0);
+            }
+            fw_update<T, HAS_L>(u, l, a, al, bb, bl);
+            if (k + 1 < mk) publish_row<T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
+            __syncthreads();
+        }
+        store_tile(u, Ut, ld, mk, mp, vec);
+        if (HAS_L) store_tile(l, Lt, ld, mk, mp, vec);
+    } else {
+        // tile (P, K): rows of block P, columns of block K
+        T* Ut = U + (size_t)op * ld + o;
+        T* Lt = HAS_L ? L + (size_t)op * ld + o : nullptr;
+        load_tile(u, Ut, ld, mp, mk, vec, E::upad());
+        if (HAS_L) load_tile(l, Lt, ld, mp, mk, vec, E::lpad());
+        publish_col<T, HAS_L>(u, l, 0, sU[0], sL[0]);
+        __syncthreads();
+        for (int k = 0; k < mk; ++k) {
+            const int b = k & 1;
+            T a[TM], al[TM], bb[TN], bl[TN];
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                a[r] = sU[b][r0 + r];
+                al[r] = HAS_L ? sL[b][r0 + r] : T(0);
+            }
+#pragma unroll
+            for (int c = 0; c < TN; ++c) {
+                bb[c] = dU[k * (FB + DPAD) + mt_col(c)];
+                bl[c] = HAS_L ? dL[k * (FB + DPAD) + mt_col(c)] : T(0);
+            }
+            if (HAS_L) {
+                const T lkk = dL[k * (FB + DPAD) + k];
+#pragma unroll
+                for (int r = 0; r < TM; ++r) al[r] = E::mx(al[r], E::sub(lkk, a[r]));
+            }
+            fw_update<T, HAS_L>(u, l, a, al, bb, bl);
+            if (k + 1 < mk) publish_col<T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
+            __syncthreads();
+        }
+        store_tile(u, Ut, ld, mp, mk, vec);
+        if (HAS_L) store_tile(l, Lt, ld, mp, mk, vec);
+    }
+}
+
+// ---------------------------------------------------------------- phase 3
+
+constexpr int BK = 16;        // k-chunk staged per pipeline stage
+constexpr int AST = BK + 4;   // column-panel row stride (elements); rows stay 16-byte aligned
+
+template <class T, bool HAS_L>
+struct P3Smem {
+    // one stage: column panel A[i][k] (FB x BK) and row panel B[k][j] (BK x FB)
+    static constexpr int A_ELEMS = FB * AST;
+    static constexpr int B_ELEMS = BK * FB;
+    static constexpr int MATS = HAS_L ? 2 : 1;
+    static constexpr int STAGE = MATS * (A_ELEMS + B_ELEMS);
+    static constexpr size_t BYTES = 2 * STAGE * sizeof(T);
+};
+
+// Stage k-chunk `c` of both panels into shared memory stage `st`.
+template <class T, bool HAS_L>
+__device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_t ld, int oi,
+                                         int oj, int ok, int mi, int mj, int mk, int c,
+                                         bool vec) {
+    using E = El<T>;
+    using S = P3Smem<T, HAS_L>;
+    // stage layout: AU | BU | AL | BL
+    T* AU = stage;
+    T* BU = stage + S::A_ELEMS;
+    T* AL = HAS_L ? BU + S::B_ELEMS : nullptr;
+    T* BL = HAS_L ? AL + S::A_ELEMS : nullptr;
+    const int kc = c * BK;
+    // column panel: FB rows x BK columns = FB * BK/4 pieces of 4 elements
+    for (int p = threadIdx.x; p < FB * (BK / 4); p += NT) {
+        const int i = p / (BK / 4);
+        const int kq = (p % (BK / 4)) * 4;
+        const size_t g = (size_t)(oi + i) * ld + ok + kc + kq;
+        const bool full = i < mi && kc + kq + 4 <= mk;
+        if (vec && full) {
+            cp_async16(AU + i * AST + kq, U + g);
+            if (HAS_L) cp_async16(AL + i * AST + kq, L + g);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool in = i < mi && kc + kq + q < mk;
+                AU[i * AST + kq + q] = in ? U[g + q] : E::upad();
+                if (HAS_L) AL[i * AST + kq + q] = in ? L[g + q] : E::lpad();
+            }
+        }
+    }
+    // row panel: BK rows x FB columns
+    for (int p = threadIdx.x; p < BK * (FB / 4); p += NT) {
+        const int k = p / (FB / 4);
+        const int j = (p % (FB / 4)) * 4;
+        const size_t g = (size_t)(ok + kc + k) * ld + oj + j;
+        const bool krow = kc + k < mk;
+        if (vec && krow && j + 4 <= mj) {
+            cp_async16(BU + k * FB + j, U + g);
+            if (HAS_L) cp_async16(BL + k * FB + j, L + g);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool in = krow && j + q < mj;
+                BU[k * FB + j + q] = in ? U[g + q] : E::upad();
+                if (HAS_L) BL[k * FB + j + q] = in ? L[g + q] : E::lpad();
+            }
+        }
+    }
+}
+
+template <class T, bool HAS_L>
+__global__ void __launch_bounds__(NT, 1)
+k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
+    using E = El<T>;
+    using S = P3Smem<T, HAS_L>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* sm = reinterpret_cast<T*>(smem_raw);
+
+    const size_t off = (size_t)blockIdx.z * (size_t)bstride;
+    U += off;
+    if (HAS_L) L += off;
+    const int nb = (n + FB - 1) / FB;
+    const int t = blockIdx.x;
+    const int ti = t / (nb - 1), tj = t % (nb - 1);
+    const int I = ti + (ti >= K), J = tj + (tj >= K);
+    const int oi = I * FB, oj = J * FB, ok = K * FB;
+    const int mi = min(FB, n - oi), mj = min(FB, n - oj), mk = min(FB, n - ok);
+
+    T u[TM][TN], l[TM][TN];
+    load_tile(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
+    if (HAS_L) load_tile(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
+
+    const int nchunks = (mk + BK - 1) / BK;
+    p3_stage<T, HAS_L>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
+    cp_async_commit();
+    const int r0 = mt_row0(), cq = mt_cq();
+    for (int c = 0; c < nchunks; ++c) {
+        if (c + 1 < nchunks)
+            p3_stage<T, HAS_L>(sm + ((c + 1) & 1) * S::STAGE, U, L, ld, oi, oj, ok, mi, mj, mk,
+                               c + 1, vec);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const T* AU = sm + (c & 1) * S::STAGE;
+        const T* BU = AU + S::A_ELEMS;
+        const T* AL = AU + S::A_ELEMS + S::B_ELEMS;
+        const T* BL = AL + S::A_ELEMS;
+#pragma unroll 4
+        for (int kk = 0; kk < BK; ++kk) {
+            T a[TM], al[TM], bb[TN], bl[TN];
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                a[r] = AU[(r0 + r) * AST + kk];
+                al[r] = HAS_L ? AL[(r0 + r) * AST + kk] : T(0);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const typename E::V4 v = *reinterpret_cast<const typename E::V4*>(BU + kk * FB + h * 64 + cq);
+                bb[h * 4 + 0] = v.x; bb[h * 4 + 1] = v.y; bb[h * 4 + 2] = v.z; bb[h * 4 + 3] = v.w;
+                if (HAS_L) {
+                    const typename E::V4 w = *reinterpret_cast<const typename E::V4*>(BL + kk * FB + h * 64 + cq);
+                    bl[h * 4 + 0] = w.x; bl[h * 4 + 1] = w.y; bl[h * 4 + 2] = w.z; bl[h * 4 + 3] = w.w;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) bl[h * 4 + q] = T(0);
+                }
+            }
+            fw_update<T, HAS_L>(u, l, a, al, bb, bl);
+        }
+        __syncthreads();
+    }
+    store_tile(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
+    if (HAS_L) store_tile(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
+}
+
+// ---------------------------------------------------------------- launchers
+
+template <class T, bool HAS_L>
+static size_t p2_smem() {
+    return (size_t)(HAS_L ? 2 : 1) * FB * (FB + DPAD) * sizeof(T);
+}
+
+template <class T, bool HAS_L>
+static cudaError_t setup_t() {
+    cudaError_t e = cudaFuncSetAttribute(k_phase2<T, HAS_L>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)p2_smem<T, HAS_L>());
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_phase3<T, HAS_L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)P3Smem<T, HAS_L>::BYTES);
+}
+
+cudaError_t blocked_setup(bool is_int) {
+    cudaError_t e = is_int ? setup_t<int, true>() : setup_t<float, true>();
+    if (e != cudaSuccess) return e;
+    return is_int ? setup_t<int, false>() : setup_t<float, false>();
+}
+
+enum class Which { One, Two, Three };
+
+template <class T, bool HAS_L>
+static cudaError_t phase_t(Which w, const Mats& m, int K, cudaStream_t s) {
+    const int nb = (m.n + FB - 1) / FB;
+    for (int b0 = 0; b0 < m.batch; b0 += 65535) {
+        const int nbz = m.batch - b0 < 65535 ? m.batch - b0 : 65535;
+        T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
+        T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
+        if (w == Which::One) {
+            before_launch(s, PH_ONE);
+            k_phase1<T, HAS_L><<<dim3(1, 1, nbz), NT, 0, s>>>(U, L, m.n, m.ld, m.bstride, K, m.vec);
+            after_launch(s, PH_ONE);
+        } else if (w == Which::Two) {
+            if (nb < 2) return cudaSuccess;
+            before_launch(s, PH_TWO);
+            k_phase2<T, HAS_L><<<dim3(nb - 1, 2, nbz), NT, p2_smem<T, HAS_L>(), s>>>(
+                U, L, m.n, m.ld, m.bstride, K, m.vec);
+            after_launch(s, PH_TWO);
+        } else {
+            if (nb < 2) return cudaSuccess;
+            before_launch(s, PH_THREE);
+            k_phase3<T, HAS_L><<<dim3((nb - 1) * (nb - 1), 1, nbz), NT, P3Smem<T, HAS_L>::BYTES,
+                                 s>>>(U, L, m.n, m.ld, m.bstride, K, m.vec);
+            after_launch(s, PH_THREE);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+static cudaError_t phase(Which w, bool is_int, const Mats& m, int K, cudaStream_t s) {
+    if (is_int) return m.L ? phase_t<int, true>(w, m, K, s) : phase_t<int, false>(w, m, K, s);
+    return m.L ? phase_t<float, true>(w, m, K, s) : phase_t<float, false>(w, m, K, s);
+}
+
+cudaError_t launch_phase1(bool is_int, const Mats& m, int K, cudaStream_t s) {
+    return phase(Which::One, is_int, m, K, s);
+}
+cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s) {
+    return phase(Which::Two, is_int, m, K, s);
+}
+cudaError_t launch_phase3(bool is_int, const Mats& m, int K, cudaStream_t s) {
+    return phase(Which::Three, is_int, m, K, s);
+}
+
+}  // namespace bs

@@ -1,0 +1,61 @@
+// Internal declarations shared by the CUDA translation units of libbsmooth.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bs {
+
+// Floyd-Warshall block (tile) size of the three-phase schedule, and the CTA
+// shape every blocked kernel uses: 256 threads, each owning an 8 x 8 micro-tile
+// of U (and of L) -- rows 8*ty .. 8*ty+7, columns 4*tx+q and 64+4*tx+q
+// (ty = tid/16, tx = tid%16, q = 0..3).
+constexpr int FB = 128;
+constexpr int NT = 256;
+constexpr int TM = 8;
+constexpr int TN = 8;
+
+// One batch of matrices as the kernels see it.
+struct Mats {
+    void* U;
+    void* L;              // nullptr: upper bounds only
+    int n;
+    int ld;
+    long long bstride;    // elements between molecules
+    int batch;
+    bool vec;             // 16-byte vector IO allowed (ld % 4 == 0, bases 16B-aligned)
+};
+
+enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3 };
+
+// Launch bookkeeping (api.cu): counts launches and, when profiling, records an
+// event pair around each launch on `s`.
+void before_launch(cudaStream_t s, int phase);
+void after_launch(cudaStream_t s, int phase);
+
+// Per-round (reference) mode, round k.
+cudaError_t launch_round(bool is_int, const Mats& m, int k, bool literal, cudaStream_t s);
+cudaError_t launch_cross(bool is_int, const Mats& m, int k, cudaStream_t s);
+
+// Blocked mode, block round K.
+cudaError_t blocked_setup(bool is_int);   // once per device: shared-memory limits
+cudaError_t launch_phase1(bool is_int, const Mats& m, int K, cudaStream_t s);
+cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
+cudaError_t launch_phase3(bool is_int, const Mats& m, int K, cudaStream_t s);
+
+// Feasibility count and precondition checks.  `count` and `flags` are device
+// words the caller has zeroed on `s`.
+cudaError_t launch_feasible(bool is_int, const Mats& m, unsigned char* mask,
+                            unsigned long long* count, cudaStream_t s);
+cudaError_t launch_validate(bool is_int, const Mats& m, unsigned int* flags, cudaStream_t s);
+
+// flag bits written by the validation kernel
+enum : unsigned int {
+    VF_DIAG = 1u,       // nonzero diagonal
+    VF_NEG = 2u,        // negative value
+    VF_NAN = 4u,        // NaN
+    VF_LINF = 8u,       // infinite lower bound
+    VF_RANGE = 16u      // int32 value >= 2^30
+};
+
+}  // namespace bs

@@ -1,0 +1,158 @@
+// Device helpers: element traits, the per-thread 8 x 8 micro-tile, and the
+// cell update of one Floyd-Warshall round.
+#pragma once
+
+#include "bs_internal.cuh"
+
+namespace bs {
+
+// Element traits.  Pads fill cells outside the n x n block; they never change
+// a real cell: an upper pad plus anything stays >= every real upper bound, and
+// a lower pad minus anything stays <= every real lower bound (>= 0).
+template <class T> struct El;
+
+template <> struct El<float> {
+    using V2 = float2;
+    using V4 = float4;
+    static __device__ __forceinline__ float upad() { return __int_as_float(0x7f800000); }   // +inf
+    static __device__ __forceinline__ float lpad() { return __int_as_float(0xff800000); }   // -inf
+    static __device__ __forceinline__ float add(float a, float b) { return __fadd_rn(a, b); }
+    static __device__ __forceinline__ float sub(float a, float b) { return __fsub_rn(a, b); }
+    static __device__ __forceinline__ float mn(float a, float b) { return fminf(a, b); }
+    static __device__ __forceinline__ float mx(float a, float b) { return fmaxf(a, b); }
+};
+
+// int32 in 1/1024 A.  Real values lie in [0, 2^30): pad + real < 2^31 and
+// lower pad - real >= -2^31, so no expression below overflows.
+template <> struct El<int> {
+    using V2 = int2;
+    using V4 = int4;
+    static __device__ __forceinline__ int upad() { return (1 << 30) - 1; }
+    static __device__ __forceinline__ int lpad() { return -(1 << 30); }
+    static __device__ __forceinline__ int add(int a, int b) { return a + b; }
+    static __device__ __forceinline__ int sub(int a, int b) { return a - b; }
+    static __device__ __forceinline__ int mn(int a, int b) { return min(a, b); }
+    static __device__ __forceinline__ int mx(int a, int b) { return max(a, b); }
+};
+
+// Micro-tile coordinates of this thread inside a FB x FB tile.
+__device__ __forceinline__ int mt_row0() { return (threadIdx.x >> 4) * TM; }
+__device__ __forceinline__ int mt_cq() { return (threadIdx.x & 15) * 4; }
+__device__ __forceinline__ int mt_col(int c) { return (c >> 2) * 64 + mt_cq() + (c & 3); }
+
+// Load the thread's 8 x 8 cells of the tile at `M` (tile origin; mr x mc cells
+// valid).  Cells outside get `pad`.
+template <class T>
+__device__ __forceinline__ void load_tile(T (&x)[TM][TN], const T* M, size_t ld, int mr,
+                                          int mc, bool vec, T pad) {
+    using V4 = typename El<T>::V4;
+    const int r0 = mt_row0(), cq = mt_cq();
+#pragma unroll
+    for (int r = 0; r < TM; ++r) {
+        const int i = r0 + r;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = h * 64 + cq;
+            if (vec && i < mr && j + 4 <= mc) {
+                const V4 v = *reinterpret_cast<const V4*>(M + (size_t)i * ld + j);
+                x[r][h * 4 + 0] = v.x;
+                x[r][h * 4 + 1] = v.y;
+                x[r][h * 4 + 2] = v.z;
+                x[r][h * 4 + 3] = v.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    x[r][h * 4 + q] = (i < mr && j + q < mc) ? M[(size_t)i * ld + j + q] : pad;
+            }
+        }
+    }
+}
+
+// Store the thread's cells that lie inside the mr x mc block.
+template <class T>
+__device__ __forceinline__ void store_tile(const T (&x)[TM][TN], T* M, size_t ld, int mr,
+                                           int mc, bool vec) {
+    using V4 = typename El<T>::V4;
+    const int r0 = mt_row0(), cq = mt_cq();
+#pragma unroll
+    for (int r = 0; r < TM; ++r) {
+        const int i = r0 + r;
+        if (i >= mr) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = h * 64 + cq;
+            if (vec && j + 4 <= mc) {
+                V4 v;
+                v.x = x[r][h * 4 + 0];
+                v.y = x[r][h * 4 + 1];
+                v.z = x[r][h * 4 + 2];
+                v.w = x[r][h * 4 + 3];
+                *reinterpret_cast<V4*>(M + (size_t)i * ld + j) = v;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j + q < mc) M[(size_t)i * ld + j + q] = x[r][h * 4 + q];
+            }
+        }
+    }
+}
+
+// One middle atom k applied to the thread's cells.  a/al: U[i,k] and the
+// lower-bound column value for the thread's rows; b/bl: U[k,j] and L[k,j] for
+// its columns.  Upper bound first, then the lower bound from the same
+// (round-invariant) upper values:
+//   U[i,j] = min(U[i,j], U[i,k] + U[k,j])
+//   L[i,j] = max(L[i,j], L[k,j] - U[i,k], Lcol[i] - U[k,j])
+template <class T, bool HAS_L>
+__device__ __forceinline__ void fw_update(T (&u)[TM][TN], T (&l)[TM][TN], const T (&a)[TM],
+                                          const T (&al)[TM], const T (&b)[TN],
+                                          const T (&bl)[TN]) {
+#pragma unroll
+    for (int r = 0; r < TM; ++r)
+#pragma unroll
+        for (int c = 0; c < TN; ++c) u[r][c] = El<T>::mn(u[r][c], El<T>::add(a[r], b[c]));
+    if (HAS_L) {
+#pragma unroll
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+            for (int c = 0; c < TN; ++c)
+                l[r][c] = El<T>::mx(l[r][c], El<T>::mx(El<T>::sub(bl[c], a[r]),
+                                                       El<T>::sub(al[r], b[c])));
+    }
+}
+
+// Row k of the tile (U and L) into shared vectors, by the threads that own it.
+template <class T, bool HAS_L>
+__device__ __forceinline__ void publish_row(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
+                                            T* dU, T* dL) {
+    const int r0 = mt_row0();
+#pragma unroll
+    for (int r = 0; r < TM; ++r) {
+        if (r0 + r == k) {
+#pragma unroll
+            for (int c = 0; c < TN; ++c) {
+                dU[mt_col(c)] = u[r][c];
+                if (HAS_L) dL[mt_col(c)] = l[r][c];
+            }
+        }
+    }
+}
+
+// Column k of the tile (U and L) into shared vectors, by the threads that own it.
+template <class T, bool HAS_L>
+__device__ __forceinline__ void publish_col(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
+                                            T* dU, T* dL) {
+    const int r0 = mt_row0();
+#pragma unroll
+    for (int c = 0; c < TN; ++c) {
+        if (mt_col(c) == k) {
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                dU[r0 + r] = u[r][c];
+                if (HAS_L) dL[r0 + r] = l[r][c];
+            }
+        }
+    }
+}
+
+}  // namespace bs

@@ -1,0 +1,119 @@
+// Infeasibility count (cells with L > U) and the optional precondition check.
+// One pass over both matrices: HBM-bound, 8 bytes read per fp32 cell.
+#include "bs_tile.cuh"
+
+namespace bs {
+
+template <class T>
+__global__ void __launch_bounds__(256)
+k_feasible(const T* __restrict__ U, const T* __restrict__ L, int n, int ld, long long bstride,
+           unsigned char* __restrict__ mask, unsigned long long* __restrict__ count) {
+    const size_t off = (size_t)blockIdx.z * (size_t)bstride;
+    U += off;
+    L += off;
+    if (mask) mask += off;
+    unsigned int c = 0;
+    for (int i = blockIdx.y; i < n; i += gridDim.y) {
+        const T* Ui = U + (size_t)i * ld;
+        const T* Li = L + (size_t)i * ld;
+        for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
+            const bool bad = Li[j] > Ui[j];
+            c += bad;
+            if (mask) mask[(size_t)i * ld + j] = bad ? 1 : 0;
+        }
+    }
+    c = __reduce_add_sync(0xffffffffu, c);
+    __shared__ unsigned int part[8];
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long s = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += part[w];
+        if (s) atomicAdd(count, s);
+    }
+}
+
+__device__ __forceinline__ unsigned int check_value(float v, bool lower, bool diag) {
+    unsigned int f = 0;
+    if (v != v) f |= VF_NAN;
+    if (v < 0.0f) f |= VF_NEG;
+    if (lower && (v == __int_as_float(0x7f800000) || v == __int_as_float(0xff800000))) f |= VF_LINF;
+    if (diag && v != 0.0f) f |= VF_DIAG;
+    return f;
+}
+
+__device__ __forceinline__ unsigned int check_value(int v, bool, bool diag) {
+    unsigned int f = 0;
+    if (v < 0) f |= VF_NEG;
+    if (v >= (1 << 30)) f |= VF_RANGE;
+    if (diag && v != 0) f |= VF_DIAG;
+    return f;
+}
+
+template <class T>
+__global__ void __launch_bounds__(256)
+k_validate(const T* __restrict__ U, const T* __restrict__ L, int n, int ld, long long bstride,
+           unsigned int* __restrict__ flags) {
+    const size_t off = (size_t)blockIdx.z * (size_t)bstride;
+    U += off;
+    if (L) L += off;
+    unsigned int f = 0;
+    for (int i = blockIdx.y; i < n; i += gridDim.y) {
+        for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
+            f |= check_value(U[(size_t)i * ld + j], false, i == j);
+            if (L) f |= check_value(L[(size_t)i * ld + j], true, i == j);
+        }
+    }
+    f = __reduce_or_sync(0xffffffffu, f);
+    if ((threadIdx.x & 31) == 0 && f) atomicOr(flags, f);
+}
+
+static dim3 pass_grid(int n, int nbz) {
+    const int gx = (n + 255) / 256 < 8 ? (n + 255) / 256 : 8;
+    const int gy = n < 4096 ? n : 4096;
+    return dim3(gx > 0 ? gx : 1, gy > 0 ? gy : 1, nbz);
+}
+
+template <class T>
+static cudaError_t feasible_t(const Mats& m, unsigned char* mask, unsigned long long* count,
+                              cudaStream_t s) {
+    for (int b0 = 0; b0 < m.batch; b0 += 65535) {
+        const int nbz = m.batch - b0 < 65535 ? m.batch - b0 : 65535;
+        const size_t o = (size_t)b0 * m.bstride;
+        before_launch(s, PH_ROUND);
+        k_feasible<T><<<pass_grid(m.n, nbz), 256, 0, s>>>(
+            static_cast<const T*>(m.U) + o, static_cast<const T*>(m.L) + o, m.n, m.ld,
+            m.bstride, mask ? mask + o : nullptr, count);
+        after_launch(s, PH_ROUND);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <class T>
+static cudaError_t validate_t(const Mats& m, unsigned int* flags, cudaStream_t s) {
+    for (int b0 = 0; b0 < m.batch; b0 += 65535) {
+        const int nbz = m.batch - b0 < 65535 ? m.batch - b0 : 65535;
+        const size_t o = (size_t)b0 * m.bstride;
+        before_launch(s, PH_ROUND);
+        k_validate<T><<<pass_grid(m.n, nbz), 256, 0, s>>>(
+            static_cast<const T*>(m.U) + o, m.L ? static_cast<const T*>(m.L) + o : nullptr,
+            m.n, m.ld, m.bstride, flags);
+        after_launch(s, PH_ROUND);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_feasible(bool is_int, const Mats& m, unsigned char* mask,
+                            unsigned long long* count, cudaStream_t s) {
+    return is_int ? feasible_t<int>(m, mask, count, s) : feasible_t<float>(m, mask, count, s);
+}
+
+cudaError_t launch_validate(bool is_int, const Mats& m, unsigned int* flags, cudaStream_t s) {
+    return is_int ? validate_t<int>(m, flags, s) : validate_t<float>(m, flags, s);
+}
+
+}  // namespace bs

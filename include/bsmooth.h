@@ -1,0 +1,135 @@
+/*
+ * bsmooth.h -- distance-bound smoothing on one GPU (sm_103a), C ABI.
+ *
+ * The operation (GPU Gems 2, ch. 43, "GPU Computing for Protein Structure
+ * Prediction"):
+ *   section 1 -- a molecule of n atoms is the complete graph K_n; pair (i, j)
+ *     carries an upper bound U[i,j] and a lower bound L[i,j], stored as two
+ *     dense n x n matrices with a zero diagonal;
+ *   section 2 -- through every middle atom k the triangle inequality tightens
+ *       U[i,j] <- min(U[i,j], U[i,k] + U[k,j])
+ *       L[i,j] <- max(L[i,j], L[i,k] - U[k,j], L[k,j] - U[i,k])
+ *     with the upper bound tightened before the lower bound uses it;
+ *   section 3 -- Floyd-Warshall: k = 0..n-1 in order, all pairs updated in
+ *     each round, each round seeing the matrix the previous round produced.
+ *
+ * Results.  Every smoothing call leaves U and L at the fixed point of those
+ * inequalities: U[i,j] is the shortest path i..j over upper-bound edges, and
+ *   L[i,j] = max(L0[i,j], max_{a,b} L0[a,b] - U[i,a] - U[b,j]).
+ * Where L[k,k] > 0 (only for contradictory bounds) the lower-bound column
+ * value of round k is first raised to max(L[i,k], L[k,k] - U[i,k]) (the
+ * "closure" rule); with consistent bounds L[k,k] stays 0 and this is the
+ * printed rule exactly.  BS_RULE_LITERAL keeps the printed formula as is, and
+ * is accepted by the per-round mode only.
+ *
+ * Data layout.  U and L are row-major n x n matrices with leading dimension
+ * ld >= n (in elements), device memory, updated in place.  Element (i, j) is
+ * at ptr[i*ld + j].  Each matrix must span (n-1)*ld + n elements; columns
+ * n..ld-1 are never read or written.  Element type: fp32 in Angstrom
+ * (BS_FP32) or int32 in units of 1/1024 Angstrom (BS_INT32_Q10).  Inputs need
+ * not be symmetric; symmetric inputs give symmetric outputs.
+ *
+ * Preconditions (not checked unless BS_VALIDATE is set):
+ *   diagonal of U and L is 0; U >= 0 and L >= 0; no NaN; fp32 U may be +inf,
+ *   fp32 L is finite; int32 values lie in [0, 2^30) so U+U cannot overflow.
+ *
+ * Streams and devices.  Work is enqueued on `stream` (NULL = the legacy
+ * default stream) of the calling thread's current device, which must hold
+ * the matrices.  Smoothing calls return before the GPU finishes.
+ * bs_check_feasible synchronises `stream` before it returns.
+ *
+ * Memory.  The caller owns U, L and the mask.  Smoothing allocates nothing.
+ * bs_check_feasible and BS_VALIDATE use one small internal device buffer per
+ * device, allocated on first use and kept until exit.
+ *
+ * Errors.  Argument errors return before anything is enqueued.  BS_ERR_CUDA
+ * reports a failed launch or CUDA call (cudaGetLastError after the launches).
+ * No call aborts the process.
+ */
+#ifndef BSMOOTH_H
+#define BSMOOTH_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; C callers need no CUDA header. */
+typedef struct CUstream_st *bs_stream_t;
+
+typedef enum {
+    BS_OK = 0,
+    BS_ERR_ARG = 1,      /* bad n, ld, batch, stride, null pointer, mode bits */
+    BS_ERR_ALIGN = 2,    /* a matrix pointer is not aligned to its element size */
+    BS_ERR_RANGE = 3,    /* BS_VALIDATE: an int32 value outside [0, 2^30) */
+    BS_ERR_CUDA = 4,     /* a CUDA launch or call failed */
+    BS_ERR_TIMEOUT = 5,  /* reserved: a bounded device wait ran out */
+    BS_ERR_INPUT = 6     /* BS_VALIDATE: nonzero diagonal, negative value, NaN,
+                            or an infinite lower bound */
+} bs_status;
+
+/* mode bits */
+enum {
+    BS_FP32 = 0,              /* element type: float, Angstrom */
+    BS_INT32_Q10 = 1,         /* element type: int32, 1/1024 Angstrom */
+    BS_DTYPE_MASK = 3,
+    BS_BLOCKED = 0,           /* three-phase blocked Floyd-Warshall (default) */
+    BS_PERK = 1 << 2,         /* one round per middle atom k, round-synchronous */
+    BS_RULE_CLOSURE = 0,      /* default lower-bound rule (see above) */
+    BS_RULE_LITERAL = 1 << 3, /* printed rule; BS_PERK only, else BS_ERR_ARG */
+    BS_VALIDATE = 1 << 4      /* check the preconditions first (synchronises) */
+};
+
+/* Upper bounds only (min-plus all-pairs shortest paths, section 3's loop).
+ * U: device, n x n, leading dimension ld.  Rule bits are ignored. */
+bs_status bs_smooth_upper(void *U, int n, int ld, bs_stream_t stream, int mode);
+
+/* Upper and lower bounds together (sections 2 and 3).
+ * U, L: device, n x n each, same leading dimension ld, distinct buffers. */
+bs_status bs_smooth_bounds(void *U, void *L, int n, int ld, bs_stream_t stream,
+                           int mode);
+
+/* `batch` independent molecules of n atoms each; molecule b starts at
+ * U + b*batch_stride and L + b*batch_stride (elements).  batch_stride >=
+ * (n-1)*ld + n.  The number of kernel launches does not depend on batch. */
+bs_status bs_smooth_bounds_batched(void *U, void *L, int n, int ld,
+                                   long long batch_stride, int batch,
+                                   bs_stream_t stream, int mode);
+
+/* Infeasibility flags: counts the cells (i, j) of the n x n block, diagonal
+ * included, with L[i,j] > U[i,j] strictly, and stores the count in
+ * *out_count (host memory).  If mask != NULL (device, same layout and ld as
+ * U, one byte per cell), mask[i*ld+j] is set to 1 for a flagged cell and 0
+ * otherwise; its columns n..ld-1 are untouched.  Only the dtype bits of
+ * `mode` are used.  Synchronises `stream`. */
+bs_status bs_check_feasible(const void *U, const void *L, int n, int ld,
+                            bs_stream_t stream, int mode, long long *out_count,
+                            unsigned char *mask);
+
+/* Static text for a status code. */
+const char *bs_strerror(bs_status status);
+
+/* ---- instrumentation (not part of the method) ---------------------------- */
+
+/* Number of kernels this library has launched since it was loaded. */
+long long bs_launch_count(void);
+
+/* Per-phase device time.  After bs_profile_begin(), every smoothing call
+ * records a CUDA event pair around each of its kernel launches on the
+ * caller's stream.  bs_profile_end() waits for those events, writes the summed
+ * milliseconds and launch counts per phase (index: 0 per-round kernels,
+ * 1 phase 1, 2 phase 2, 3 phase 3) and stops recording.  At most 1<<16 launches
+ * are recorded per session; more set *overflow to 1. */
+typedef struct {
+    double ms[4];
+    long long launches[4];
+    int overflow;
+} bs_profile;
+
+bs_status bs_profile_begin(void);
+bs_status bs_profile_end(bs_profile *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSMOOTH_H */

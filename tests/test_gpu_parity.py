@@ -1,0 +1,315 @@
+"""GPU parity: the CUDA path against the CPU oracle, through the C ABI.
+
+Bit-exact in int32 (1/1024 A) and in the per-round mode; fp32 blocked results
+on the 1/1024 grid are bit-exact too (every sum that can win is exact below
+2^14 A), which is stricter than the stated fp32 gate of 1e-5 relative /
+1e-4 A absolute.  That gate is exercised on off-grid inputs in
+test_fp32_off_grid_within_tolerance.
+"""
+import numpy as np
+import pytest
+
+import blocked_floyd_warshall_gb300 as bsm
+import oracle
+from workloads import molecules as W
+
+from gpu_util import dev, gpu_bounds, gpu_upper, host, same_bits, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    t = torch()
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bsm.build()
+    bsm.library()
+
+
+def as_dtype(Uq, Lq, dtype):
+    if dtype == "f32":
+        return W.to_f32(Uq), W.to_f32(Lq)
+    return Uq, Lq
+
+
+SIZES_PERK = [1, 2, 3, 4, 5, 7, 31, 33, 64, 255, 256]
+SIZES_BLOCKED = [1, 2, 3, 5, 31, 64, 127, 128, 129, 255, 256, 257, 300, 383, 385, 513]
+
+
+@pytest.mark.parametrize("n", SIZES_PERK)
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+@pytest.mark.parametrize("rule", ["closure", "literal"])
+def test_per_round_matches_oracle(n, dtype, rule):
+    Uq, Lq = W.random_bounds(n, 1000 + n, p_known=0.3, p_bad=0.03)
+    U0, L0 = as_dtype(Uq, Lq, dtype)
+    flags = bsm.BS_PERK | (bsm.BS_RULE_LITERAL if rule == "literal" else 0)
+    r = oracle.RULE_LITERAL if rule == "literal" else oracle.RULE_CLOSURE
+    Uo, Lo = oracle.smooth(U0, L0, rule=r)
+    Ug, Lg, ok = gpu_bounds(U0, L0, flags)
+    assert ok
+    assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
+@pytest.mark.parametrize("n", SIZES_BLOCKED)
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_blocked_matches_oracle(n, dtype):
+    Uq, Lq = W.random_bounds(n, 2000 + n, p_known=0.2, p_bad=0.02)
+    U0, L0 = as_dtype(Uq, Lq, dtype)
+    Uo, Lo = oracle.smooth(U0, L0)
+    Ug, Lg, ok = gpu_bounds(U0, L0)
+    assert ok
+    assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
+@pytest.mark.parametrize("n", [129, 300])
+def test_blocked_asymmetric(n):
+    Uq, Lq = W.random_bounds(n, 3000 + n, p_known=0.3, p_bad=0.02, symmetric=False)
+    Uo, Lo = oracle.smooth(Uq, Lq)
+    Ug, Lg, ok = gpu_bounds(Uq, Lq)
+    assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
+@pytest.mark.parametrize("n,ld,offset", [(130, 140, 0), (130, 133, 0), (257, 260, 1),
+                                         (97, 101, 3), (200, 200, 1)])
+@pytest.mark.parametrize("algo", ["blocked", "perk"])
+def test_leading_dimension_and_misalignment(n, ld, offset, algo):
+    """ld > n keeps the padding untouched; ld % 4 != 0 or a base not 16-byte
+    aligned takes the scalar-IO instantiation with identical results."""
+    Uq, Lq = W.random_bounds(n, 4000 + n, p_bad=0.02)
+    U0, L0 = W.to_f32(Uq), W.to_f32(Lq)
+    flags = bsm.BS_PERK if algo == "perk" else 0
+    Uo, Lo = oracle.smooth(U0, L0)
+    Ug, Lg, ok = gpu_bounds(U0, L0, flags, ld=ld, offset=offset)
+    assert ok
+    assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
+@pytest.mark.parametrize("n", [1, 5, 128, 129, 300])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+@pytest.mark.parametrize("algo", ["blocked", "perk"])
+def test_upper_only(n, dtype, algo):
+    Uq, _ = W.random_bounds(n, 5000 + n, p_known=0.25)
+    U0 = W.to_f32(Uq) if dtype == "f32" else Uq
+    Uo = oracle.smooth_upper(U0)
+    Ug, ok = gpu_upper(U0, bsm.BS_PERK if algo == "perk" else 0, ld=n + 3)
+    assert ok and same_bits(Ug, Uo)
+
+
+@pytest.mark.parametrize("n", [1, 64, 131])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_feasibility_count_and_mask(n, dtype):
+    Uq, Lq = W.random_bounds(n, 6000 + n, p_known=0.4, p_bad=0.05)
+    U0, L0 = as_dtype(Uq, Lq, dtype)
+    Uo, Lo = oracle.smooth(U0, L0)
+    ld = n + 4
+    t = torch()
+    U = dev(np.pad(Uo, ((0, 0), (0, 4))))
+    L = dev(np.pad(Lo, ((0, 0), (0, 4))))
+    mask = t.full((n, ld), 7, dtype=t.uint8, device="cuda")
+    cnt = bsm.bs_check_feasible(U, L, n, ld, None, None, mask)
+    assert cnt == oracle.count_infeasible(Uo, Lo)
+    m = host(mask)
+    assert np.array_equal(m[:, :n].astype(bool), Lo > Uo)
+    assert np.all(m[:, n:] == 7)
+
+
+def test_feasibility_count_example_c():
+    """The worked example with 16 flags (closure) and 15 (printed rule, per round)."""
+    U0 = np.full((4, 4), 100.0, np.float32)
+    L0 = np.full((4, 4), 1.0, np.float32)
+    np.fill_diagonal(U0, 0)
+    np.fill_diagonal(L0, 0)
+    for i, j, lo, hi in [(0, 1, 3, 4), (1, 2, 3, 4), (0, 2, 9, 10), (2, 3, 0.125, 0.25)]:
+        U0[i, j] = U0[j, i] = hi
+        L0[i, j] = L0[j, i] = lo
+    for flags, expect in [(0, 16), (bsm.BS_PERK, 16), (bsm.BS_PERK | bsm.BS_RULE_LITERAL, 15)]:
+        U, L = dev(U0), dev(L0)
+        bsm.bs_smooth_bounds(U, L, flags=flags)
+        assert bsm.bs_check_feasible(U, L) == expect
+
+
+def test_fp32_off_grid_within_tolerance():
+    """Values off the 1/1024 grid: fp32 blocked vs the fp64 oracle within
+    1e-4 A absolute or 1e-5 relative, per cell."""
+    rng = np.random.default_rng(7)
+    n = 300
+    Uq, Lq = W.random_bounds(n, 7000, p_known=0.3, p_bad=0.0)
+    U0 = (Uq / 1024.0 + rng.random((n, n)) * 1e-3).astype(np.float32)
+    L0 = np.maximum(Lq / 1024.0 - rng.random((n, n)) * 1e-3, 0).astype(np.float32)
+    U0 = np.minimum(U0, U0.T)
+    L0 = np.minimum(L0, L0.T)
+    np.fill_diagonal(U0, 0)
+    np.fill_diagonal(L0, 0)
+    Uo, Lo = oracle.smooth(U0.astype(np.float64), L0.astype(np.float64))
+    Ug, Lg, ok = gpu_bounds(U0, L0)
+    for g, o in ((Ug, Uo), (Lg, Lo)):
+        err = np.abs(g.astype(np.float64) - o)
+        assert np.all((err <= 1e-4) | (err <= 1e-5 * np.abs(o)))
+
+
+# ------------------------------------------------------------------ benchmark molecules
+
+
+@pytest.mark.parametrize("idx", [0, 1])
+@pytest.mark.parametrize("algo", ["blocked", "perk"])
+def test_chain_configs(idx, algo):
+    m = W.make_config(idx)
+    flags = bsm.BS_PERK if algo == "perk" else 0
+    for U0, L0 in ((W.to_f32(m["U"]), W.to_f32(m["L"])), (m["U"], m["L"])):
+        Uo, Lo = oracle.smooth(U0, L0)
+        Ug, Lg, ok = gpu_bounds(U0, L0, flags)
+        assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
+        assert oracle.count_infeasible(Uo, Lo) == 0
+
+
+@pytest.fixture(scope="module")
+def globule4096():
+    m = W.make_config(2)
+    Uo, Lo = oracle.smooth(m["U"], m["L"])          # int32, all 4096 rounds
+    return m, Uo, Lo
+
+
+def test_globule_4096_int32_blocked(globule4096):
+    m, Uo, Lo = globule4096
+    Ug, Lg, ok = gpu_bounds(m["U"], m["L"])
+    assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
+    U, L = dev(Ug), dev(Lg)
+    assert bsm.bs_check_feasible(U, L) == oracle.count_infeasible(Uo, Lo) > 0
+
+
+def test_globule_4096_fp32_blocked_and_per_round(globule4096):
+    m, Uo, Lo = globule4096
+    U0, L0 = W.to_f32(m["U"]), W.to_f32(m["L"])
+    expect_flags = oracle.count_infeasible(Uo, Lo)
+    for flags in (0, bsm.BS_PERK):
+        Ug, Lg, ok = gpu_bounds(U0, L0, flags)
+        assert ok
+        # fp32 on the grid equals int32 / 1024 exactly
+        assert np.array_equal(Ug * 1024, Uo.astype(np.float32))
+        assert np.array_equal(Lg * 1024, Lo.astype(np.float32))
+        assert bsm.bs_check_feasible(dev(Ug), dev(Lg)) == expect_flags
+
+
+def test_batched_chains():
+    """Batch of 256 molecules n=512 in one call; every 32nd molecule against the
+    oracle, all molecules against a per-molecule GPU call."""
+    m = W.make_config(3)
+    B, n = m["batch"], m["n"]
+    U0, L0 = W.to_f32(m["U"]), W.to_f32(m["L"])
+    U, L = dev(U0), dev(L0)
+    bsm.bs_smooth_bounds_batched(U, L)
+    Ug, Lg = host(U), host(L)
+    for b in range(0, B, 32):
+        Uo, Lo = oracle.smooth(U0[b], L0[b])
+        assert same_bits(Ug[b], Uo) and same_bits(Lg[b], Lo)
+    for b in range(B):
+        Us, Ls, _ = gpu_bounds(U0[b], L0[b])
+        assert same_bits(Ug[b], Us) and same_bits(Lg[b], Ls)
+    del n
+
+
+def test_batched_per_round_and_strided():
+    """Per-round mode and a batch stride larger than one molecule."""
+    B, n, ld = 5, 70, 72
+    stride = n * ld + 16
+    t = torch()
+    Us = [W.random_bounds(n, 8000 + b, p_bad=0.02) for b in range(B)]
+    Ubuf = t.full((B * stride,), -1.0, dtype=t.float32, device="cuda")
+    Lbuf = t.full((B * stride,), -1.0, dtype=t.float32, device="cuda")
+    for b, (uq, lq) in enumerate(Us):
+        Ubuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(uq))
+        Lbuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(lq))
+    for flags in (bsm.BS_PERK, 0):
+        U, L = Ubuf.clone(), Lbuf.clone()
+        bsm.bs_smooth_bounds_batched(U, L, n, ld, stride, B, None, bsm.BS_FP32 | flags)
+        Uh, Lh = host(U), host(L)
+        for b, (uq, lq) in enumerate(Us):
+            Uo, Lo = oracle.smooth(W.to_f32(uq), W.to_f32(lq))
+            blk = slice(b * stride, b * stride + n * ld)
+            assert same_bits(Uh[blk].reshape(n, ld)[:, :n], Uo)
+            assert same_bits(Lh[blk].reshape(n, ld)[:, :n], Lo)
+            assert np.all(Uh[blk].reshape(n, ld)[:, n:] == -1.0)
+            assert np.all(Uh[b * stride + n * ld: (b + 1) * stride] == -1.0)
+
+
+def test_globule_16384_sampled_rows():
+    """n = 16384, fp32, blocked, as timed by the benchmark: sampled rows
+    against the oracle's shortest-path rows, plus properties of every cell."""
+    m = W.make_config(4)
+    n = m["n"]
+    t = torch()
+    U, L = dev(W.to_f32(m["U"])), dev(W.to_f32(m["L"]))
+    bsm.bs_smooth_bounds(U, L)
+    t.cuda.synchronize()
+    rows = np.array([0, 1, 4097, 8191, 12000, n - 1])
+    Ur, Lr = oracle.closure_rows(m["U"], m["L"], rows)
+    Ug = U[t.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64) * 1024
+    Lg = L[t.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64) * 1024
+    assert np.array_equal(Ug, Ur) and np.array_equal(Lg, Lr)
+    # every cell: symmetric, consistent (no flags), diagonal zero
+    assert bool((U == U.T).all()) and bool((L == L.T).all())
+    assert bsm.bs_check_feasible(U, L) == 0
+    assert bool((t.diagonal(U) == 0).all()) and bool((t.diagonal(L) == 0).all())
+    # the generating coordinates lie inside every smoothed bound (sampled rows)
+    x = m["coords"]
+    d = np.sqrt(((x[rows][:, None] - x[None]) ** 2).sum(-1)) * 1024
+    assert np.all(Lg <= d + 1e-6) and np.all(d <= Ug + 1e-6)
+
+
+# ------------------------------------------------------------------ checks and errors
+
+
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_validate_flag(dtype):
+    Uq, Lq = W.random_bounds(40, 9000, p_bad=0.02)
+    U0, L0 = as_dtype(Uq, Lq, dtype)
+    U, L = dev(U0), dev(L0)
+    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_VALIDATE)        # valid input passes
+    bad_diag = U0.copy()
+    bad_diag[3, 3] = 1
+    bad_neg = L0.copy()
+    bad_neg[2, 5] = -1
+    cases = [(bad_diag, L0, bsm.BS_ERR_INPUT), (U0, bad_neg, bsm.BS_ERR_INPUT)]
+    if dtype == "f32":
+        bad_nan = L0.copy()
+        bad_nan[1, 2] = np.nan
+        bad_inf = L0.copy()
+        bad_inf[1, 2] = np.inf
+        cases += [(U0, bad_nan, bsm.BS_ERR_INPUT), (U0, bad_inf, bsm.BS_ERR_INPUT)]
+    else:
+        big = U0.copy()
+        big[0, 1] = 1 << 30
+        cases += [(big, L0, bsm.BS_ERR_RANGE)]
+    for u, l, code in cases:
+        with pytest.raises(bsm.BSError) as e:
+            bsm.bs_smooth_bounds(dev(u), dev(l), flags=bsm.BS_VALIDATE)
+        assert e.value.status == code
+
+
+def test_literal_rule_rejected_in_blocked_mode():
+    U, L = dev(np.zeros((4, 4), np.float32)), dev(np.zeros((4, 4), np.float32))
+    with pytest.raises(bsm.BSError) as e:
+        bsm.bs_smooth_bounds(U, L, flags=bsm.BS_RULE_LITERAL)
+    assert e.value.status == bsm.BS_ERR_ARG
+
+
+def test_empty_and_launch_counting():
+    t = torch()
+    U = t.zeros((0, 0), dtype=t.float32, device="cuda")
+    before = bsm.bs_launch_count()
+    bsm.bs_smooth_bounds(U, U.clone())
+    assert bsm.bs_launch_count() == before
+    Uq, Lq = W.random_bounds(300, 1, p_bad=0.01)
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)))
+    assert bsm.bs_launch_count() - before == 3 * 3        # three phases x three block rounds
+
+
+def test_profile_records_every_launch():
+    Uq, Lq = W.random_bounds(300, 2, p_bad=0.01)
+    U, L = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
+    bsm.bs_profile_begin()
+    bsm.bs_smooth_bounds(U, L)
+    p = bsm.bs_profile_end()
+    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 3]
+    assert p["phase3"]["ms"] > 0
