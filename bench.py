@@ -34,7 +34,19 @@ FP32_LANES_PER_SM = 128
 WORKLOADS = {
     "globule16384": dict(config=4, desc="lattice globule n=16384, fp32 U+L, blocked"),
     "globule4096": dict(config=2, desc="lattice globule n=4096, fp32 U+L, blocked"),
+    # profiling size: inputs 4x larger than L2, a few GB on the device
+    "globule8192": dict(box=(32, 16, 16), seed=1005, p_long=0.005,
+                        desc="lattice globule n=8192 (profiling size), fp32 U+L, blocked"),
 }
+
+
+def make_workload(name):
+    from workloads import make_config
+    from workloads.molecules import globule_bounds
+    wl = WORKLOADS[name]
+    if "config" in wl:
+        return make_config(wl["config"])
+    return globule_bounds(wl["box"], wl["seed"], wl["p_long"])
 
 
 def load_peaks():
@@ -183,9 +195,9 @@ def oracle_rate(U0, L0, seconds, max_rounds=None):
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
-    from workloads import make_config, to_f32
+    from workloads import to_f32
     wl = WORKLOADS[args.workload]
-    m = make_config(wl["config"])
+    m = make_workload(args.workload)
     U0, L0 = to_f32(m["U"]), to_f32(m["L"])
     n = m["n"]
     times, rates = [], []
@@ -224,6 +236,8 @@ def main():
                     help="oracle rounds per step for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-probe", action="store_true",
+                    help="skip the ALU issue-rate probes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -234,7 +248,7 @@ def main():
 
     import torch
     import blocked_floyd_warshall_gb300 as bsm
-    from workloads import make_config, to_f32
+    from workloads import to_f32
 
     torch.cuda.set_device(local)
     if ws > 1:
@@ -244,7 +258,7 @@ def main():
     bsm.library()
 
     wl = WORKLOADS[args.workload]
-    m = make_config(wl["config"])
+    m = make_workload(args.workload)
     n = m["n"]
     U0, L0 = to_f32(m["U"]), to_f32(m["L"])
     dU0 = torch.from_numpy(U0).cuda()
@@ -341,6 +355,9 @@ def main():
         "clocks": clocks,
     }
 
+    if not args.no_probe:
+        line["alu_probe_instr_per_clk_per_sm"] = {
+            name: round(bsm.bs_probe_alu(name), 2) for name in bsm.PROBES}
     if not args.no_e2e:
         line["e2e"] = e2e_leg(torch, bsm, U0, L0, args, ws)
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:

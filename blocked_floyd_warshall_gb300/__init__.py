@@ -45,6 +45,9 @@ BS_VALIDATE = 1 << 4
 
 PHASES = ("round", "phase1", "phase2", "phase3")
 
+PROBES = {"fadd": 0, "fmnmx": 1, "fmnmx3": 2, "fadd2": 3, "fadd2+fmnmx3": 4,
+          "iadd": 5, "imnmx": 6, "viaddmin": 7, "vimnmx3": 8}
+
 
 class BSError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -89,6 +92,8 @@ def library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = args
             f.restype = i
+        lib.bs_probe_alu.argtypes = [i, i, ctypes.POINTER(ctypes.c_double)]
+        lib.bs_probe_alu.restype = i
         lib.bs_strerror.argtypes = [i]
         lib.bs_strerror.restype = ctypes.c_char_p
         lib.bs_launch_count.argtypes = []
@@ -216,3 +221,12 @@ def bs_profile_end() -> dict:
     _check(library().bs_profile_end(ctypes.byref(p)), "bs_profile_end")
     return {name: {"ms": p.ms[i], "launches": int(p.launches[i])}
             for i, name in enumerate(PHASES)} | {"overflow": bool(p.overflow)}
+
+
+def bs_probe_alu(which, iters: int = 20000) -> float:
+    """Measured thread-instructions per clock per SM for one instruction form
+    (a BS_PROBE_* code or a PROBES name)."""
+    code = PROBES[which] if isinstance(which, str) else int(which)
+    out = ctypes.c_double(0.0)
+    _check(library().bs_probe_alu(code, int(iters), ctypes.byref(out)), "bs_probe_alu")
+    return float(out.value)

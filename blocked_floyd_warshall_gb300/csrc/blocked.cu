@@ -21,6 +21,8 @@
 // Inside phases 1 and 2 each step k is round-synchronous: every thread keeps
 // its cells in registers, row k / column k are published to a shared vector
 // double-buffered by k parity, one barrier per step.
+#include <type_traits>
+
 #include "bs_tile.cuh"
 
 namespace bs {
@@ -189,76 +191,171 @@ k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
 }
 
 // ---------------------------------------------------------------- phase 3
+//
+// Phase 3 updates tile (I,J) from the finished column panel (I,K) and row
+// panel (K,J).  Both are streamed through shared memory in chunks of BK
+// middle atoms (two stages, cp.async).  The inner loop takes the middle atoms
+// two at a time: a thread holds, per row r, the pair (U[i,k], U[i,k+1]) in one
+// 64-bit register (the column panel is stored [i][k], so the pair is one
+// 8-byte load), and per column c the pair (U[k,j], U[k+1,j]) (the row panel is
+// stored k-interleaved, [k/2][j][k%2]).  For fp32 one add.rn.f32x2 then forms
+// both candidate sums of a cell and one three-input min.f32 folds them into
+// the accumulator; the lower bound takes two sub.rn.f32x2 and two three-input
+// max.f32.  3 instructions per cell update instead of 6.  min and max are
+// exact, so the grouping of k changes no result; every sum is the same
+// round-to-nearest fp32 add.  int32 uses the add-then-min/max forms
+// (__viaddmin_s32 / __viaddmax_s32).
 
-constexpr int BK = 16;        // k-chunk staged per pipeline stage
+constexpr int BK = 16;        // middle atoms staged per pipeline stage
 constexpr int AST = BK + 4;   // column-panel row stride (elements); rows stay 16-byte aligned
 
 template <class T, bool HAS_L>
 struct P3Smem {
-    // one stage: column panel A[i][k] (FB x BK) and row panel B[k][j] (BK x FB)
+    // one stage: column panel A[i][k] (FB x AST) and row panel B[k/2][j][k%2]
     static constexpr int A_ELEMS = FB * AST;
     static constexpr int B_ELEMS = BK * FB;
     static constexpr int MATS = HAS_L ? 2 : 1;
-    static constexpr int STAGE = MATS * (A_ELEMS + B_ELEMS);
+    static constexpr int STAGE = MATS * (A_ELEMS + B_ELEMS);   // layout AU | BU | AL | BL
     static constexpr size_t BYTES = 2 * STAGE * sizeof(T);
 };
 
-// Stage k-chunk `c` of both panels into shared memory stage `st`.
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+// Stage k-chunk `c` of both panels into shared memory stage `stage`.
 template <class T, bool HAS_L>
 __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_t ld, int oi,
                                          int oj, int ok, int mi, int mj, int mk, int c,
                                          bool vec) {
     using E = El<T>;
     using S = P3Smem<T, HAS_L>;
-    // stage layout: AU | BU | AL | BL
     T* AU = stage;
     T* BU = stage + S::A_ELEMS;
     T* AL = HAS_L ? BU + S::B_ELEMS : nullptr;
     T* BL = HAS_L ? AL + S::A_ELEMS : nullptr;
     const int kc = c * BK;
-    // column panel: FB rows x BK columns = FB * BK/4 pieces of 4 elements
-    for (int p = threadIdx.x; p < FB * (BK / 4); p += NT) {
-        const int i = p / (BK / 4);
-        const int kq = (p % (BK / 4)) * 4;
-        const size_t g = (size_t)(oi + i) * ld + ok + kc + kq;
-        const bool full = i < mi && kc + kq + 4 <= mk;
-        if (vec && full) {
-            cp_async16(AU + i * AST + kq, U + g);
-            if (HAS_L) cp_async16(AL + i * AST + kq, L + g);
-        } else {
+    // column panel: FB rows x BK middle atoms, [i][k]
+    if (vec) {
+        for (int p = threadIdx.x; p < FB * (BK / 4); p += NT) {
+            const int i = p / (BK / 4);
+            const int kq = (p % (BK / 4)) * 4;
+            const size_t g = (size_t)(oi + i) * ld + ok + kc + kq;
+            if (i < mi && kc + kq + 4 <= mk) {
+                cp_async16(AU + i * AST + kq, U + g);
+                if (HAS_L) cp_async16(AL + i * AST + kq, L + g);
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const bool in = i < mi && kc + kq + q < mk;
-                AU[i * AST + kq + q] = in ? U[g + q] : E::upad();
-                if (HAS_L) AL[i * AST + kq + q] = in ? L[g + q] : E::lpad();
+                for (int q = 0; q < 4; ++q) {
+                    const bool in = i < mi && kc + kq + q < mk;
+                    AU[i * AST + kq + q] = in ? U[g + q] : E::upad();
+                    if (HAS_L) AL[i * AST + kq + q] = in ? L[g + q] : E::lpad();
+                }
+            }
+        }
+    } else {
+        for (int p = threadIdx.x; p < FB * BK; p += NT) {
+            const int i = p / BK, k = p % BK;
+            const size_t g = (size_t)(oi + i) * ld + ok + kc + k;
+            if (i < mi && kc + k < mk) {
+                cp_async4(AU + i * AST + k, U + g);
+                if (HAS_L) cp_async4(AL + i * AST + k, L + g);
+            } else {
+                AU[i * AST + k] = E::upad();
+                if (HAS_L) AL[i * AST + k] = E::lpad();
             }
         }
     }
-    // row panel: BK rows x FB columns
-    for (int p = threadIdx.x; p < BK * (FB / 4); p += NT) {
-        const int k = p / (FB / 4);
-        const int j = (p % (FB / 4)) * 4;
+    // row panel: BK middle atoms x FB columns, k-interleaved
+    for (int p = threadIdx.x; p < BK * FB; p += NT) {
+        const int k = p / FB, j = p % FB;
+        const int d = (k >> 1) * (2 * FB) + j * 2 + (k & 1);
         const size_t g = (size_t)(ok + kc + k) * ld + oj + j;
-        const bool krow = kc + k < mk;
-        if (vec && krow && j + 4 <= mj) {
-            cp_async16(BU + k * FB + j, U + g);
-            if (HAS_L) cp_async16(BL + k * FB + j, L + g);
+        if (kc + k < mk && j < mj) {
+            cp_async4(BU + d, U + g);
+            if (HAS_L) cp_async4(BL + d, L + g);
         } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const bool in = krow && j + q < mj;
-                BU[k * FB + j + q] = in ? U[g + q] : E::upad();
-                if (HAS_L) BL[k * FB + j + q] = in ? L[g + q] : E::lpad();
-            }
+            BU[d] = E::upad();
+            if (HAS_L) BL[d] = E::lpad();
         }
     }
 }
+
+// Cell updates for a pair of middle atoms (k, k+1).
+//   a, al : (U[i,k], U[i,k+1]), (L[i,k], L[i,k+1])   -- row i of the thread
+//   b, bl : (U[k,j], U[k+1,j]), (L[k,j], L[k+1,j])   -- column j of the thread
+template <class T> struct PairOps;
+
+template <> struct PairOps<float> {
+    using P = unsigned long long;   // two fp32 lanes: low = k, high = k+1
+    static __device__ __forceinline__ void upper(float& u, P a, P b) {
+        asm("{\n\t.reg .b64 s;\n\t.reg .f32 s0, s1;\n\t"
+            "add.rn.f32x2 s, %1, %2;\n\t"
+            "mov.b64 {s0, s1}, s;\n\t"
+            "min.f32 %0, %0, s0, s1;\n\t}"
+            : "+f"(u) : "l"(a), "l"(b));
+    }
+    // L = max(L, L[k,j] - U[i,k], L[i,k] - U[k,j]) over both k
+    static __device__ __forceinline__ void lower(float& l, P a, P al, P b, P bl) {
+        asm("{\n\t.reg .b64 d1, d2;\n\t.reg .f32 x0, x1, y0, y1;\n\t"
+            "sub.rn.f32x2 d1, %1, %3;\n\t"
+            "sub.rn.f32x2 d2, %2, %4;\n\t"
+            "mov.b64 {x0, x1}, d1;\n\t"
+            "mov.b64 {y0, y1}, d2;\n\t"
+            "max.f32 %0, %0, x0, x1;\n\t"
+            "max.f32 %0, %0, y0, y1;\n\t}"
+            : "+f"(l) : "l"(bl), "l"(al), "l"(a), "l"(b));
+    }
+};
+
+template <> struct PairOps<int> {
+    using P = int2;
+    static __device__ __forceinline__ void upper(int& u, P a, P b) {
+        u = __viaddmin_s32(a.x, b.x, u);
+        u = __viaddmin_s32(a.y, b.y, u);
+    }
+    // na, nb: negated a, b
+    static __device__ __forceinline__ void lower(int& l, P na, P al, P nb, P bl) {
+        l = __viaddmax_s32(bl.x, na.x, l);
+        l = __viaddmax_s32(bl.y, na.y, l);
+        l = __viaddmax_s32(al.x, nb.x, l);
+        l = __viaddmax_s32(al.y, nb.y, l);
+    }
+};
+
+template <class T> struct PairLoad;
+template <> struct PairLoad<float> {
+    using P = unsigned long long;
+    static __device__ __forceinline__ P ld2(const float* p) {
+        return *reinterpret_cast<const unsigned long long*>(p);
+    }
+    static __device__ __forceinline__ void ld4(const float* p, P& x, P& y) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
+        x = v.x;
+        y = v.y;
+    }
+    static __device__ __forceinline__ P neg(P x) { return x; }
+};
+template <> struct PairLoad<int> {
+    using P = int2;
+    static __device__ __forceinline__ P ld2(const int* p) { return *reinterpret_cast<const int2*>(p); }
+    static __device__ __forceinline__ void ld4(const int* p, P& x, P& y) {
+        const int4 v = *reinterpret_cast<const int4*>(p);
+        x = make_int2(v.x, v.y);
+        y = make_int2(v.z, v.w);
+    }
+    static __device__ __forceinline__ P neg(P x) { return make_int2(-x.x, -x.y); }
+};
 
 template <class T, bool HAS_L>
 __global__ void __launch_bounds__(NT, 1)
 k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
     using E = El<T>;
     using S = P3Smem<T, HAS_L>;
+    using LD = PairLoad<T>;
+    using P = typename LD::P;
+    constexpr bool NEG = std::is_same<T, int>::value;   // int lower bound adds negated values
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* sm = reinterpret_cast<T*>(smem_raw);
 
@@ -289,29 +386,43 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
         __syncthreads();
         const T* AU = sm + (c & 1) * S::STAGE;
         const T* BU = AU + S::A_ELEMS;
-        const T* AL = AU + S::A_ELEMS + S::B_ELEMS;
+        const T* AL = BU + S::B_ELEMS;
         const T* BL = AL + S::A_ELEMS;
-#pragma unroll 4
-        for (int kk = 0; kk < BK; ++kk) {
-            T a[TM], al[TM], bb[TN], bl[TN];
+#pragma unroll 1
+        for (int kk = 0; kk < BK; kk += 2) {
+            P a[TM], al[TM], b[TN], bl[TN];
 #pragma unroll
             for (int r = 0; r < TM; ++r) {
-                a[r] = AU[(r0 + r) * AST + kk];
-                al[r] = HAS_L ? AL[(r0 + r) * AST + kk] : T(0);
+                a[r] = LD::ld2(AU + (r0 + r) * AST + kk);
+                if (HAS_L) al[r] = LD::ld2(AL + (r0 + r) * AST + kk);
             }
+            const int bo = (kk >> 1) * (2 * FB);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const typename E::V4 v = *reinterpret_cast<const typename E::V4*>(BU + kk * FB + h * 64 + cq);
-                bb[h * 4 + 0] = v.x; bb[h * 4 + 1] = v.y; bb[h * 4 + 2] = v.z; bb[h * 4 + 3] = v.w;
+                LD::ld4(BU + bo + (h * 64 + cq) * 2, b[h * 4 + 0], b[h * 4 + 1]);
+                LD::ld4(BU + bo + (h * 64 + cq) * 2 + 4, b[h * 4 + 2], b[h * 4 + 3]);
                 if (HAS_L) {
-                    const typename E::V4 w = *reinterpret_cast<const typename E::V4*>(BL + kk * FB + h * 64 + cq);
-                    bl[h * 4 + 0] = w.x; bl[h * 4 + 1] = w.y; bl[h * 4 + 2] = w.z; bl[h * 4 + 3] = w.w;
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) bl[h * 4 + q] = T(0);
+                    LD::ld4(BL + bo + (h * 64 + cq) * 2, bl[h * 4 + 0], bl[h * 4 + 1]);
+                    LD::ld4(BL + bo + (h * 64 + cq) * 2 + 4, bl[h * 4 + 2], bl[h * 4 + 3]);
                 }
             }
-            fw_update<T, HAS_L>(u, l, a, al, bb, bl);
+#pragma unroll
+            for (int r = 0; r < TM; ++r)
+#pragma unroll
+                for (int q = 0; q < TN; ++q) PairOps<T>::upper(u[r][q], a[r], b[q]);
+            if (HAS_L) {
+                if (NEG) {
+#pragma unroll
+                    for (int r = 0; r < TM; ++r) a[r] = LD::neg(a[r]);
+#pragma unroll
+                    for (int q = 0; q < TN; ++q) b[q] = LD::neg(b[q]);
+                }
+#pragma unroll
+                for (int r = 0; r < TM; ++r)
+#pragma unroll
+                    for (int q = 0; q < TN; ++q)
+                        PairOps<T>::lower(l[r][q], a[r], al[r], b[q], bl[q]);
+            }
         }
         __syncthreads();
     }

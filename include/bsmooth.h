@@ -128,6 +128,24 @@ typedef struct {
 bs_status bs_profile_begin(void);
 bs_status bs_profile_end(bs_profile *out);
 
+/* ALU issue-rate probe.  Runs one 1024-thread CTA per SM, each thread
+ * iterating `iters` x 128 instructions of one form in 8 independent chains,
+ * and stores the measured thread-instructions retired per SM clock (SM cycle
+ * counter around the loop, mean over SMs) in *instr_per_clk_per_sm.
+ * Allocates and frees a small device buffer; synchronises the device. */
+enum {
+    BS_PROBE_FADD = 0,         /* add.rn.f32 */
+    BS_PROBE_FMNMX = 1,        /* min.f32, two inputs */
+    BS_PROBE_FMNMX3 = 2,       /* min.f32, three inputs */
+    BS_PROBE_FADD2 = 3,        /* add.rn.f32x2 (two lanes per instruction) */
+    BS_PROBE_FADD2_FMNMX3 = 4, /* the two above interleaved 1:1 */
+    BS_PROBE_IADD = 5,         /* add.s32 */
+    BS_PROBE_IMNMX = 6,        /* min.s32 */
+    BS_PROBE_VIADDMIN = 7,     /* __viaddmin_s32: min(a + b, c) */
+    BS_PROBE_VIMNMX3 = 8       /* __vimin3_s32: min(a, b, c) */
+};
+bs_status bs_probe_alu(int which, int iters, double *instr_per_clk_per_sm);
+
 #ifdef __cplusplus
 }
 #endif
