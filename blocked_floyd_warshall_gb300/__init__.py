@@ -92,6 +92,9 @@ def library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = args
             f.restype = i
+        lib.bs_check_feasible_noalloc.argtypes = [vp, vp, i, i, ll, i, vp, i,
+                                                  ctypes.POINTER(ll)]
+        lib.bs_check_feasible_noalloc.restype = i
         lib.bs_probe_alu.argtypes = [i, i, ctypes.POINTER(ctypes.c_double)]
         lib.bs_probe_alu.restype = i
         lib.bs_strerror.argtypes = [i]
@@ -201,6 +204,36 @@ def bs_check_feasible(U, L, n=None, ld=None, stream=None, mode=None, mask=None) 
                                      _dtype_bits(U, mode), ctypes.byref(out), _ptr(mask))
     _check(st, "bs_check_feasible")
     return int(out.value)
+
+
+BS_NOALLOC_MAX_BATCH = 4096
+
+
+def bs_check_feasible_noalloc(U, L, n=None, ld=None, batch_stride=None, batch=None,
+                              stream=None, mode=None) -> list:
+    """Per-molecule L > U counts without any device allocation.
+
+    For callers that cannot allocate device memory (their allocator owns it
+    all, or cudaMalloc's synchronisation is not allowed on their path): the
+    counters live in a fixed array of BS_NOALLOC_MAX_BATCH entries inside the
+    library.  U, L: (batch, n, ld) or (n, ld) tensors.  Calls that overlap on
+    the GPU share that array and race; the first call on a device should come
+    before any stream capture.
+    """
+    n, ld = _geometry(U, n, ld)
+    if _is_tensor(U):
+        if batch is None:
+            batch = U.shape[0] if U.dim() == 3 else 1
+        if batch_stride is None:
+            batch_stride = U.stride(0) if U.dim() == 3 else n * ld
+    if batch is None or batch_stride is None:
+        raise ValueError("batch and batch_stride are required for raw pointers")
+    out = (ctypes.c_longlong * max(1, int(batch)))()
+    st = library().bs_check_feasible_noalloc(_ptr(U), _ptr(L), n, ld, int(batch_stride),
+                                             int(batch), _stream(stream), _dtype_bits(U, mode),
+                                             out)
+    _check(st, "bs_check_feasible_noalloc")
+    return [int(out[b]) for b in range(int(batch))]
 
 
 def bs_strerror(status: int) -> str:

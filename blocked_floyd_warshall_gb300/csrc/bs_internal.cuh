@@ -32,6 +32,8 @@ enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3 };
 // event pair around each launch on `s`.
 void before_launch(cudaStream_t s, int phase);
 void after_launch(cudaStream_t s, int phase);
+// Counts a launch without recording profile events.
+void note_launch();
 
 // Per-round (reference) mode, round k.
 cudaError_t launch_round(bool is_int, const Mats& m, int k, bool literal, cudaStream_t s);

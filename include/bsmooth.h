@@ -108,6 +108,37 @@ bs_status bs_check_feasible(const void *U, const void *L, int n, int ld,
 /* Static text for a status code. */
 const char *bs_strerror(bs_status status);
 
+/* Infeasibility counts for callers that cannot allocate device memory.
+ * The method has no counterpart of this call; it exists for callers whose
+ * device memory belongs entirely to their own allocator (a framework's caching
+ * allocator that accounts for every byte, or a budget reserved up front) and
+ * for paths where the implicit synchronisation and latency of cudaMalloc are
+ * not allowed.  bs_check_feasible allocates a small buffer on its first call on
+ * a device; this call allocates nothing (no cudaMalloc, cudaFree or other
+ * allocating routine): its counters live in a fixed array of
+ * BS_NOALLOC_MAX_BATCH 8-byte counters in the library's own static device
+ * memory, which every device that loads the library holds until the process
+ * exits.
+ *
+ * Counts, for each of `batch` molecules (molecule b at U + b*batch_stride and
+ * L + b*batch_stride elements, as in bs_smooth_bounds_batched), the cells of
+ * its n x n block with L > U strictly, diagonal included, into out_counts[b]
+ * (host array of `batch` entries).  batch > BS_NOALLOC_MAX_BATCH returns
+ * BS_ERR_ARG without touching the GPU.  Only the dtype bits of `mode` are
+ * accepted.  Synchronises `stream`.
+ *
+ * The first call on each device looks up the device address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture on the device.  Every call clears the counters it
+ * uses, but all calls share one array: calls whose GPU work can overlap
+ * (different streams or host threads) race and must be serialised by the
+ * caller. */
+#define BS_NOALLOC_MAX_BATCH 4096
+bs_status bs_check_feasible_noalloc(const void *U, const void *L, int n, int ld,
+                                    long long batch_stride, int batch,
+                                    bs_stream_t stream, int mode,
+                                    long long *out_counts);
+
 /* ---- instrumentation (not part of the method) ---------------------------- */
 
 /* Number of kernels this library has launched since it was loaded. */
