@@ -238,6 +238,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-probe", action="store_true",
                     help="skip the ALU issue-rate probes")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every benchmark molecule (one JSON line each) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -245,6 +247,8 @@ def main():
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, ws, rank)
+    if args.sweep:
+        return sweep(args)
 
     import torch
     import blocked_floyd_warshall_gb300 as bsm
@@ -370,6 +374,71 @@ def main():
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+    return 0
+
+
+SCHEDULE_FLAGS = {"auto": 0, "t64": 1 << 5, "t128": 1 << 6, "t64_serial": (1 << 5) | (1 << 7),
+                  "t128_serial": (1 << 6) | (1 << 7), "perk": 1 << 2}
+ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial")
+SWEEP = (
+    # (config, dtype, schedules, description)
+    (0, "f32", ALL_SCHEDULES, "chain n=256"),
+    (1, "f32", ALL_SCHEDULES, "chain n=1000"),
+    (2, "f32", ALL_SCHEDULES + ("perk",), "globule n=4096"),
+    (2, "i32", ("auto",), "globule n=4096"),
+    (3, "f32", ALL_SCHEDULES, "256 chains n=512, batched"),
+    (4, "f32", ("auto", "t128_serial"), "globule n=16384"),
+)
+
+
+def sweep(args):
+    """Device time of one smoothing for every benchmark molecule."""
+    import torch
+    import blocked_floyd_warshall_gb300 as bsm
+    from workloads import make_config, to_f32
+    bsm.build()
+    props = torch.cuda.get_device_properties(0)
+    peaks = load_peaks()
+    alu = props.multi_processor_count * FP32_LANES_PER_SM * peaks["sm_max_mhz"] * 1e6
+    cache = {}
+    for cfg, dt, scheds, desc in SWEEP:
+        for algo in scheds:
+            if cfg not in cache:
+                cache.clear()
+                cache[cfg] = make_config(cfg)
+            m = cache[cfg]
+            U0, L0 = (to_f32(m["U"]), to_f32(m["L"])) if dt == "f32" else (m["U"], m["L"])
+            dU0, dL0 = torch.from_numpy(U0).cuda(), torch.from_numpy(L0).cuda()
+            n = m["n"]
+            batch = m.get("batch", 1)
+            flags = SCHEDULE_FLAGS[algo]
+            reps = max(3, min(args.steps, 20)) if n < 16384 else max(3, min(args.steps, 5))
+            times = []
+            for r in range(args.warmup + reps):
+                U, L = dU0.clone(), dL0.clone()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                if batch > 1:
+                    bsm.bs_smooth_bounds_batched(U, L, flags=flags)
+                else:
+                    bsm.bs_smooth_bounds(U, L, flags=flags)
+                b.record()
+                torch.cuda.synchronize()
+                if r >= args.warmup:
+                    times.append(a.elapsed_time(b))
+            ms = statistics.median(times)
+            cells = batch * float(n) ** 3
+            rate = cells / (ms * 1e-3)
+            line = {"sweep": desc, "config": cfg, "dtype": dt, "mode": algo, "n": n, "batch": batch,
+                    "ms_median": ms, "ms_best": min(times), "cell_updates_per_s": rate,
+                    "fp32_alu_frac": rate * OPS_PER_CELL / alu}
+            if algo == "perk":
+                gbs = rate * 16 / 1e9
+                line["hbm_gbs_algorithmic"] = gbs
+                line["hbm_frac"] = gbs / peaks["hbm_gbs"]
+            print(json.dumps(line), flush=True)
+            del dU0, dL0
     return 0
 
 

@@ -42,6 +42,9 @@ BS_PERK = 1 << 2
 BS_RULE_CLOSURE = 0
 BS_RULE_LITERAL = 1 << 3
 BS_VALIDATE = 1 << 4
+BS_TILE_64 = 1 << 5
+BS_TILE_128 = 1 << 6
+BS_NO_LOOKAHEAD = 1 << 7
 
 PHASES = ("round", "phase1", "phase2", "phase3")
 

@@ -12,9 +12,18 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// A side stream and two events for the look-ahead schedule.  A call holds
+// one exclusively while it enqueues, so concurrent callers never share events.
+struct SideCtx {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr;   // recorded on the caller's stream
+    cudaEvent_t join = nullptr;   // recorded on the side stream
+};
+
 struct DeviceState {
     bool ready = false;                   // kernel attributes set
     unsigned long long* scratch = nullptr;  // [0] count, [1] validation flags
+    std::vector<SideCtx> free_side;       // idle look-ahead contexts
 };
 
 std::mutex g_mu;
@@ -67,6 +76,88 @@ cudaError_t device_scratch(unsigned long long** out) {
     return cudaSuccess;
 }
 
+cudaError_t acquire_side(DeviceState* d, SideCtx* out) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!d->free_side.empty()) {
+            *out = d->free_side.back();
+            d->free_side.pop_back();
+            return cudaSuccess;
+        }
+    }
+    // Highest priority: the work distributor then hands the next free SM slot
+    // to phases 1 and 2 of round K+1 instead of to more tiles of round K.
+    SideCtx c;
+    int lo = 0, hi = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, hi);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        if (c.join) cudaEventDestroy(c.join);
+        if (c.fork) cudaEventDestroy(c.fork);
+        if (c.side) cudaStreamDestroy(c.side);
+        return e;
+    }
+    *out = c;
+    return cudaSuccess;
+}
+
+void release_side(DeviceState* d, const SideCtx& c) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    d->free_side.push_back(c);
+}
+
+// Tile size for the blocked schedule: 64 x 64 tiles for small matrices, where
+// the serial phases 1 and 2 dominate, 128 x 128 otherwise.
+int choose_tile(int n, int batch, int mode) {
+    if (mode & BS_TILE_64) return bs::FB_SMALL;
+    if (mode & BS_TILE_128) return bs::FB_LARGE;
+    (void)batch;
+    return n <= 1536 ? bs::FB_SMALL : bs::FB_LARGE;
+}
+
+// The blocked schedule.  Without look-ahead: for each block round K, phase 1,
+// phase 2, phase 3 on `s`.  With look-ahead (nb >= 3), phase 3 of round K is
+// split: the tiles of block-row/column K+1 first, then phases 1 and 2 of round
+// K+1 on the side stream while the remaining tiles of round K run on `s`.
+// The split is exact: those remaining tiles neither read nor write anything
+// phases 1 and 2 of round K+1 touch.
+cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
+                        DeviceState* d) {
+    const int nb = (m.n + m.fb - 1) / m.fb;
+    cudaError_t e = bs::launch_phase1(is_int, m, 0, s);
+    if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, 0, s);
+    if (e != cudaSuccess) return e;
+    if (!lookahead || nb < 3) {
+        for (int K = 0; K < nb && e == cudaSuccess; ++K) {
+            e = bs::launch_phase3(is_int, m, K, bs::P3_ALL, s);
+            if (e == cudaSuccess && K + 1 < nb) e = bs::launch_phase1(is_int, m, K + 1, s);
+            if (e == cudaSuccess && K + 1 < nb) e = bs::launch_phase2(is_int, m, K + 1, s);
+        }
+        return e;
+    }
+    SideCtx c;
+    e = acquire_side(d, &c);
+    if (e != cudaSuccess) return e;
+    for (int K = 0; K < nb && e == cudaSuccess; ++K) {
+        if (K + 1 == nb) {
+            e = bs::launch_phase3(is_int, m, K, bs::P3_ALL, s);
+            break;
+        }
+        e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT, s);
+        if (e == cudaSuccess) e = cudaEventRecord(c.fork, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c.side, c.fork, 0);
+        if (e == cudaSuccess) e = bs::launch_phase1(is_int, m, K + 1, c.side);
+        if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K + 1, c.side);
+        if (e == cudaSuccess) e = cudaEventRecord(c.join, c.side);
+        if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, bs::P3_REST, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c.join, 0);
+    }
+    release_side(d, c);
+    return e;
+}
+
 bs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BS_OK : BS_ERR_CUDA; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -74,8 +165,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Common argument checks.  Returns BS_OK and fills `m`, or an error.
 bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
                      long long bstride, int batch, int mode, bs::Mats* m) {
-    const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE;
+    const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE | BS_TILE_64 |
+                      BS_TILE_128 | BS_NO_LOOKAHEAD;
     if (mode & ~known) return BS_ERR_ARG;
+    if ((mode & BS_TILE_64) && (mode & BS_TILE_128)) return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
     if (n < 0 || batch < 0) return BS_ERR_ARG;
     if (n > 0 && ld < n) return BS_ERR_ARG;
@@ -94,6 +187,7 @@ bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
     m->batch = batch;
     m->vec = (ld % 4 == 0) && aligned(U, 16) && (!bounds || aligned(L, 16)) &&
              (batch <= 1 || bstride % 4 == 0);
+    m->fb = choose_tile(n, batch, mode);
     return BS_OK;
 }
 
@@ -136,12 +230,7 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
             if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
         }
     } else {
-        const int nb = (n + bs::FB - 1) / bs::FB;
-        for (int K = 0; K < nb && e == cudaSuccess; ++K) {
-            e = bs::launch_phase1(is_int, m, K, s);
-            if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K, s);
-            if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, s);
-        }
+        e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0, d);
     }
     return cuda_status(e);
 }

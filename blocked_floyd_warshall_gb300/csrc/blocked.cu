@@ -45,8 +45,8 @@ __device__ __forceinline__ void cp_async_wait() {
 
 // ---------------------------------------------------------------- phase 1
 
-template <class T, bool HAS_L>
-__global__ void __launch_bounds__(NT, 1)
+template <class T, bool HAS_L, int FB>
+__global__ void __launch_bounds__(TileShape<FB>::NT)
 k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
     using E = El<T>;
     __shared__ T sRU[2][FB], sRL[2][FB], sCU[2][FB], sCL[2][FB];
@@ -59,13 +59,13 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     T* Lt = HAS_L ? L + (size_t)o * ld + o : nullptr;
 
     T u[TM][TN], l[TM][TN];
-    load_tile(u, Ut, ld, m, m, vec, E::upad());
-    if (HAS_L) load_tile(l, Lt, ld, m, m, vec, E::lpad());
-    publish_row<T, HAS_L>(u, l, 0, sRU[0], sRL[0]);
-    publish_col<T, HAS_L>(u, l, 0, sCU[0], sCL[0]);
+    load_tile<FB>(u, Ut, ld, m, m, vec, E::upad());
+    if (HAS_L) load_tile<FB>(l, Lt, ld, m, m, vec, E::lpad());
+    publish_row<FB, T, HAS_L>(u, l, 0, sRU[0], sRL[0]);
+    publish_col<FB, T, HAS_L>(u, l, 0, sCU[0], sCL[0]);
     __syncthreads();
 
-    const int r0 = mt_row0();
+    const int r0 = mt_row0<FB>();
     for (int k = 0; k < m; ++k) {
         const int b = k & 1;
         T a[TM], al[TM], bb[TN], bl[TN];
@@ -76,8 +76,8 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
         }
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
-            bb[c] = sRU[b][mt_col(c)];
-            bl[c] = HAS_L ? sRL[b][mt_col(c)] : T(0);
+            bb[c] = sRU[b][mt_col<FB>(c)];
+            bl[c] = HAS_L ? sRL[b][mt_col<FB>(c)] : T(0);
         }
         if (HAS_L) {
             const T lkk = sRL[b][k];
@@ -86,26 +86,28 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
         }
         fw_update<T, HAS_L>(u, l, a, al, bb, bl);
         if (k + 1 < m) {
-            publish_row<T, HAS_L>(u, l, k + 1, sRU[b ^ 1], sRL[b ^ 1]);
-            publish_col<T, HAS_L>(u, l, k + 1, sCU[b ^ 1], sCL[b ^ 1]);
+            publish_row<FB, T, HAS_L>(u, l, k + 1, sRU[b ^ 1], sRL[b ^ 1]);
+            publish_col<FB, T, HAS_L>(u, l, k + 1, sCU[b ^ 1], sCL[b ^ 1]);
         }
         __syncthreads();
     }
-    store_tile(u, Ut, ld, m, m, vec);
-    if (HAS_L) store_tile(l, Lt, ld, m, m, vec);
+    store_tile<FB>(u, Ut, ld, m, m, vec);
+    if (HAS_L) store_tile<FB>(l, Lt, ld, m, m, vec);
 }
 
 // ---------------------------------------------------------------- phase 2
 
 constexpr int DPAD = 1;   // diagonal tile row stride FB + DPAD in shared memory
 
-template <class T, bool HAS_L>
-__global__ void __launch_bounds__(NT, 1)
+template <class T, bool HAS_L, int FB>
+__global__ void __launch_bounds__(TileShape<FB>::NT)
 k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
     using E = El<T>;
+    constexpr int NT = TileShape<FB>::NT;
+    constexpr int DS = FB + DPAD;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* dU = reinterpret_cast<T*>(smem_raw);
-    T* dL = dU + FB * (FB + DPAD);
+    T* dL = dU + FB * DS;
     __shared__ T sU[2][FB], sL[2][FB];
 
     const size_t off = (size_t)blockIdx.z * (size_t)bstride;
@@ -122,46 +124,46 @@ k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     for (int e = threadIdx.x; e < FB * FB; e += NT) {
         const int i = e / FB, j = e % FB;
         const bool in = i < mk && j < mk;
-        dU[i * (FB + DPAD) + j] = in ? U[(size_t)(o + i) * ld + o + j] : E::upad();
-        if (HAS_L) dL[i * (FB + DPAD) + j] = in ? L[(size_t)(o + i) * ld + o + j] : E::lpad();
+        dU[i * DS + j] = in ? U[(size_t)(o + i) * ld + o + j] : E::upad();
+        if (HAS_L) dL[i * DS + j] = in ? L[(size_t)(o + i) * ld + o + j] : E::lpad();
     }
 
-    const int r0 = mt_row0();
+    const int r0 = mt_row0<FB>();
     T u[TM][TN], l[TM][TN];
     if (row_panel) {
         // tile (K, P): rows of block K, columns of block P
         T* Ut = U + (size_t)o * ld + op;
         T* Lt = HAS_L ? L + (size_t)o * ld + op : nullptr;
-        load_tile(u, Ut, ld, mk, mp, vec, E::upad());
-        if (HAS_L) load_tile(l, Lt, ld, mk, mp, vec, E::lpad());
-        publish_row<T, HAS_L>(u, l, 0, sU[0], sL[0]);
+        load_tile<FB>(u, Ut, ld, mk, mp, vec, E::upad());
+        if (HAS_L) load_tile<FB>(l, Lt, ld, mk, mp, vec, E::lpad());
+        publish_row<FB, T, HAS_L>(u, l, 0, sU[0], sL[0]);
         __syncthreads();
         for (int k = 0; k < mk; ++k) {
             const int b = k & 1;
             T a[TM], al[TM], bb[TN], bl[TN];
 #pragma unroll
             for (int r = 0; r < TM; ++r) {
-                a[r] = dU[(r0 + r) * (FB + DPAD) + k];
-                al[r] = HAS_L ? dL[(r0 + r) * (FB + DPAD) + k] : T(0);
+                a[r] = dU[(r0 + r) * DS + k];
+                al[r] = HAS_L ? dL[(r0 + r) * DS + k] : T(0);
             }
 #pragma unroll
             for (int c = 0; c < TN; ++c) {
-                bb[c] = sU[b][mt_col(c)];
-                bl[c] = HAS_L ? sL[b][mt_col(c)] : T(0);
+                bb[c] = sU[b][mt_col<FB>(c)];
+                bl[c] = HAS_L ? sL[b][mt_col<FB>(c)] : T(0);
             }
             fw_update<T, HAS_L>(u, l, a, al, bb, bl);
-            if (k + 1 < mk) publish_row<T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
+            if (k + 1 < mk) publish_row<FB, T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
             __syncthreads();
         }
-        store_tile(u, Ut, ld, mk, mp, vec);
-        if (HAS_L) store_tile(l, Lt, ld, mk, mp, vec);
+        store_tile<FB>(u, Ut, ld, mk, mp, vec);
+        if (HAS_L) store_tile<FB>(l, Lt, ld, mk, mp, vec);
     } else {
         // tile (P, K): rows of block P, columns of block K
         T* Ut = U + (size_t)op * ld + o;
         T* Lt = HAS_L ? L + (size_t)op * ld + o : nullptr;
-        load_tile(u, Ut, ld, mp, mk, vec, E::upad());
-        if (HAS_L) load_tile(l, Lt, ld, mp, mk, vec, E::lpad());
-        publish_col<T, HAS_L>(u, l, 0, sU[0], sL[0]);
+        load_tile<FB>(u, Ut, ld, mp, mk, vec, E::upad());
+        if (HAS_L) load_tile<FB>(l, Lt, ld, mp, mk, vec, E::lpad());
+        publish_col<FB, T, HAS_L>(u, l, 0, sU[0], sL[0]);
         __syncthreads();
         for (int k = 0; k < mk; ++k) {
             const int b = k & 1;
@@ -173,20 +175,20 @@ k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
             }
 #pragma unroll
             for (int c = 0; c < TN; ++c) {
-                bb[c] = dU[k * (FB + DPAD) + mt_col(c)];
-                bl[c] = HAS_L ? dL[k * (FB + DPAD) + mt_col(c)] : T(0);
+                bb[c] = dU[k * DS + mt_col<FB>(c)];
+                bl[c] = HAS_L ? dL[k * DS + mt_col<FB>(c)] : T(0);
             }
             if (HAS_L) {
-                const T lkk = dL[k * (FB + DPAD) + k];
+                const T lkk = dL[k * DS + k];
 #pragma unroll
                 for (int r = 0; r < TM; ++r) al[r] = E::mx(al[r], E::sub(lkk, a[r]));
             }
             fw_update<T, HAS_L>(u, l, a, al, bb, bl);
-            if (k + 1 < mk) publish_col<T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
+            if (k + 1 < mk) publish_col<FB, T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
             __syncthreads();
         }
-        store_tile(u, Ut, ld, mp, mk, vec);
-        if (HAS_L) store_tile(l, Lt, ld, mp, mk, vec);
+        store_tile<FB>(u, Ut, ld, mp, mk, vec);
+        if (HAS_L) store_tile<FB>(l, Lt, ld, mp, mk, vec);
     }
 }
 
@@ -209,7 +211,7 @@ k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
 constexpr int BK = 16;        // middle atoms staged per pipeline stage
 constexpr int AST = BK + 4;   // column-panel row stride (elements); rows stay 16-byte aligned
 
-template <class T, bool HAS_L>
+template <class T, bool HAS_L, int FB>
 struct P3Smem {
     // one stage: column panel A[i][k] (FB x AST) and row panel B[k/2][j][k%2]
     static constexpr int A_ELEMS = FB * AST;
@@ -225,12 +227,13 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
 }
 
 // Stage k-chunk `c` of both panels into shared memory stage `stage`.
-template <class T, bool HAS_L>
+template <class T, bool HAS_L, int FB>
 __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_t ld, int oi,
                                          int oj, int ok, int mi, int mj, int mk, int c,
                                          bool vec) {
     using E = El<T>;
-    using S = P3Smem<T, HAS_L>;
+    using S = P3Smem<T, HAS_L, FB>;
+    constexpr int NT = TileShape<FB>::NT;
     T* AU = stage;
     T* BU = stage + S::A_ELEMS;
     T* AL = HAS_L ? BU + S::B_ELEMS : nullptr;
@@ -348,11 +351,38 @@ template <> struct PairLoad<int> {
     static __device__ __forceinline__ P neg(P x) { return make_int2(-x.x, -x.y); }
 };
 
-template <class T, bool HAS_L>
-__global__ void __launch_bounds__(NT, 1)
-k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
+// Which tiles a phase-3 launch covers (block round K, nb tile rows):
+//   P3_ALL  : every tile outside block-row K and block-column K, (nb-1)^2;
+//   P3_NEXT : those in block-row K+1 or block-column K+1, 2nb-3 (the tiles the
+//             next block round's phases 1 and 2 read and write);
+//   P3_REST : the others, (nb-2)^2.
+__device__ __forceinline__ void p3_tile(int part, int t, int nb, int K, int& I, int& J) {
+    if (part == P3_ALL) {
+        const int ti = t / (nb - 1), tj = t % (nb - 1);
+        I = ti + (ti >= K);
+        J = tj + (tj >= K);
+    } else if (part == P3_NEXT) {
+        if (t < nb - 1) {
+            I = K + 1;
+            J = t + (t >= K);
+        } else {
+            const int u = t - (nb - 1);
+            I = u + 2 * (u >= K);
+            J = K + 1;
+        }
+    } else {
+        const int ti = t / (nb - 2), tj = t % (nb - 2);
+        I = ti + 2 * (ti >= K);
+        J = tj + 2 * (tj >= K);
+    }
+}
+
+template <class T, bool HAS_L, int FB>
+__global__ void __launch_bounds__(TileShape<FB>::NT)
+k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K,
+         int part, bool vec) {
     using E = El<T>;
-    using S = P3Smem<T, HAS_L>;
+    using S = P3Smem<T, HAS_L, FB>;
     using LD = PairLoad<T>;
     using P = typename LD::P;
     constexpr bool NEG = std::is_same<T, int>::value;   // int lower bound adds negated values
@@ -363,24 +393,23 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     U += off;
     if (HAS_L) L += off;
     const int nb = (n + FB - 1) / FB;
-    const int t = blockIdx.x;
-    const int ti = t / (nb - 1), tj = t % (nb - 1);
-    const int I = ti + (ti >= K), J = tj + (tj >= K);
+    int I, J;
+    p3_tile(part, blockIdx.x, nb, K, I, J);
     const int oi = I * FB, oj = J * FB, ok = K * FB;
     const int mi = min(FB, n - oi), mj = min(FB, n - oj), mk = min(FB, n - ok);
 
     T u[TM][TN], l[TM][TN];
-    load_tile(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
-    if (HAS_L) load_tile(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
+    load_tile<FB>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
+    if (HAS_L) load_tile<FB>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
 
     const int nchunks = (mk + BK - 1) / BK;
-    p3_stage<T, HAS_L>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
+    p3_stage<T, HAS_L, FB>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
     cp_async_commit();
-    const int r0 = mt_row0(), cq = mt_cq();
+    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
     for (int c = 0; c < nchunks; ++c) {
         if (c + 1 < nchunks)
-            p3_stage<T, HAS_L>(sm + ((c + 1) & 1) * S::STAGE, U, L, ld, oi, oj, ok, mi, mj, mk,
-                               c + 1, vec);
+            p3_stage<T, HAS_L, FB>(sm + ((c + 1) & 1) * S::STAGE, U, L, ld, oi, oj, ok, mi, mj,
+                                   mk, c + 1, vec);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
@@ -399,11 +428,12 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
             const int bo = (kk >> 1) * (2 * FB);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                LD::ld4(BU + bo + (h * 64 + cq) * 2, b[h * 4 + 0], b[h * 4 + 1]);
-                LD::ld4(BU + bo + (h * 64 + cq) * 2 + 4, b[h * 4 + 2], b[h * 4 + 3]);
+                const int jb = bo + (h * (FB / 2) + cq) * 2;
+                LD::ld4(BU + jb, b[h * 4 + 0], b[h * 4 + 1]);
+                LD::ld4(BU + jb + 4, b[h * 4 + 2], b[h * 4 + 3]);
                 if (HAS_L) {
-                    LD::ld4(BL + bo + (h * 64 + cq) * 2, bl[h * 4 + 0], bl[h * 4 + 1]);
-                    LD::ld4(BL + bo + (h * 64 + cq) * 2 + 4, bl[h * 4 + 2], bl[h * 4 + 3]);
+                    LD::ld4(BL + jb, bl[h * 4 + 0], bl[h * 4 + 1]);
+                    LD::ld4(BL + jb + 4, bl[h * 4 + 2], bl[h * 4 + 3]);
                 }
             }
 #pragma unroll
@@ -426,57 +456,70 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
         }
         __syncthreads();
     }
-    store_tile(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
-    if (HAS_L) store_tile(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
+    store_tile<FB>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
+    if (HAS_L) store_tile<FB>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
 }
 
 // ---------------------------------------------------------------- launchers
 
-template <class T, bool HAS_L>
+template <class T, bool HAS_L, int FB>
 static size_t p2_smem() {
     return (size_t)(HAS_L ? 2 : 1) * FB * (FB + DPAD) * sizeof(T);
 }
 
-template <class T, bool HAS_L>
+template <class T, bool HAS_L, int FB>
 static cudaError_t setup_t() {
-    cudaError_t e = cudaFuncSetAttribute(k_phase2<T, HAS_L>,
+    cudaError_t e = cudaFuncSetAttribute(k_phase2<T, HAS_L, FB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p2_smem<T, HAS_L>());
+                                         (int)p2_smem<T, HAS_L, FB>());
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_phase3<T, HAS_L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)P3Smem<T, HAS_L>::BYTES);
+    return cudaFuncSetAttribute(k_phase3<T, HAS_L, FB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)P3Smem<T, HAS_L, FB>::BYTES);
 }
 
-cudaError_t blocked_setup(bool is_int) {
-    cudaError_t e = is_int ? setup_t<int, true>() : setup_t<float, true>();
-    if (e != cudaSuccess) return e;
-    return is_int ? setup_t<int, false>() : setup_t<float, false>();
+template <class T>
+static cudaError_t setup_all() {
+    cudaError_t e = setup_t<T, true, FB_LARGE>();
+    if (e == cudaSuccess) e = setup_t<T, false, FB_LARGE>();
+    if (e == cudaSuccess) e = setup_t<T, true, FB_SMALL>();
+    if (e == cudaSuccess) e = setup_t<T, false, FB_SMALL>();
+    return e;
 }
+
+cudaError_t blocked_setup(bool is_int) { return is_int ? setup_all<int>() : setup_all<float>(); }
 
 enum class Which { One, Two, Three };
 
-template <class T, bool HAS_L>
-static cudaError_t phase_t(Which w, const Mats& m, int K, cudaStream_t s) {
+template <class T, bool HAS_L, int FB>
+static cudaError_t phase_t(Which w, const Mats& m, int K, int part, cudaStream_t s) {
+    constexpr int NT = TileShape<FB>::NT;
     const int nb = (m.n + FB - 1) / FB;
+    int tiles = 0;
+    if (w == Which::Three) {
+        tiles = part == P3_ALL ? (nb - 1) * (nb - 1)
+                : part == P3_NEXT ? (K + 1 < nb ? 2 * nb - 3 : 0)
+                                  : (K + 1 < nb ? (nb - 2) * (nb - 2) : 0);
+        if (nb < 2 || tiles <= 0) return cudaSuccess;
+    }
+    if (w == Which::Two && nb < 2) return cudaSuccess;
     for (int b0 = 0; b0 < m.batch; b0 += 65535) {
         const int nbz = m.batch - b0 < 65535 ? m.batch - b0 : 65535;
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
         if (w == Which::One) {
             before_launch(s, PH_ONE);
-            k_phase1<T, HAS_L><<<dim3(1, 1, nbz), NT, 0, s>>>(U, L, m.n, m.ld, m.bstride, K, m.vec);
+            k_phase1<T, HAS_L, FB><<<dim3(1, 1, nbz), NT, 0, s>>>(U, L, m.n, m.ld, m.bstride, K,
+                                                                  m.vec);
             after_launch(s, PH_ONE);
         } else if (w == Which::Two) {
-            if (nb < 2) return cudaSuccess;
             before_launch(s, PH_TWO);
-            k_phase2<T, HAS_L><<<dim3(nb - 1, 2, nbz), NT, p2_smem<T, HAS_L>(), s>>>(
+            k_phase2<T, HAS_L, FB><<<dim3(nb - 1, 2, nbz), NT, p2_smem<T, HAS_L, FB>(), s>>>(
                 U, L, m.n, m.ld, m.bstride, K, m.vec);
             after_launch(s, PH_TWO);
         } else {
-            if (nb < 2) return cudaSuccess;
             before_launch(s, PH_THREE);
-            k_phase3<T, HAS_L><<<dim3((nb - 1) * (nb - 1), 1, nbz), NT, P3Smem<T, HAS_L>::BYTES,
-                                 s>>>(U, L, m.n, m.ld, m.bstride, K, m.vec);
+            k_phase3<T, HAS_L, FB><<<dim3(tiles, 1, nbz), NT, P3Smem<T, HAS_L, FB>::BYTES, s>>>(
+                U, L, m.n, m.ld, m.bstride, K, part, m.vec);
             after_launch(s, PH_THREE);
         }
         cudaError_t e = cudaGetLastError();
@@ -485,19 +528,25 @@ static cudaError_t phase_t(Which w, const Mats& m, int K, cudaStream_t s) {
     return cudaSuccess;
 }
 
-static cudaError_t phase(Which w, bool is_int, const Mats& m, int K, cudaStream_t s) {
-    if (is_int) return m.L ? phase_t<int, true>(w, m, K, s) : phase_t<int, false>(w, m, K, s);
-    return m.L ? phase_t<float, true>(w, m, K, s) : phase_t<float, false>(w, m, K, s);
+template <class T, bool HAS_L>
+static cudaError_t phase_fb(Which w, const Mats& m, int K, int part, cudaStream_t s) {
+    return m.fb == FB_SMALL ? phase_t<T, HAS_L, FB_SMALL>(w, m, K, part, s)
+                            : phase_t<T, HAS_L, FB_LARGE>(w, m, K, part, s);
+}
+
+static cudaError_t phase(Which w, bool is_int, const Mats& m, int K, int part, cudaStream_t s) {
+    if (is_int) return m.L ? phase_fb<int, true>(w, m, K, part, s) : phase_fb<int, false>(w, m, K, part, s);
+    return m.L ? phase_fb<float, true>(w, m, K, part, s) : phase_fb<float, false>(w, m, K, part, s);
 }
 
 cudaError_t launch_phase1(bool is_int, const Mats& m, int K, cudaStream_t s) {
-    return phase(Which::One, is_int, m, K, s);
+    return phase(Which::One, is_int, m, K, P3_ALL, s);
 }
 cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s) {
-    return phase(Which::Two, is_int, m, K, s);
+    return phase(Which::Two, is_int, m, K, P3_ALL, s);
 }
-cudaError_t launch_phase3(bool is_int, const Mats& m, int K, cudaStream_t s) {
-    return phase(Which::Three, is_int, m, K, s);
+cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s) {
+    return phase(Which::Three, is_int, m, K, part, s);
 }
 
 }  // namespace bs

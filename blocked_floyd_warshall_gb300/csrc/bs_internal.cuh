@@ -6,14 +6,17 @@
 
 namespace bs {
 
-// Floyd-Warshall block (tile) size of the three-phase schedule, and the CTA
-// shape every blocked kernel uses: 256 threads, each owning an 8 x 8 micro-tile
-// of U (and of L) -- rows 8*ty .. 8*ty+7, columns 4*tx+q and 64+4*tx+q
-// (ty = tid/16, tx = tid%16, q = 0..3).
-constexpr int FB = 128;
-constexpr int NT = 256;
+// Floyd-Warshall block (tile) sizes of the three-phase schedule: 128 for large
+// matrices, 64 for small ones (a quarter of the serial work per block round).
+// Every blocked kernel runs (FB/8)^2 threads (256 or 64), each owning an 8 x 8
+// micro-tile of U (and of L).
+constexpr int FB_LARGE = 128;
+constexpr int FB_SMALL = 64;
 constexpr int TM = 8;
 constexpr int TN = 8;
+template <int FB> struct TileShape {
+    static constexpr int NT = (FB / 8) * (FB / 8);
+};
 
 // One batch of matrices as the kernels see it.
 struct Mats {
@@ -24,6 +27,7 @@ struct Mats {
     long long bstride;    // elements between molecules
     int batch;
     bool vec;             // 16-byte vector IO allowed (ld % 4 == 0, bases 16B-aligned)
+    int fb;               // blocked mode: tile size FB_LARGE or FB_SMALL
 };
 
 enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3 };
@@ -43,7 +47,9 @@ cudaError_t launch_cross(bool is_int, const Mats& m, int k, cudaStream_t s);
 cudaError_t blocked_setup(bool is_int);   // once per device: shared-memory limits
 cudaError_t launch_phase1(bool is_int, const Mats& m, int K, cudaStream_t s);
 cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
-cudaError_t launch_phase3(bool is_int, const Mats& m, int K, cudaStream_t s);
+// Phase 3 of block round K over the tiles `part` selects (P3_* below).
+cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s);
+enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2 };
 
 // Feasibility count and precondition checks.  `count` and `flags` are device
 // words the caller has zeroed on `s`.

@@ -35,24 +35,27 @@ template <> struct El<int> {
     static __device__ __forceinline__ int mx(int a, int b) { return max(a, b); }
 };
 
-// Micro-tile coordinates of this thread inside a FB x FB tile.
-__device__ __forceinline__ int mt_row0() { return (threadIdx.x >> 4) * TM; }
-__device__ __forceinline__ int mt_cq() { return (threadIdx.x & 15) * 4; }
-__device__ __forceinline__ int mt_col(int c) { return (c >> 2) * 64 + mt_cq() + (c & 3); }
+// Micro-tile coordinates of this thread inside an FB x FB tile (FB/8 x FB/8
+// threads): rows 8*ty .. 8*ty+7, columns 4*tx+q and FB/2+4*tx+q.
+template <int FB> __device__ __forceinline__ int mt_row0() { return (threadIdx.x / (FB / 8)) * TM; }
+template <int FB> __device__ __forceinline__ int mt_cq() { return (threadIdx.x % (FB / 8)) * 4; }
+template <int FB> __device__ __forceinline__ int mt_col(int c) {
+    return (c >> 2) * (FB / 2) + mt_cq<FB>() + (c & 3);
+}
 
 // Load the thread's 8 x 8 cells of the tile at `M` (tile origin; mr x mc cells
 // valid).  Cells outside get `pad`.
-template <class T>
+template <int FB, class T>
 __device__ __forceinline__ void load_tile(T (&x)[TM][TN], const T* M, size_t ld, int mr,
                                           int mc, bool vec, T pad) {
     using V4 = typename El<T>::V4;
-    const int r0 = mt_row0(), cq = mt_cq();
+    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
 #pragma unroll
     for (int r = 0; r < TM; ++r) {
         const int i = r0 + r;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int j = h * 64 + cq;
+            const int j = h * (FB / 2) + cq;
             if (vec && i < mr && j + 4 <= mc) {
                 const V4 v = *reinterpret_cast<const V4*>(M + (size_t)i * ld + j);
                 x[r][h * 4 + 0] = v.x;
@@ -69,18 +72,18 @@ __device__ __forceinline__ void load_tile(T (&x)[TM][TN], const T* M, size_t ld,
 }
 
 // Store the thread's cells that lie inside the mr x mc block.
-template <class T>
+template <int FB, class T>
 __device__ __forceinline__ void store_tile(const T (&x)[TM][TN], T* M, size_t ld, int mr,
                                            int mc, bool vec) {
     using V4 = typename El<T>::V4;
-    const int r0 = mt_row0(), cq = mt_cq();
+    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
 #pragma unroll
     for (int r = 0; r < TM; ++r) {
         const int i = r0 + r;
         if (i >= mr) continue;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int j = h * 64 + cq;
+            const int j = h * (FB / 2) + cq;
             if (vec && j + 4 <= mc) {
                 V4 v;
                 v.x = x[r][h * 4 + 0];
@@ -122,30 +125,30 @@ __device__ __forceinline__ void fw_update(T (&u)[TM][TN], T (&l)[TM][TN], const 
 }
 
 // Row k of the tile (U and L) into shared vectors, by the threads that own it.
-template <class T, bool HAS_L>
+template <int FB, class T, bool HAS_L>
 __device__ __forceinline__ void publish_row(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
                                             T* dU, T* dL) {
-    const int r0 = mt_row0();
+    const int r0 = mt_row0<FB>();
 #pragma unroll
     for (int r = 0; r < TM; ++r) {
         if (r0 + r == k) {
 #pragma unroll
             for (int c = 0; c < TN; ++c) {
-                dU[mt_col(c)] = u[r][c];
-                if (HAS_L) dL[mt_col(c)] = l[r][c];
+                dU[mt_col<FB>(c)] = u[r][c];
+                if (HAS_L) dL[mt_col<FB>(c)] = l[r][c];
             }
         }
     }
 }
 
 // Column k of the tile (U and L) into shared vectors, by the threads that own it.
-template <class T, bool HAS_L>
+template <int FB, class T, bool HAS_L>
 __device__ __forceinline__ void publish_col(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
                                             T* dU, T* dL) {
-    const int r0 = mt_row0();
+    const int r0 = mt_row0<FB>();
 #pragma unroll
     for (int c = 0; c < TN; ++c) {
-        if (mt_col(c) == k) {
+        if (mt_col<FB>(c) == k) {
 #pragma unroll
             for (int r = 0; r < TM; ++r) {
                 dU[r0 + r] = u[r][c];

@@ -36,7 +36,11 @@
  * Streams and devices.  Work is enqueued on `stream` (NULL = the legacy
  * default stream) of the calling thread's current device, which must hold
  * the matrices.  Smoothing calls return before the GPU finishes.
- * bs_check_feasible synchronises `stream` before it returns.
+ * bs_check_feasible synchronises `stream` before it returns.  In blocked mode
+ * (unless BS_NO_LOOKAHEAD) phases 1 and 2 of block round K+1 run on an
+ * internal stream of the library, forked from and joined back into `stream`
+ * with events inside the call, while the rest of round K's phase 3 runs on
+ * `stream`; all work still completes in `stream` order.
  *
  * Memory.  The caller owns U, L and the mask.  Smoothing allocates nothing.
  * bs_check_feasible and BS_VALIDATE use one small internal device buffer per
@@ -76,7 +80,12 @@ enum {
     BS_PERK = 1 << 2,         /* one round per middle atom k, round-synchronous */
     BS_RULE_CLOSURE = 0,      /* default lower-bound rule (see above) */
     BS_RULE_LITERAL = 1 << 3, /* printed rule; BS_PERK only, else BS_ERR_ARG */
-    BS_VALIDATE = 1 << 4      /* check the preconditions first (synchronises) */
+    BS_VALIDATE = 1 << 4,     /* check the preconditions first (synchronises) */
+    /* Blocked-mode schedule knobs; every setting gives identical results. */
+    BS_TILE_64 = 1 << 5,      /* force 64 x 64 tiles (default: chosen from n) */
+    BS_TILE_128 = 1 << 6,     /* force 128 x 128 tiles; both tile bits: BS_ERR_ARG */
+    BS_NO_LOOKAHEAD = 1 << 7  /* run the three phases of each block round in
+                                 sequence on `stream` only (see below) */
 };
 
 /* Upper bounds only (min-plus all-pairs shortest paths, section 3's loop).

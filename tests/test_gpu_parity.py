@@ -34,7 +34,15 @@ def as_dtype(Uq, Lq, dtype):
 
 
 SIZES_PERK = [1, 2, 3, 4, 5, 7, 31, 33, 64, 255, 256]
-SIZES_BLOCKED = [1, 2, 3, 5, 31, 64, 127, 128, 129, 255, 256, 257, 300, 383, 385, 513]
+SIZES_BLOCKED = [1, 2, 3, 5, 31, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 383, 385, 513]
+# blocked-mode schedules: automatic, forced tile sizes, with and without look-ahead
+SCHEDULES = {
+    "auto": 0,
+    "t64": bsm.BS_TILE_64,
+    "t128": bsm.BS_TILE_128,
+    "t64_serial": bsm.BS_TILE_64 | bsm.BS_NO_LOOKAHEAD,
+    "t128_serial": bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD,
+}
 
 
 @pytest.mark.parametrize("n", SIZES_PERK)
@@ -53,32 +61,34 @@ def test_per_round_matches_oracle(n, dtype, rule):
 
 @pytest.mark.parametrize("n", SIZES_BLOCKED)
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-def test_blocked_matches_oracle(n, dtype):
+@pytest.mark.parametrize("sched", sorted(SCHEDULES))
+def test_blocked_matches_oracle(n, dtype, sched):
     Uq, Lq = W.random_bounds(n, 2000 + n, p_known=0.2, p_bad=0.02)
     U0, L0 = as_dtype(Uq, Lq, dtype)
     Uo, Lo = oracle.smooth(U0, L0)
-    Ug, Lg, ok = gpu_bounds(U0, L0)
+    Ug, Lg, ok = gpu_bounds(U0, L0, SCHEDULES[sched])
     assert ok
     assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
 
 
 @pytest.mark.parametrize("n", [129, 300])
-def test_blocked_asymmetric(n):
+@pytest.mark.parametrize("sched", ["t64", "t128"])
+def test_blocked_asymmetric(n, sched):
     Uq, Lq = W.random_bounds(n, 3000 + n, p_known=0.3, p_bad=0.02, symmetric=False)
     Uo, Lo = oracle.smooth(Uq, Lq)
-    Ug, Lg, ok = gpu_bounds(Uq, Lq)
+    Ug, Lg, ok = gpu_bounds(Uq, Lq, SCHEDULES[sched])
     assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
 
 
 @pytest.mark.parametrize("n,ld,offset", [(130, 140, 0), (130, 133, 0), (257, 260, 1),
                                          (97, 101, 3), (200, 200, 1)])
-@pytest.mark.parametrize("algo", ["blocked", "perk"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
 def test_leading_dimension_and_misalignment(n, ld, offset, algo):
     """ld > n keeps the padding untouched; ld % 4 != 0 or a base not 16-byte
     aligned takes the scalar-IO instantiation with identical results."""
     Uq, Lq = W.random_bounds(n, 4000 + n, p_bad=0.02)
     U0, L0 = W.to_f32(Uq), W.to_f32(Lq)
-    flags = bsm.BS_PERK if algo == "perk" else 0
+    flags = bsm.BS_PERK if algo == "perk" else SCHEDULES[algo]
     Uo, Lo = oracle.smooth(U0, L0)
     Ug, Lg, ok = gpu_bounds(U0, L0, flags, ld=ld, offset=offset)
     assert ok
@@ -87,12 +97,12 @@ def test_leading_dimension_and_misalignment(n, ld, offset, algo):
 
 @pytest.mark.parametrize("n", [1, 5, 128, 129, 300])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("algo", ["blocked", "perk"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
 def test_upper_only(n, dtype, algo):
     Uq, _ = W.random_bounds(n, 5000 + n, p_known=0.25)
     U0 = W.to_f32(Uq) if dtype == "f32" else Uq
     Uo = oracle.smooth_upper(U0)
-    Ug, ok = gpu_upper(U0, bsm.BS_PERK if algo == "perk" else 0, ld=n + 3)
+    Ug, ok = gpu_upper(U0, bsm.BS_PERK if algo == "perk" else SCHEDULES[algo], ld=n + 3)
     assert ok and same_bits(Ug, Uo)
 
 
@@ -170,9 +180,10 @@ def globule4096():
     return m, Uo, Lo
 
 
-def test_globule_4096_int32_blocked(globule4096):
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial"])
+def test_globule_4096_int32_blocked(globule4096, sched):
     m, Uo, Lo = globule4096
-    Ug, Lg, ok = gpu_bounds(m["U"], m["L"])
+    Ug, Lg, ok = gpu_bounds(m["U"], m["L"], SCHEDULES[sched])
     assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
     U, L = dev(Ug), dev(Lg)
     assert bsm.bs_check_feasible(U, L) == oracle.count_infeasible(Uo, Lo) > 0
@@ -191,14 +202,15 @@ def test_globule_4096_fp32_blocked_and_per_round(globule4096):
         assert bsm.bs_check_feasible(dev(Ug), dev(Lg)) == expect_flags
 
 
-def test_batched_chains():
+@pytest.mark.parametrize("sched", ["auto", "t128"])
+def test_batched_chains(sched):
     """Batch of 256 molecules n=512 in one call; every 32nd molecule against the
     oracle, all molecules against a per-molecule GPU call."""
     m = W.make_config(3)
     B, n = m["batch"], m["n"]
     U0, L0 = W.to_f32(m["U"]), W.to_f32(m["L"])
     U, L = dev(U0), dev(L0)
-    bsm.bs_smooth_bounds_batched(U, L)
+    bsm.bs_smooth_bounds_batched(U, L, flags=SCHEDULES[sched])
     Ug, Lg = host(U), host(L)
     for b in range(0, B, 32):
         Uo, Lo = oracle.smooth(U0[b], L0[b])
@@ -220,7 +232,7 @@ def test_batched_per_round_and_strided():
     for b, (uq, lq) in enumerate(Us):
         Ubuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(uq))
         Lbuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(lq))
-    for flags in (bsm.BS_PERK, 0):
+    for flags in (bsm.BS_PERK, 0, bsm.BS_TILE_128):
         U, L = Ubuf.clone(), Lbuf.clone()
         bsm.bs_smooth_bounds_batched(U, L, n, ld, stride, B, None, bsm.BS_FP32 | flags)
         Uh, Lh = host(U), host(L)
@@ -301,15 +313,20 @@ def test_empty_and_launch_counting():
     bsm.bs_smooth_bounds(U, U.clone())
     assert bsm.bs_launch_count() == before
     Uq, Lq = W.random_bounds(300, 1, p_bad=0.01)
-    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)))
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)),
+                         flags=bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD)
     assert bsm.bs_launch_count() - before == 3 * 3        # three phases x three block rounds
+    before = bsm.bs_launch_count()
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_TILE_64)
+    # 5 block rounds: 5 x (phase 1, phase 2); phase 3 split in two for rounds 0..3
+    assert bsm.bs_launch_count() - before == 5 + 5 + 4 * 2 + 1
 
 
 def test_profile_records_every_launch():
     Uq, Lq = W.random_bounds(300, 2, p_bad=0.01)
     U, L = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
     bsm.bs_profile_begin()
-    bsm.bs_smooth_bounds(U, L)
+    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_TILE_128)
     p = bsm.bs_profile_end()
-    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 3]
+    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 5]   # rounds 0, 1: phase 3 split
     assert p["phase3"]["ms"] > 0
