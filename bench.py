@@ -49,6 +49,35 @@ def make_workload(name):
     return globule_bounds(wl["box"], wl["seed"], wl["p_long"])
 
 
+def tile_size(n, flags=0):
+    """Tile size the library picks (mirrors its rule; forced by the tile bits)."""
+    if flags & (1 << 5):
+        return 64
+    if flags & (1 << 6):
+        return 128
+    return 64 if n <= 1536 else 128
+
+
+def phase_cells(n, fb, sym=False):
+    """Cell updates (i, j, k) each phase executes in one blocked smoothing.
+    Without symmetry the three phases sum to n^3 exactly."""
+    nb = (n + fb - 1) // fb
+    sizes = [min(fb, n - K * fb) for K in range(nb)]
+    p1 = p2 = p3 = 0
+    for K, mk in enumerate(sizes):
+        rest = n - mk
+        p1 += mk ** 3
+        p2 += (1 if sym else 2) * rest * mk * mk
+        if sym:
+            others = [sizes[I] for I in range(nb) if I != K]
+            cells = sum(others[a] * others[b] for a in range(len(others))
+                        for b in range(a, len(others)))
+            p3 += cells * mk
+        else:
+            p3 += rest * rest * mk
+    return p1, p2, p3
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -70,9 +99,10 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(n):
-    """DRAM bytes per phase-3 launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+def committed_traffic(n, fb=128):
+    """DRAM bytes of phase 3 per smoothing step from the committed ncu summary
+    (bytes per cell update x the step's phase-3 cell updates), if the summary
+    was taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "phase3_traffic.json")
     if not os.path.exists(p):
         return None
@@ -83,8 +113,7 @@ def committed_traffic(n):
     per_cell_k = d.get("dram_bytes_per_cell_k")
     if per_cell_k is None:
         return None
-    fb = 128
-    return per_cell_k * float(n - fb) ** 2 * fb
+    return per_cell_k * float(phase_cells(n, fb)[2])
 
 
 # ------------------------------------------------------------------ clocks
@@ -238,6 +267,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-probe", action="store_true",
                     help="skip the ALU issue-rate probes")
+    ap.add_argument("--no-symmetric", action="store_true",
+                    help="skip the extra timing of the symmetric half-work mode")
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark molecule (one JSON line each) instead")
     args = ap.parse_args()
@@ -321,11 +352,12 @@ def main():
     fmax = peaks["sm_max_mhz"] * 1e6
     alu_peak_ops = sms * FP32_LANES_PER_SM * fmax            # ALU ops/s
     p3 = prof["phase3"]
-    fb = 128
-    p3_ops_per_launch = float(n - fb) ** 2 * fb * OPS_PER_CELL
-    p3_avg_s = p3["ms"] * 1e-3 / max(1, p3["launches"])
-    p3_achieved = p3_ops_per_launch / p3_avg_s if p3["launches"] else None
-    traffic = committed_traffic(n)
+    fb = tile_size(n)
+    p3_cells_step = phase_cells(n, fb)[2]
+    p3_ops_step = p3_cells_step * OPS_PER_CELL
+    p3_s_step = p3["ms"] * 1e-3 / args.steps
+    p3_achieved = p3_ops_step / p3_s_step if p3["launches"] else None
+    traffic = committed_traffic(n, fb)
     clocks = clk.summary()
 
     line = {
@@ -347,9 +379,14 @@ def main():
             "peak": alu_peak_ops / 1e12, "unit": "Tops/s",
             "frac": (p3_achieved / alu_peak_ops) if p3_achieved else None,
             "traffic": traffic,
-            "ops_per_launch": p3_ops_per_launch,
-            "avg_launch_ms": p3_avg_s * 1e3,
-            "launches": p3["launches"],
+            "traffic_basis": "DRAM bytes of all phase-3 launches of one smoothing step",
+            "ops_per_step": p3_ops_step,
+            "ms_per_step": p3_s_step * 1e3,
+            "launches_per_step": p3["launches"] / args.steps,
+            "achieved_basis": "6 ops x phase-3 cell updates of one step / summed device time of "
+                              "that step's phase-3 launches (each launch timed with CUDA events "
+                              "on its stream; phases 1-2 of the next round run concurrently on a "
+                              "side stream, so this understates the kernel alone)",
             "share_of_step": p3["ms"] / max(1e-9, sum(prof[k]["ms"] for k in bsm.PHASES)),
             "peak_basis": "SMs x 128 FP32 lanes x max SM clock, 6 ALU ops per cell update (%s)"
                           % peaks["source"],
@@ -359,6 +396,8 @@ def main():
         "clocks": clocks,
     }
 
+    if not args.no_symmetric:
+        line["symmetric"] = symmetric_leg(torch, bsm, dU0, dL0, copies, args, value / ws)
     if not args.no_probe:
         line["alu_probe_instr_per_clk_per_sm"] = {
             name: round(bsm.bs_probe_alu(name), 2) for name in bsm.PROBES}
@@ -378,8 +417,8 @@ def main():
 
 
 SCHEDULE_FLAGS = {"auto": 0, "t64": 1 << 5, "t128": 1 << 6, "t64_serial": (1 << 5) | (1 << 7),
-                  "t128_serial": (1 << 6) | (1 << 7), "perk": 1 << 2}
-ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial")
+                  "t128_serial": (1 << 6) | (1 << 7), "perk": 1 << 2, "sym": 1 << 8}
+ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial", "sym")
 SWEEP = (
     # (config, dtype, schedules, description)
     (0, "f32", ALL_SCHEDULES, "chain n=256"),
@@ -387,7 +426,7 @@ SWEEP = (
     (2, "f32", ALL_SCHEDULES + ("perk",), "globule n=4096"),
     (2, "i32", ("auto",), "globule n=4096"),
     (3, "f32", ALL_SCHEDULES, "256 chains n=512, batched"),
-    (4, "f32", ("auto", "t128_serial"), "globule n=16384"),
+    (4, "f32", ("auto", "t128_serial", "sym"), "globule n=16384"),
 )
 
 
@@ -433,6 +472,10 @@ def sweep(args):
             line = {"sweep": desc, "config": cfg, "dtype": dt, "mode": algo, "n": n, "batch": batch,
                     "ms_median": ms, "ms_best": min(times), "cell_updates_per_s": rate,
                     "fp32_alu_frac": rate * OPS_PER_CELL / alu}
+            if algo == "sym":
+                executed = batch * float(sum(phase_cells(n, tile_size(n, flags), sym=True)))
+                line["executed_cell_updates"] = executed
+                line["fp32_alu_frac_executed"] = executed / (ms * 1e-3) * OPS_PER_CELL / alu
             if algo == "perk":
                 gbs = rate * 16 / 1e9
                 line["hbm_gbs_algorithmic"] = gbs
@@ -440,6 +483,34 @@ def sweep(args):
             print(json.dumps(line), flush=True)
             del dU0, dL0
     return 0
+
+
+def symmetric_leg(torch, bsm, dU0, dL0, copies, args, general_rate):
+    """The same smoothing with BS_SYMMETRIC (tiles on and above the diagonal,
+    mirrored): same output, about half the cell updates executed.  Each step
+    restores its copy from the resident input outside the timed events."""
+    n = dU0.shape[0]
+    times = []
+    for s in range(args.steps):
+        U, L = copies[s % len(copies)]
+        U.copy_(dU0)
+        L.copy_(dL0)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        bsm.bs_smooth_bounds(U, L, flags=bsm.BS_SYMMETRIC)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    rate = float(n) ** 3 / (ms * 1e-3)
+    executed = float(sum(phase_cells(n, tile_size(n), sym=True)))
+    return {"ms_per_step": ms, "value": rate, "unit": UNIT + " (n^3 / time, same output)",
+            "speedup_vs_general": rate / general_rate,
+            "executed_cell_updates": executed,
+            "executed_cell_updates_per_s": executed / (ms * 1e-3),
+            "note": "inputs are symmetric; only tiles with I <= J are computed and mirrored, "
+                    "so about half of the n^3 cell updates are executed"}
 
 
 def e2e_leg(torch, bsm, U0, L0, args, ws):

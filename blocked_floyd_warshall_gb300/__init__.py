@@ -45,6 +45,7 @@ BS_VALIDATE = 1 << 4
 BS_TILE_64 = 1 << 5
 BS_TILE_128 = 1 << 6
 BS_NO_LOOKAHEAD = 1 << 7
+BS_SYMMETRIC = 1 << 8
 
 PHASES = ("round", "phase1", "phase2", "phase3")
 

@@ -166,7 +166,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
                      long long bstride, int batch, int mode, bs::Mats* m) {
     const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE | BS_TILE_64 |
-                      BS_TILE_128 | BS_NO_LOOKAHEAD;
+                      BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC;
     if (mode & ~known) return BS_ERR_ARG;
     if ((mode & BS_TILE_64) && (mode & BS_TILE_128)) return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
@@ -188,6 +188,7 @@ bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
     m->vec = (ld % 4 == 0) && aligned(U, 16) && (!bounds || aligned(L, 16)) &&
              (batch <= 1 || bstride % 4 == 0);
     m->fb = choose_tile(n, batch, mode);
+    m->sym = (mode & BS_SYMMETRIC) != 0;
     return BS_OK;
 }
 
@@ -202,7 +203,7 @@ bs_status validate(const bs::Mats& m, bool is_int, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaMemcpyAsync(&h, flags, sizeof h, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return BS_ERR_CUDA;
-    if (h & (bs::VF_DIAG | bs::VF_NEG | bs::VF_NAN | bs::VF_LINF)) return BS_ERR_INPUT;
+    if (h & (bs::VF_DIAG | bs::VF_NEG | bs::VF_NAN | bs::VF_LINF | bs::VF_ASYM)) return BS_ERR_INPUT;
     if (h & bs::VF_RANGE) return BS_ERR_RANGE;
     return BS_OK;
 }
@@ -215,6 +216,7 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
     const bool perk = (mode & BS_PERK) != 0;
     const bool literal = bounds && (mode & BS_RULE_LITERAL) != 0;
     if (literal && !perk) return BS_ERR_ARG;
+    if (perk && (mode & BS_SYMMETRIC)) return BS_ERR_ARG;
     if (n == 0 || batch == 0) return BS_OK;
     const bool is_int = (mode & BS_DTYPE_MASK) == BS_INT32_Q10;
     DeviceState* d = nullptr;

@@ -101,7 +101,8 @@ constexpr int DPAD = 1;   // diagonal tile row stride FB + DPAD in shared memory
 
 template <class T, bool HAS_L, int FB>
 __global__ void __launch_bounds__(TileShape<FB>::NT)
-k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
+k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec,
+         bool sym) {
     using E = El<T>;
     constexpr int NT = TileShape<FB>::NT;
     constexpr int DS = FB + DPAD;
@@ -157,6 +158,11 @@ k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
         }
         store_tile<FB>(u, Ut, ld, mk, mp, vec);
         if (HAS_L) store_tile<FB>(l, Lt, ld, mk, mp, vec);
+        if (sym) {
+            // symmetric inputs: the column panel tile (P, K) is the transpose
+            store_tile_t<FB>(u, U + (size_t)op * ld + o, ld, mk, mp, vec);
+            if (HAS_L) store_tile_t<FB>(l, L + (size_t)op * ld + o, ld, mk, mp, vec);
+        }
     } else {
         // tile (P, K): rows of block P, columns of block K
         T* Ut = U + (size_t)op * ld + o;
@@ -352,35 +358,69 @@ template <> struct PairLoad<int> {
 };
 
 // Which tiles a phase-3 launch covers (block round K, nb tile rows):
-//   P3_ALL  : every tile outside block-row K and block-column K, (nb-1)^2;
-//   P3_NEXT : those in block-row K+1 or block-column K+1, 2nb-3 (the tiles the
-//             next block round's phases 1 and 2 read and write);
-//   P3_REST : the others, (nb-2)^2.
-__device__ __forceinline__ void p3_tile(int part, int t, int nb, int K, int& I, int& J) {
-    if (part == P3_ALL) {
-        const int ti = t / (nb - 1), tj = t % (nb - 1);
-        I = ti + (ti >= K);
-        J = tj + (tj >= K);
-    } else if (part == P3_NEXT) {
-        if (t < nb - 1) {
-            I = K + 1;
-            J = t + (t >= K);
+//   P3_ALL  : every tile outside block-row K and block-column K;
+//   P3_NEXT : those in block-row K+1 or block-column K+1 (the tiles the next
+//             block round's phases 1 and 2 read and write);
+//   P3_REST : the others.
+// With symmetric inputs only tiles with I <= J are computed (each off-diagonal
+// one is also stored transposed): (nb-1)nb/2, nb-1 and (nb-2)(nb-1)/2 tiles.
+
+// t -> (a, b), a <= b, enumerating the upper triangle column by column.
+__device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
+    int c = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+    while (c * (c + 1) / 2 > t) --c;
+    while ((c + 1) * (c + 2) / 2 <= t) ++c;
+    b = c;
+    a = t - c * (c + 1) / 2;
+}
+
+__device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K, int& I,
+                                        int& J) {
+    if (!sym) {
+        if (part == P3_ALL) {
+            const int ti = t / (nb - 1), tj = t % (nb - 1);
+            I = ti + (ti >= K);
+            J = tj + (tj >= K);
+        } else if (part == P3_NEXT) {
+            if (t < nb - 1) {
+                I = K + 1;
+                J = t + (t >= K);
+            } else {
+                const int u = t - (nb - 1);
+                I = u + 2 * (u >= K);
+                J = K + 1;
+            }
         } else {
-            const int u = t - (nb - 1);
-            I = u + 2 * (u >= K);
+            const int ti = t / (nb - 2), tj = t % (nb - 2);
+            I = ti + 2 * (ti >= K);
+            J = tj + 2 * (tj >= K);
+        }
+        return;
+    }
+    int a, b;
+    if (part == P3_ALL) {
+        p3_tri(t, a, b);
+        I = a + (a >= K);
+        J = b + (b >= K);
+    } else if (part == P3_NEXT) {
+        if (t < nb - K - 1) {
+            I = K + 1;
+            J = K + 1 + t;
+        } else {
+            I = t - (nb - K - 1);
             J = K + 1;
         }
     } else {
-        const int ti = t / (nb - 2), tj = t % (nb - 2);
-        I = ti + 2 * (ti >= K);
-        J = tj + 2 * (tj >= K);
+        p3_tri(t, a, b);
+        I = a + 2 * (a >= K);
+        J = b + 2 * (b >= K);
     }
 }
 
 template <class T, bool HAS_L, int FB>
 __global__ void __launch_bounds__(TileShape<FB>::NT)
 k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K,
-         int part, bool vec) {
+         int part, bool vec, bool sym) {
     using E = El<T>;
     using S = P3Smem<T, HAS_L, FB>;
     using LD = PairLoad<T>;
@@ -394,7 +434,7 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     if (HAS_L) L += off;
     const int nb = (n + FB - 1) / FB;
     int I, J;
-    p3_tile(part, blockIdx.x, nb, K, I, J);
+    p3_tile(part, sym, blockIdx.x, nb, K, I, J);
     const int oi = I * FB, oj = J * FB, ok = K * FB;
     const int mi = min(FB, n - oi), mj = min(FB, n - oj), mk = min(FB, n - ok);
 
@@ -458,6 +498,10 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     }
     store_tile<FB>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
     if (HAS_L) store_tile<FB>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
+    if (sym && I != J) {
+        store_tile_t<FB>(u, U + (size_t)oj * ld + oi, ld, mi, mj, vec);
+        if (HAS_L) store_tile_t<FB>(l, L + (size_t)oj * ld + oi, ld, mi, mj, vec);
+    }
 }
 
 // ---------------------------------------------------------------- launchers
@@ -496,9 +540,14 @@ static cudaError_t phase_t(Which w, const Mats& m, int K, int part, cudaStream_t
     const int nb = (m.n + FB - 1) / FB;
     int tiles = 0;
     if (w == Which::Three) {
-        tiles = part == P3_ALL ? (nb - 1) * (nb - 1)
-                : part == P3_NEXT ? (K + 1 < nb ? 2 * nb - 3 : 0)
-                                  : (K + 1 < nb ? (nb - 2) * (nb - 2) : 0);
+        if (m.sym)
+            tiles = part == P3_ALL ? (nb - 1) * nb / 2
+                    : part == P3_NEXT ? (K + 1 < nb ? nb - 1 : 0)
+                                      : (K + 1 < nb ? (nb - 2) * (nb - 1) / 2 : 0);
+        else
+            tiles = part == P3_ALL ? (nb - 1) * (nb - 1)
+                    : part == P3_NEXT ? (K + 1 < nb ? 2 * nb - 3 : 0)
+                                      : (K + 1 < nb ? (nb - 2) * (nb - 2) : 0);
         if (nb < 2 || tiles <= 0) return cudaSuccess;
     }
     if (w == Which::Two && nb < 2) return cudaSuccess;
@@ -513,13 +562,13 @@ static cudaError_t phase_t(Which w, const Mats& m, int K, int part, cudaStream_t
             after_launch(s, PH_ONE);
         } else if (w == Which::Two) {
             before_launch(s, PH_TWO);
-            k_phase2<T, HAS_L, FB><<<dim3(nb - 1, 2, nbz), NT, p2_smem<T, HAS_L, FB>(), s>>>(
-                U, L, m.n, m.ld, m.bstride, K, m.vec);
+            k_phase2<T, HAS_L, FB><<<dim3(nb - 1, m.sym ? 1 : 2, nbz), NT, p2_smem<T, HAS_L, FB>(),
+                                     s>>>(U, L, m.n, m.ld, m.bstride, K, m.vec, m.sym);
             after_launch(s, PH_TWO);
         } else {
             before_launch(s, PH_THREE);
             k_phase3<T, HAS_L, FB><<<dim3(tiles, 1, nbz), NT, P3Smem<T, HAS_L, FB>::BYTES, s>>>(
-                U, L, m.n, m.ld, m.bstride, K, part, m.vec);
+                U, L, m.n, m.ld, m.bstride, K, part, m.vec, m.sym);
             after_launch(s, PH_THREE);
         }
         cudaError_t e = cudaGetLastError();

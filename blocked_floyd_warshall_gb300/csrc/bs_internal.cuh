@@ -28,6 +28,7 @@ struct Mats {
     int batch;
     bool vec;             // 16-byte vector IO allowed (ld % 4 == 0, bases 16B-aligned)
     int fb;               // blocked mode: tile size FB_LARGE or FB_SMALL
+    bool sym;             // blocked mode: inputs symmetric, compute half and mirror
 };
 
 enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3 };
@@ -63,7 +64,8 @@ enum : unsigned int {
     VF_NEG = 2u,        // negative value
     VF_NAN = 4u,        // NaN
     VF_LINF = 8u,       // infinite lower bound
-    VF_RANGE = 16u      // int32 value >= 2^30
+    VF_RANGE = 16u,     // int32 value >= 2^30
+    VF_ASYM = 32u       // Mats::sym set but U or L not symmetric
 };
 
 }  // namespace bs

@@ -100,6 +100,30 @@ __device__ __forceinline__ void store_tile(const T (&x)[TM][TN], T* M, size_t ld
     }
 }
 
+// Store the transpose of the thread's cells: cell (i, j) of an mr x mc tile
+// goes to MT[j*ld + i], MT being the origin of the mirrored tile.  For a fixed
+// column the thread's 8 rows are 8 consecutive elements (one 32-byte sector).
+template <int FB, class T>
+__device__ __forceinline__ void store_tile_t(const T (&x)[TM][TN], T* MT, size_t ld, int mr,
+                                             int mc, bool vec) {
+    using V4 = typename El<T>::V4;
+    const int r0 = mt_row0<FB>();
+#pragma unroll
+    for (int c = 0; c < TN; ++c) {
+        const int j = mt_col<FB>(c);
+        if (j >= mc) continue;
+        T* row = MT + (size_t)j * ld + r0;
+        if (vec && r0 + TM <= mr) {
+            *reinterpret_cast<V4*>(row) = V4{x[0][c], x[1][c], x[2][c], x[3][c]};
+            *reinterpret_cast<V4*>(row + 4) = V4{x[4][c], x[5][c], x[6][c], x[7][c]};
+        } else {
+#pragma unroll
+            for (int r = 0; r < TM; ++r)
+                if (r0 + r < mr) row[r] = x[r][c];
+        }
+    }
+}
+
 // One middle atom k applied to the thread's cells.  a/al: U[i,k] and the
 // lower-bound column value for the thread's rows; b/bl: U[k,j] and L[k,j] for
 // its columns.  Upper bound first, then the lower bound from the same

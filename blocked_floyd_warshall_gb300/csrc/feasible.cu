@@ -53,7 +53,7 @@ __device__ __forceinline__ unsigned int check_value(int v, bool, bool diag) {
 template <class T>
 __global__ void __launch_bounds__(256)
 k_validate(const T* __restrict__ U, const T* __restrict__ L, int n, int ld, long long bstride,
-           unsigned int* __restrict__ flags) {
+           bool sym, unsigned int* __restrict__ flags) {
     const size_t off = (size_t)blockIdx.z * (size_t)bstride;
     U += off;
     if (L) L += off;
@@ -62,6 +62,10 @@ k_validate(const T* __restrict__ U, const T* __restrict__ L, int n, int ld, long
         for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
             f |= check_value(U[(size_t)i * ld + j], false, i == j);
             if (L) f |= check_value(L[(size_t)i * ld + j], true, i == j);
+            if (sym && j > i) {
+                if (!(U[(size_t)i * ld + j] == U[(size_t)j * ld + i])) f |= VF_ASYM;
+                if (L && !(L[(size_t)i * ld + j] == L[(size_t)j * ld + i])) f |= VF_ASYM;
+            }
         }
     }
     f = __reduce_or_sync(0xffffffffu, f);
@@ -99,7 +103,7 @@ static cudaError_t validate_t(const Mats& m, unsigned int* flags, cudaStream_t s
         before_launch(s, PH_ROUND);
         k_validate<T><<<pass_grid(m.n, nbz), 256, 0, s>>>(
             static_cast<const T*>(m.U) + o, m.L ? static_cast<const T*>(m.L) + o : nullptr,
-            m.n, m.ld, m.bstride, flags);
+            m.n, m.ld, m.bstride, m.sym, flags);
         after_launch(s, PH_ROUND);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -84,8 +84,14 @@ enum {
     /* Blocked-mode schedule knobs; every setting gives identical results. */
     BS_TILE_64 = 1 << 5,      /* force 64 x 64 tiles (default: chosen from n) */
     BS_TILE_128 = 1 << 6,     /* force 128 x 128 tiles; both tile bits: BS_ERR_ARG */
-    BS_NO_LOOKAHEAD = 1 << 7  /* run the three phases of each block round in
+    BS_NO_LOOKAHEAD = 1 << 7, /* run the three phases of each block round in
                                  sequence on `stream` only (see below) */
+    BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
+                                 stored, section 6): only tiles on and above the
+                                 diagonal are computed, each mirrored into its
+                                 transpose -- about half the work, same output.
+                                 With BS_PERK: BS_ERR_ARG.  With BS_VALIDATE,
+                                 asymmetric input returns BS_ERR_INPUT. */
 };
 
 /* Upper bounds only (min-plus all-pairs shortest paths, section 3's loop).

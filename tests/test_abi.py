@@ -73,6 +73,7 @@ FAKE2 = ctypes.c_void_p(2 << 20)
     ((FAKE, FAKE2, 8, 8, None, 2), bsm.BS_ERR_ARG),                       # unknown dtype
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_RULE_LITERAL), bsm.BS_ERR_ARG),     # literal needs per-round
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_TILE_64 | bsm.BS_TILE_128), bsm.BS_ERR_ARG),
+    ((FAKE, FAKE2, 8, 8, None, bsm.BS_PERK | bsm.BS_SYMMETRIC), bsm.BS_ERR_ARG),
     ((None, FAKE2, 8, 8, None, 0), bsm.BS_ERR_ARG),                       # null U
     ((FAKE, None, 8, 8, None, 0), bsm.BS_ERR_ARG),                        # null L
     ((FAKE, FAKE, 8, 8, None, 0), bsm.BS_ERR_ARG),                        # U aliases L

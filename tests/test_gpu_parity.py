@@ -42,6 +42,7 @@ SCHEDULES = {
     "t128": bsm.BS_TILE_128,
     "t64_serial": bsm.BS_TILE_64 | bsm.BS_NO_LOOKAHEAD,
     "t128_serial": bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD,
+    "sym": bsm.BS_SYMMETRIC,
 }
 
 
@@ -69,6 +70,28 @@ def test_blocked_matches_oracle(n, dtype, sched):
     Ug, Lg, ok = gpu_bounds(U0, L0, SCHEDULES[sched])
     assert ok
     assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
+@pytest.mark.parametrize("n", [1, 2, 5, 63, 64, 65, 127, 129, 257, 300, 513])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "t64_serial", "t128_serial"])
+def test_symmetric_mode_matches_oracle(n, dtype, sched):
+    """Half the tiles computed and mirrored: bit-identical to the oracle."""
+    Uq, Lq = W.random_bounds(n, 2500 + n, p_known=0.2, p_bad=0.02)
+    U0, L0 = as_dtype(Uq, Lq, dtype)
+    Uo, Lo = oracle.smooth(U0, L0)
+    Ug, Lg, ok = gpu_bounds(U0, L0, SCHEDULES[sched] | bsm.BS_SYMMETRIC, ld=n + 4)
+    assert ok
+    assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
+@pytest.mark.parametrize("n", [65, 300])
+@pytest.mark.parametrize("algo", ["t64", "t128"])
+def test_symmetric_upper_only(n, algo):
+    Uq, _ = W.random_bounds(n, 5500 + n, p_known=0.25)
+    Uo = oracle.smooth_upper(Uq)
+    Ug, ok = gpu_upper(Uq, SCHEDULES[algo] | bsm.BS_SYMMETRIC, ld=n + 1)
+    assert ok and same_bits(Ug, Uo)
 
 
 @pytest.mark.parametrize("n", [129, 300])
@@ -162,10 +185,10 @@ def test_fp32_off_grid_within_tolerance():
 
 
 @pytest.mark.parametrize("idx", [0, 1])
-@pytest.mark.parametrize("algo", ["blocked", "perk"])
+@pytest.mark.parametrize("algo", ["blocked", "perk", "symmetric"])
 def test_chain_configs(idx, algo):
     m = W.make_config(idx)
-    flags = bsm.BS_PERK if algo == "perk" else 0
+    flags = {"blocked": 0, "perk": bsm.BS_PERK, "symmetric": bsm.BS_SYMMETRIC}[algo]
     for U0, L0 in ((W.to_f32(m["U"]), W.to_f32(m["L"])), (m["U"], m["L"])):
         Uo, Lo = oracle.smooth(U0, L0)
         Ug, Lg, ok = gpu_bounds(U0, L0, flags)
@@ -180,7 +203,7 @@ def globule4096():
     return m, Uo, Lo
 
 
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial", "sym"])
 def test_globule_4096_int32_blocked(globule4096, sched):
     m, Uo, Lo = globule4096
     Ug, Lg, ok = gpu_bounds(m["U"], m["L"], SCHEDULES[sched])
@@ -202,7 +225,7 @@ def test_globule_4096_fp32_blocked_and_per_round(globule4096):
         assert bsm.bs_check_feasible(dev(Ug), dev(Lg)) == expect_flags
 
 
-@pytest.mark.parametrize("sched", ["auto", "t128"])
+@pytest.mark.parametrize("sched", ["auto", "t128", "sym"])
 def test_batched_chains(sched):
     """Batch of 256 molecules n=512 in one call; every 32nd molecule against the
     oracle, all molecules against a per-molecule GPU call."""
@@ -245,17 +268,24 @@ def test_batched_per_round_and_strided():
             assert np.all(Uh[b * stride + n * ld: (b + 1) * stride] == -1.0)
 
 
-def test_globule_16384_sampled_rows():
+@pytest.fixture(scope="module")
+def globule16384():
+    """n = 16384 globule and the oracle's shortest-path rows for six sources."""
+    m = W.make_config(4)
+    rows = np.array([0, 1, 4097, 8191, 12000, m["n"] - 1])
+    Ur, Lr = oracle.closure_rows(m["U"], m["L"], rows)
+    return m, rows, Ur, Lr
+
+
+@pytest.mark.parametrize("sched", ["auto", "sym"])
+def test_globule_16384_sampled_rows(globule16384, sched):
     """n = 16384, fp32, blocked, as timed by the benchmark: sampled rows
     against the oracle's shortest-path rows, plus properties of every cell."""
-    m = W.make_config(4)
-    n = m["n"]
+    m, rows, Ur, Lr = globule16384
     t = torch()
     U, L = dev(W.to_f32(m["U"])), dev(W.to_f32(m["L"]))
-    bsm.bs_smooth_bounds(U, L)
+    bsm.bs_smooth_bounds(U, L, flags=SCHEDULES[sched])
     t.cuda.synchronize()
-    rows = np.array([0, 1, 4097, 8191, 12000, n - 1])
-    Ur, Lr = oracle.closure_rows(m["U"], m["L"], rows)
     Ug = U[t.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64) * 1024
     Lg = L[t.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64) * 1024
     assert np.array_equal(Ug, Ur) and np.array_equal(Lg, Lr)
@@ -297,6 +327,18 @@ def test_validate_flag(dtype):
         with pytest.raises(bsm.BSError) as e:
             bsm.bs_smooth_bounds(dev(u), dev(l), flags=bsm.BS_VALIDATE)
         assert e.value.status == code
+
+
+def test_symmetric_flag_checks():
+    """BS_VALIDATE rejects asymmetric input in symmetric mode."""
+    Uq, Lq = W.random_bounds(40, 9100, p_bad=0.02, symmetric=False)
+    U, L = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
+    with pytest.raises(bsm.BSError) as e:
+        bsm.bs_smooth_bounds(U, L, flags=bsm.BS_SYMMETRIC | bsm.BS_VALIDATE)
+    assert e.value.status == bsm.BS_ERR_INPUT
+    Us, Ls = W.random_bounds(40, 9101, p_bad=0.02)
+    bsm.bs_smooth_bounds(dev(W.to_f32(Us)), dev(W.to_f32(Ls)),
+                         flags=bsm.BS_SYMMETRIC | bsm.BS_VALIDATE)
 
 
 def test_literal_rule_rejected_in_blocked_mode():
