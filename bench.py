@@ -195,6 +195,22 @@ def dist_setup():
     return ws, rank, local
 
 
+def aggregate(ms, units, device="cpu"):
+    """Whole-job figures over ranks: (max time over ranks, units summed over
+    ranks).  Each rank smooths its own replica (the path has no exchange step),
+    so the job rate is the summed units over the slowest rank's time.  Without
+    an initialised multi-rank process group the local values come back."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms), float(units)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 # ------------------------------------------------------------------ oracle leg
 
 
@@ -334,14 +350,12 @@ def main():
         prof = bsm.bs_profile_end()
     launches = bsm.bs_launch_count() - launches0
     total_ms = t_start.elapsed_time(t_end)
+    cells = float(n) ** 3
+    total_ms, units = aggregate(total_ms, args.steps * cells, device="cuda")
     if ws > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    cells = float(n) ** 3
-    value = ws * args.steps * cells / (total_ms * 1e-3)
+    value = units / (total_ms * 1e-3)
 
     # parity of the timed output: the stored result is the fixed point, so one
     # more smoothing must leave it unchanged and the flags must be zero
@@ -538,13 +552,9 @@ def e2e_leg(torch, bsm, U0, L0, args, ws):
         oL.copy_(dL, non_blocking=True)
     t1.record()
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, units = aggregate(t0.elapsed_time(t1), steps * float(n) ** 3, device="cuda")
     nbytes = 2 * n * n * 4
-    return {"value": ws * steps * float(n) ** 3 / (ms * 1e-3), "unit": UNIT,
+    return {"value": units / (ms * 1e-3), "unit": UNIT,
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": steps,
             "ms_per_step": ms / steps}
 
