@@ -43,6 +43,74 @@ __device__ __forceinline__ void cp_async_wait() {
 
 }  // namespace
 
+// ---------------------------------------------------------------- paired middle atoms
+
+// Cell updates for a pair of middle atoms (k, k+1).
+//   a, al : (U[i,k], U[i,k+1]), (L[i,k], L[i,k+1])   -- row i of the thread
+//   b, bl : (U[k,j], U[k+1,j]), (L[k,j], L[k+1,j])   -- column j of the thread
+template <class T> struct PairOps;
+
+template <> struct PairOps<float> {
+    using P = unsigned long long;   // two fp32 lanes: low = k, high = k+1
+    static __device__ __forceinline__ void upper(float& u, P a, P b) {
+        asm("{\n\t.reg .b64 s;\n\t.reg .f32 s0, s1;\n\t"
+            "add.rn.f32x2 s, %1, %2;\n\t"
+            "mov.b64 {s0, s1}, s;\n\t"
+            "min.f32 %0, %0, s0, s1;\n\t}"
+            : "+f"(u) : "l"(a), "l"(b));
+    }
+    // L = max(L, L[k,j] - U[i,k], L[i,k] - U[k,j]) over both k
+    static __device__ __forceinline__ void lower(float& l, P a, P al, P b, P bl) {
+        asm("{\n\t.reg .b64 d1, d2;\n\t.reg .f32 x0, x1, y0, y1;\n\t"
+            "sub.rn.f32x2 d1, %1, %3;\n\t"
+            "sub.rn.f32x2 d2, %2, %4;\n\t"
+            "mov.b64 {x0, x1}, d1;\n\t"
+            "mov.b64 {y0, y1}, d2;\n\t"
+            "max.f32 %0, %0, x0, x1;\n\t"
+            "max.f32 %0, %0, y0, y1;\n\t}"
+            : "+f"(l) : "l"(bl), "l"(al), "l"(a), "l"(b));
+    }
+};
+
+template <> struct PairOps<int> {
+    using P = int2;
+    static __device__ __forceinline__ void upper(int& u, P a, P b) {
+        u = __viaddmin_s32(a.x, b.x, u);
+        u = __viaddmin_s32(a.y, b.y, u);
+    }
+    // na, nb: negated a, b
+    static __device__ __forceinline__ void lower(int& l, P na, P al, P nb, P bl) {
+        l = __viaddmax_s32(bl.x, na.x, l);
+        l = __viaddmax_s32(bl.y, na.y, l);
+        l = __viaddmax_s32(al.x, nb.x, l);
+        l = __viaddmax_s32(al.y, nb.y, l);
+    }
+};
+
+template <class T> struct PairLoad;
+template <> struct PairLoad<float> {
+    using P = unsigned long long;
+    static __device__ __forceinline__ P ld2(const float* p) {
+        return *reinterpret_cast<const unsigned long long*>(p);
+    }
+    static __device__ __forceinline__ void ld4(const float* p, P& x, P& y) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
+        x = v.x;
+        y = v.y;
+    }
+    static __device__ __forceinline__ P neg(P x) { return x; }
+};
+template <> struct PairLoad<int> {
+    using P = int2;
+    static __device__ __forceinline__ P ld2(const int* p) { return *reinterpret_cast<const int2*>(p); }
+    static __device__ __forceinline__ void ld4(const int* p, P& x, P& y) {
+        const int4 v = *reinterpret_cast<const int4*>(p);
+        x = make_int2(v.x, v.y);
+        y = make_int2(v.z, v.w);
+    }
+    static __device__ __forceinline__ P neg(P x) { return make_int2(-x.x, -x.y); }
+};
+
 // ---------------------------------------------------------------- phase 1
 
 template <class T, bool HAS_L, int FB>
@@ -96,8 +164,204 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
 }
 
 // ---------------------------------------------------------------- phase 2
+//
+// Panels of block round K against the finished diagonal tile D = (K,K), two
+// middle atoms (k, k+1) per barrier.  Row k and row k+1 of a row-panel tile
+// (columns k and k+1 of a column-panel tile) belong to one thread: it applies
+// step k to line k+1 from its own registers and publishes the pair (line k,
+// line k+1 after step k).  Every cell then takes both steps with the paired
+// instructions of phase 3 -- the same sums and the same exact min/max as two
+// sequential steps.
+//   row panel (K,P):   b = (U[k,j], U'[k+1,j]),      a = (D_U[i,k], D_U[i,k+1])
+//   column panel (P,K): a = (U[i,k], U'[i,k+1]),      b = (D_U[k,j], D_U[k+1,j])
+//                       al = the column values raised by the closure rule.
+// D is staged as [i][k] (row panel) or k-interleaved [k/2][j][k%2] (column
+// panel), so each operand pair is one 8-byte load.  An odd last step pairs
+// with a padding line, which changes nothing.
 
-constexpr int DPAD = 1;   // diagonal tile row stride FB + DPAD in shared memory
+constexpr int DPAD = 2;   // diagonal tile row stride FB + DPAD: even, so pairs stay aligned
+
+// Row panel: the owner of rows k, k+1 publishes (row k, row k+1 after step k).
+template <class T, bool HAS_L, int FB>
+__device__ __forceinline__ void p2_publish_rows(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
+                                                const T* dU, const T* dL, T* sU, T* sL) {
+    using E = El<T>;
+    constexpr int DS = FB + DPAD;
+    const int r0 = mt_row0<FB>();
+#pragma unroll
+    for (int rr = 0; rr < TM; rr += 2) {
+        if (r0 + rr != k) continue;
+        const T a1 = dU[(k + 1) * DS + k];
+        const T al1 = HAS_L ? dL[(k + 1) * DS + k] : T(0);
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const int j = mt_col<FB>(c);
+            sU[2 * j] = u[rr][c];
+            sU[2 * j + 1] = E::mn(u[rr + 1][c], E::add(a1, u[rr][c]));
+            if (HAS_L) {
+                sL[2 * j] = l[rr][c];
+                sL[2 * j + 1] = E::mx(l[rr + 1][c], E::mx(E::sub(l[rr][c], a1), E::sub(al1, u[rr][c])));
+            }
+        }
+    }
+}
+
+// Column panel: the owner of columns k, k+1 publishes, per row, (U[i,k],
+// U'[i,k+1]) and the closure-raised column values (Lc_k[i], Lc_k+1[i]).
+// dU, dL: the diagonal tile, k-interleaved.
+template <class T, bool HAS_L, int FB>
+__device__ __forceinline__ void p2_publish_cols(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
+                                                const T* dU, const T* dL, T* sU, T* sL) {
+    using E = El<T>;
+    const int r0 = mt_row0<FB>();
+#pragma unroll
+    for (int c = 0; c < TN; c += 2) {
+        if (mt_col<FB>(c) != k) continue;
+        const int kb = (k >> 1) * (2 * FB);
+        const T ukk1 = dU[kb + 2 * (k + 1)];                        // D[k][k+1]
+        const T lkk = HAS_L ? dL[kb + 2 * k] : T(0);                // D[k][k]
+        const T lkk1 = HAS_L ? dL[kb + 2 * (k + 1)] : T(0);         // D[k][k+1]
+        const T lk1k1 = HAS_L ? dL[kb + 2 * (k + 1) + 1] : T(0);    // D[k+1][k+1]
+#pragma unroll
+        for (int r = 0; r < TM; ++r) {
+            const T uk = u[r][c];
+            const T u1 = E::mn(u[r][c + 1], E::add(uk, ukk1));
+            sU[2 * (r0 + r)] = uk;
+            sU[2 * (r0 + r) + 1] = u1;
+            if (HAS_L) {
+                const T lc0 = E::mx(l[r][c], E::sub(lkk, uk));
+                const T l1 = E::mx(l[r][c + 1], E::mx(E::sub(lkk1, uk), E::sub(lc0, ukk1)));
+                sL[2 * (r0 + r)] = lc0;
+                sL[2 * (r0 + r) + 1] = E::mx(l1, E::sub(lk1k1, u1));
+            }
+        }
+    }
+}
+
+template <class T, bool HAS_L, int FB>
+__device__ __forceinline__ void p2_row_panel(T* U, T* L, size_t ld, int o, int op, int mk,
+                                             int mp, bool vec, bool sym, T* dU, T* dL,
+                                             T (*sU)[2 * FB], T (*sL)[2 * FB]) {
+    using E = El<T>;
+    using LD = PairLoad<T>;
+    using P = typename LD::P;
+    constexpr bool NEG = std::is_same<T, int>::value;
+    constexpr int DS = FB + DPAD;
+    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
+    T* Ut = U + (size_t)o * ld + op;
+    T* Lt = HAS_L ? L + (size_t)o * ld + op : nullptr;
+    T u[TM][TN], l[TM][TN];
+    load_tile<FB>(u, Ut, ld, mk, mp, vec, E::upad());
+    if (HAS_L) load_tile<FB>(l, Lt, ld, mk, mp, vec, E::lpad());
+
+    p2_publish_rows<T, HAS_L, FB>(u, l, 0, dU, dL, sU[0], sL[0]);
+    __syncthreads();
+#pragma unroll 1
+    for (int k = 0; k < mk; k += 2) {
+        const int b = (k >> 1) & 1;
+        P a[TM], al[TM], bb[TN], bl[TN];
+#pragma unroll
+        for (int r = 0; r < TM; ++r) {
+            a[r] = LD::ld2(dU + (r0 + r) * DS + k);
+            if (HAS_L) al[r] = LD::ld2(dL + (r0 + r) * DS + k);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int jb = (h * (FB / 2) + cq) * 2;
+            LD::ld4(&sU[b][jb], bb[h * 4 + 0], bb[h * 4 + 1]);
+            LD::ld4(&sU[b][jb + 4], bb[h * 4 + 2], bb[h * 4 + 3]);
+            if (HAS_L) {
+                LD::ld4(&sL[b][jb], bl[h * 4 + 0], bl[h * 4 + 1]);
+                LD::ld4(&sL[b][jb + 4], bl[h * 4 + 2], bl[h * 4 + 3]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+            for (int q = 0; q < TN; ++q) PairOps<T>::upper(u[r][q], a[r], bb[q]);
+        if (HAS_L) {
+            if (NEG) {
+#pragma unroll
+                for (int r = 0; r < TM; ++r) a[r] = LD::neg(a[r]);
+#pragma unroll
+                for (int q = 0; q < TN; ++q) bb[q] = LD::neg(bb[q]);
+            }
+#pragma unroll
+            for (int r = 0; r < TM; ++r)
+#pragma unroll
+                for (int q = 0; q < TN; ++q) PairOps<T>::lower(l[r][q], a[r], al[r], bb[q], bl[q]);
+        }
+        if (k + 2 < mk) p2_publish_rows<T, HAS_L, FB>(u, l, k + 2, dU, dL, sU[b ^ 1], sL[b ^ 1]);
+        __syncthreads();
+    }
+    store_tile<FB>(u, Ut, ld, mk, mp, vec);
+    if (HAS_L) store_tile<FB>(l, Lt, ld, mk, mp, vec);
+    if (sym) {
+        // symmetric inputs: the column panel tile (P, K) is the transpose
+        store_tile_t<FB>(u, U + (size_t)op * ld + o, ld, mk, mp, vec);
+        if (HAS_L) store_tile_t<FB>(l, L + (size_t)op * ld + o, ld, mk, mp, vec);
+    }
+}
+
+template <class T, bool HAS_L, int FB>
+__device__ __forceinline__ void p2_col_panel(T* U, T* L, size_t ld, int o, int op, int mk,
+                                             int mp, bool vec, T* dU, T* dL,
+                                             T (*sU)[2 * FB], T (*sL)[2 * FB]) {
+    using E = El<T>;
+    using LD = PairLoad<T>;
+    using P = typename LD::P;
+    constexpr bool NEG = std::is_same<T, int>::value;
+    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
+    T* Ut = U + (size_t)op * ld + o;
+    T* Lt = HAS_L ? L + (size_t)op * ld + o : nullptr;
+    T u[TM][TN], l[TM][TN];
+    load_tile<FB>(u, Ut, ld, mp, mk, vec, E::upad());
+    if (HAS_L) load_tile<FB>(l, Lt, ld, mp, mk, vec, E::lpad());
+
+    p2_publish_cols<T, HAS_L, FB>(u, l, 0, dU, dL, sU[0], sL[0]);
+    __syncthreads();
+#pragma unroll 1
+    for (int k = 0; k < mk; k += 2) {
+        const int b = (k >> 1) & 1;
+        P a[TM], al[TM], bb[TN], bl[TN];
+#pragma unroll
+        for (int r = 0; r < TM; ++r) {
+            a[r] = LD::ld2(&sU[b][2 * (r0 + r)]);
+            if (HAS_L) al[r] = LD::ld2(&sL[b][2 * (r0 + r)]);
+        }
+        const int bo = (k >> 1) * (2 * FB);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int jb = bo + (h * (FB / 2) + cq) * 2;
+            LD::ld4(dU + jb, bb[h * 4 + 0], bb[h * 4 + 1]);
+            LD::ld4(dU + jb + 4, bb[h * 4 + 2], bb[h * 4 + 3]);
+            if (HAS_L) {
+                LD::ld4(dL + jb, bl[h * 4 + 0], bl[h * 4 + 1]);
+                LD::ld4(dL + jb + 4, bl[h * 4 + 2], bl[h * 4 + 3]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+            for (int q = 0; q < TN; ++q) PairOps<T>::upper(u[r][q], a[r], bb[q]);
+        if (HAS_L) {
+            if (NEG) {
+#pragma unroll
+                for (int r = 0; r < TM; ++r) a[r] = LD::neg(a[r]);
+#pragma unroll
+                for (int q = 0; q < TN; ++q) bb[q] = LD::neg(bb[q]);
+            }
+#pragma unroll
+            for (int r = 0; r < TM; ++r)
+#pragma unroll
+                for (int q = 0; q < TN; ++q) PairOps<T>::lower(l[r][q], a[r], al[r], bb[q], bl[q]);
+        }
+        if (k + 2 < mk) p2_publish_cols<T, HAS_L, FB>(u, l, k + 2, dU, dL, sU[b ^ 1], sL[b ^ 1]);
+        __syncthreads();
+    }
+    store_tile<FB>(u, Ut, ld, mp, mk, vec);
+    if (HAS_L) store_tile<FB>(l, Lt, ld, mp, mk, vec);
+}
 
 template <class T, bool HAS_L, int FB>
 __global__ void __launch_bounds__(TileShape<FB>::NT)
@@ -109,7 +373,8 @@ k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* dU = reinterpret_cast<T*>(smem_raw);
     T* dL = dU + FB * DS;
-    __shared__ T sU[2][FB], sL[2][FB];
+    __shared__ __align__(16) T sU[2][2 * FB];
+    __shared__ __align__(16) T sL[2][2 * FB];
 
     const size_t off = (size_t)blockIdx.z * (size_t)bstride;
     U += off;
@@ -121,81 +386,20 @@ k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     const int mp = min(FB, n - op);
     const bool row_panel = blockIdx.y == 0;
 
-    // the finished diagonal tile, padded
+    // the finished diagonal tile, padded: [i][k] for the row panel,
+    // k-interleaved [k/2][j][k%2] for the column panel
     for (int e = threadIdx.x; e < FB * FB; e += NT) {
         const int i = e / FB, j = e % FB;
         const bool in = i < mk && j < mk;
-        dU[i * DS + j] = in ? U[(size_t)(o + i) * ld + o + j] : E::upad();
-        if (HAS_L) dL[i * DS + j] = in ? L[(size_t)(o + i) * ld + o + j] : E::lpad();
+        const int d = row_panel ? i * DS + j : (i >> 1) * (2 * FB) + 2 * j + (i & 1);
+        dU[d] = in ? U[(size_t)(o + i) * ld + o + j] : E::upad();
+        if (HAS_L) dL[d] = in ? L[(size_t)(o + i) * ld + o + j] : E::lpad();
     }
-
-    const int r0 = mt_row0<FB>();
-    T u[TM][TN], l[TM][TN];
-    if (row_panel) {
-        // tile (K, P): rows of block K, columns of block P
-        T* Ut = U + (size_t)o * ld + op;
-        T* Lt = HAS_L ? L + (size_t)o * ld + op : nullptr;
-        load_tile<FB>(u, Ut, ld, mk, mp, vec, E::upad());
-        if (HAS_L) load_tile<FB>(l, Lt, ld, mk, mp, vec, E::lpad());
-        publish_row<FB, T, HAS_L>(u, l, 0, sU[0], sL[0]);
-        __syncthreads();
-        for (int k = 0; k < mk; ++k) {
-            const int b = k & 1;
-            T a[TM], al[TM], bb[TN], bl[TN];
-#pragma unroll
-            for (int r = 0; r < TM; ++r) {
-                a[r] = dU[(r0 + r) * DS + k];
-                al[r] = HAS_L ? dL[(r0 + r) * DS + k] : T(0);
-            }
-#pragma unroll
-            for (int c = 0; c < TN; ++c) {
-                bb[c] = sU[b][mt_col<FB>(c)];
-                bl[c] = HAS_L ? sL[b][mt_col<FB>(c)] : T(0);
-            }
-            fw_update<T, HAS_L>(u, l, a, al, bb, bl);
-            if (k + 1 < mk) publish_row<FB, T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
-            __syncthreads();
-        }
-        store_tile<FB>(u, Ut, ld, mk, mp, vec);
-        if (HAS_L) store_tile<FB>(l, Lt, ld, mk, mp, vec);
-        if (sym) {
-            // symmetric inputs: the column panel tile (P, K) is the transpose
-            store_tile_t<FB>(u, U + (size_t)op * ld + o, ld, mk, mp, vec);
-            if (HAS_L) store_tile_t<FB>(l, L + (size_t)op * ld + o, ld, mk, mp, vec);
-        }
-    } else {
-        // tile (P, K): rows of block P, columns of block K
-        T* Ut = U + (size_t)op * ld + o;
-        T* Lt = HAS_L ? L + (size_t)op * ld + o : nullptr;
-        load_tile<FB>(u, Ut, ld, mp, mk, vec, E::upad());
-        if (HAS_L) load_tile<FB>(l, Lt, ld, mp, mk, vec, E::lpad());
-        publish_col<FB, T, HAS_L>(u, l, 0, sU[0], sL[0]);
-        __syncthreads();
-        for (int k = 0; k < mk; ++k) {
-            const int b = k & 1;
-            T a[TM], al[TM], bb[TN], bl[TN];
-#pragma unroll
-            for (int r = 0; r < TM; ++r) {
-                a[r] = sU[b][r0 + r];
-                al[r] = HAS_L ? sL[b][r0 + r] : T(0);
-            }
-#pragma unroll
-            for (int c = 0; c < TN; ++c) {
-                bb[c] = dU[k * DS + mt_col<FB>(c)];
-                bl[c] = HAS_L ? dL[k * DS + mt_col<FB>(c)] : T(0);
-            }
-            if (HAS_L) {
-                const T lkk = dL[k * DS + k];
-#pragma unroll
-                for (int r = 0; r < TM; ++r) al[r] = E::mx(al[r], E::sub(lkk, a[r]));
-            }
-            fw_update<T, HAS_L>(u, l, a, al, bb, bl);
-            if (k + 1 < mk) publish_col<FB, T, HAS_L>(u, l, k + 1, sU[b ^ 1], sL[b ^ 1]);
-            __syncthreads();
-        }
-        store_tile<FB>(u, Ut, ld, mp, mk, vec);
-        if (HAS_L) store_tile<FB>(l, Lt, ld, mp, mk, vec);
-    }
+    __syncthreads();
+    if (row_panel)
+        p2_row_panel<T, HAS_L, FB>(U, L, ld, o, op, mk, mp, vec, sym, dU, dL, sU, sL);
+    else
+        p2_col_panel<T, HAS_L, FB>(U, L, ld, o, op, mk, mp, vec, dU, dL, sU, sL);
 }
 
 // ---------------------------------------------------------------- phase 3
@@ -290,72 +494,6 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
         }
     }
 }
-
-// Cell updates for a pair of middle atoms (k, k+1).
-//   a, al : (U[i,k], U[i,k+1]), (L[i,k], L[i,k+1])   -- row i of the thread
-//   b, bl : (U[k,j], U[k+1,j]), (L[k,j], L[k+1,j])   -- column j of the thread
-template <class T> struct PairOps;
-
-template <> struct PairOps<float> {
-    using P = unsigned long long;   // two fp32 lanes: low = k, high = k+1
-    static __device__ __forceinline__ void upper(float& u, P a, P b) {
-        asm("{\n\t.reg .b64 s;\n\t.reg .f32 s0, s1;\n\t"
-            "add.rn.f32x2 s, %1, %2;\n\t"
-            "mov.b64 {s0, s1}, s;\n\t"
-            "min.f32 %0, %0, s0, s1;\n\t}"
-            : "+f"(u) : "l"(a), "l"(b));
-    }
-    // L = max(L, L[k,j] - U[i,k], L[i,k] - U[k,j]) over both k
-    static __device__ __forceinline__ void lower(float& l, P a, P al, P b, P bl) {
-        asm("{\n\t.reg .b64 d1, d2;\n\t.reg .f32 x0, x1, y0, y1;\n\t"
-            "sub.rn.f32x2 d1, %1, %3;\n\t"
-            "sub.rn.f32x2 d2, %2, %4;\n\t"
-            "mov.b64 {x0, x1}, d1;\n\t"
-            "mov.b64 {y0, y1}, d2;\n\t"
-            "max.f32 %0, %0, x0, x1;\n\t"
-            "max.f32 %0, %0, y0, y1;\n\t}"
-            : "+f"(l) : "l"(bl), "l"(al), "l"(a), "l"(b));
-    }
-};
-
-template <> struct PairOps<int> {
-    using P = int2;
-    static __device__ __forceinline__ void upper(int& u, P a, P b) {
-        u = __viaddmin_s32(a.x, b.x, u);
-        u = __viaddmin_s32(a.y, b.y, u);
-    }
-    // na, nb: negated a, b
-    static __device__ __forceinline__ void lower(int& l, P na, P al, P nb, P bl) {
-        l = __viaddmax_s32(bl.x, na.x, l);
-        l = __viaddmax_s32(bl.y, na.y, l);
-        l = __viaddmax_s32(al.x, nb.x, l);
-        l = __viaddmax_s32(al.y, nb.y, l);
-    }
-};
-
-template <class T> struct PairLoad;
-template <> struct PairLoad<float> {
-    using P = unsigned long long;
-    static __device__ __forceinline__ P ld2(const float* p) {
-        return *reinterpret_cast<const unsigned long long*>(p);
-    }
-    static __device__ __forceinline__ void ld4(const float* p, P& x, P& y) {
-        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
-        x = v.x;
-        y = v.y;
-    }
-    static __device__ __forceinline__ P neg(P x) { return x; }
-};
-template <> struct PairLoad<int> {
-    using P = int2;
-    static __device__ __forceinline__ P ld2(const int* p) { return *reinterpret_cast<const int2*>(p); }
-    static __device__ __forceinline__ void ld4(const int* p, P& x, P& y) {
-        const int4 v = *reinterpret_cast<const int4*>(p);
-        x = make_int2(v.x, v.y);
-        y = make_int2(v.z, v.w);
-    }
-    static __device__ __forceinline__ P neg(P x) { return make_int2(-x.x, -x.y); }
-};
 
 // Which tiles a phase-3 launch covers (block round K, nb tile rows):
 //   P3_ALL  : every tile outside block-row K and block-column K;
