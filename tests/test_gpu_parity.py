@@ -162,23 +162,44 @@ def test_feasibility_count_example_c():
         assert bsm.bs_check_feasible(U, L) == expect
 
 
-def test_fp32_off_grid_within_tolerance():
-    """Values off the 1/1024 grid: fp32 blocked vs the fp64 oracle within
-    1e-4 A absolute or 1e-5 relative, per cell."""
-    rng = np.random.default_rng(7)
-    n = 300
-    Uq, Lq = W.random_bounds(n, 7000, p_known=0.3, p_bad=0.0)
+def off_grid(n, seed, p_bad, symmetric=True):
+    """Bounds with values off the 1/1024 grid (fp32), optionally inverted pairs."""
+    rng = np.random.default_rng(seed)
+    Uq, Lq = W.random_bounds(n, seed, p_known=0.3, p_bad=p_bad, symmetric=symmetric)
     U0 = (Uq / 1024.0 + rng.random((n, n)) * 1e-3).astype(np.float32)
     L0 = np.maximum(Lq / 1024.0 - rng.random((n, n)) * 1e-3, 0).astype(np.float32)
-    U0 = np.minimum(U0, U0.T)
-    L0 = np.minimum(L0, L0.T)
+    if symmetric:
+        U0 = np.minimum(U0, U0.T)
+        L0 = np.minimum(L0, L0.T)
     np.fill_diagonal(U0, 0)
     np.fill_diagonal(L0, 0)
+    return U0, L0
+
+
+@pytest.mark.parametrize("n,p_bad", [(300, 0.0), (300, 0.02), (700, 0.01)])
+@pytest.mark.parametrize("sched", ["t64", "t128", "sym"])
+def test_fp32_off_grid_within_tolerance(n, p_bad, sched):
+    """Off the 1/1024 grid fp32 sums round, so the schedule changes the last
+    bits.  Against the fp64 oracle on the same fp32 inputs:
+      * the stated gate: |g - o| <= 1e-4 A or <= 1e-5 |o|, every cell;
+      * U: a computed upper bound is the fp32 sum of the edges of one path of
+        at most n-1 edges, each add rounding to nearest, so
+        |g - o| <= (n-1) 2^-24 o;
+      * the L > U flags agree wherever |L - U| exceeds the tolerance."""
+    U0, L0 = off_grid(n, 7000 + n, p_bad)
     Uo, Lo = oracle.smooth(U0.astype(np.float64), L0.astype(np.float64))
-    Ug, Lg, ok = gpu_bounds(U0, L0)
+    Ug, Lg, ok = gpu_bounds(U0, L0, SCHEDULES[sched])
+    assert ok
     for g, o in ((Ug, Uo), (Lg, Lo)):
         err = np.abs(g.astype(np.float64) - o)
         assert np.all((err <= 1e-4) | (err <= 1e-5 * np.abs(o)))
+    assert np.all(np.abs(Ug - Uo) <= (n - 1) * 2.0 ** -24 * Uo + 1e-30)
+    margin = np.abs(Lo - Uo)
+    clear = margin > 2e-4 + 2e-5 * np.maximum(np.abs(Lo), np.abs(Uo))
+    assert np.array_equal((Lg > Ug)[clear], (Lo > Uo)[clear])
+    # the fp32 round-by-round oracle differs from fp64 by rounding only as well
+    Uf, Lf = oracle.smooth(U0, L0)
+    assert np.max(np.abs(Uf.astype(np.float64) - Uo)) <= np.max(Uo) * (n - 1) * 2.0 ** -24
 
 
 # ------------------------------------------------------------------ benchmark molecules
