@@ -55,7 +55,7 @@ def tile_size(n, flags=0):
         return 64
     if flags & (1 << 6):
         return 128
-    return 64 if n <= 1536 else 128
+    return 64 if n <= 3072 else 128
 
 
 def phase_cells(n, fb, sym=False):
@@ -430,13 +430,16 @@ def main():
     return 0
 
 
-SCHEDULE_FLAGS = {"auto": 0, "t64": 1 << 5, "t128": 1 << 6, "t64_serial": (1 << 5) | (1 << 7),
-                  "t128_serial": (1 << 6) | (1 << 7), "perk": 1 << 2, "sym": 1 << 8}
+SCHEDULE_FLAGS = {"auto": 0, "t64": (1 << 5) | (1 << 9), "t128": (1 << 6) | (1 << 9),
+                  "t64_serial": (1 << 5) | (1 << 7), "t128_serial": (1 << 6) | (1 << 7),
+                  "perk": 1 << 2, "sym": 1 << 8}
 ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial", "sym")
 SWEEP = (
-    # (config, dtype, schedules, description)
+    # (config, dtype, schedules, description); config None: random bounds of size n
     (0, "f32", ALL_SCHEDULES, "chain n=256"),
     (1, "f32", ALL_SCHEDULES, "chain n=1000"),
+    (("random", 2048), "f32", ALL_SCHEDULES, "random bounds n=2048"),
+    (("random", 3000), "f32", ("auto", "t64", "t128", "t128_serial"), "random bounds n=3000"),
     (2, "f32", ALL_SCHEDULES + ("perk",), "globule n=4096"),
     (2, "i32", ("auto",), "globule n=4096"),
     (3, "f32", ALL_SCHEDULES, "256 chains n=512, batched"),
@@ -458,7 +461,12 @@ def sweep(args):
         for algo in scheds:
             if cfg not in cache:
                 cache.clear()
-                cache[cfg] = make_config(cfg)
+                if isinstance(cfg, tuple):
+                    from workloads import random_bounds
+                    Uq, Lq = random_bounds(cfg[1], 4242, p_known=0.2)
+                    cache[cfg] = dict(U=Uq, L=Lq, n=cfg[1])
+                else:
+                    cache[cfg] = make_config(cfg)
             m = cache[cfg]
             U0, L0 = (to_f32(m["U"]), to_f32(m["L"])) if dt == "f32" else (m["U"], m["L"])
             dU0, dL0 = torch.from_numpy(U0).cuda(), torch.from_numpy(L0).cuda()

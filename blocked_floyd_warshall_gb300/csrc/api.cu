@@ -114,7 +114,7 @@ int choose_tile(int n, int batch, int mode) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
     if (mode & BS_TILE_128) return bs::FB_LARGE;
     (void)batch;
-    return n <= 1536 ? bs::FB_SMALL : bs::FB_LARGE;
+    return n <= 3072 ? bs::FB_SMALL : bs::FB_LARGE;
 }
 
 // The blocked schedule.  Without look-ahead: for each block round K, phase 1,
@@ -124,11 +124,16 @@ int choose_tile(int n, int batch, int mode) {
 // The split is exact: those remaining tiles neither read nor write anything
 // phases 1 and 2 of round K+1 touch.
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
-                        DeviceState* d) {
+                        bool force, DeviceState* d) {
     const int nb = (m.n + m.fb - 1) / m.fb;
     cudaError_t e = bs::launch_phase1(is_int, m, 0, s);
     if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, 0, s);
     if (e != cudaSuccess) return e;
+    // Look-ahead pays only when the rest of a round's phase 3 is large enough to
+    // hide phases 1 and 2 of the next round; with a wave or two of tiles, the
+    // serial phase 1 running beside them only gets slower.
+    const double rest_cells = (double)(nb - 2) * (nb - 2) * m.fb * m.fb * m.batch;
+    if (rest_cells < 2097152.0 && !force) lookahead = false;
     if (!lookahead || nb < 3) {
         for (int K = 0; K < nb && e == cudaSuccess; ++K) {
             e = bs::launch_phase3(is_int, m, K, bs::P3_ALL, s);
@@ -166,9 +171,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
                      long long bstride, int batch, int mode, bs::Mats* m) {
     const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE | BS_TILE_64 |
-                      BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC;
+                      BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC | BS_FORCE_LOOKAHEAD;
     if (mode & ~known) return BS_ERR_ARG;
     if ((mode & BS_TILE_64) && (mode & BS_TILE_128)) return BS_ERR_ARG;
+    if ((mode & BS_NO_LOOKAHEAD) && (mode & BS_FORCE_LOOKAHEAD)) return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
     if (n < 0 || batch < 0) return BS_ERR_ARG;
     if (n > 0 && ld < n) return BS_ERR_ARG;
@@ -232,7 +238,8 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
             if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
         }
     } else {
-        e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0, d);
+        e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0,
+                        (mode & BS_FORCE_LOOKAHEAD) != 0, d);
     }
     return cuda_status(e);
 }

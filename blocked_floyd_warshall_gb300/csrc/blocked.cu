@@ -43,6 +43,13 @@ __device__ __forceinline__ void cp_async_wait() {
 
 }  // namespace
 
+// Micro-tile shapes.  Phases 1 and 2 advance one (or two) middle atoms per
+// barrier, so they want many threads with few cells each: 4 x 4 cells on 64-wide
+// tiles (256 threads), 8 x 4 on 128-wide tiles (512 threads).  Phase 3 has no
+// barrier per step and wants many cells per thread: 8 x 8 (64 or 256 threads).
+template <int FB> using P12 = Shape<FB, (FB == FB_SMALL ? 4 : 8), 4>;
+template <int FB> using P3S = Shape<FB, 8, 8>;
+
 // ---------------------------------------------------------------- paired middle atoms
 
 // Cell updates for a pair of middle atoms (k, k+1).
@@ -114,8 +121,9 @@ template <> struct PairLoad<int> {
 // ---------------------------------------------------------------- phase 1
 
 template <class T, bool HAS_L, int FB>
-__global__ void __launch_bounds__(TileShape<FB>::NT)
+__global__ void __launch_bounds__(P12<FB>::NT)
 k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
+    using S = P12<FB>;
     using E = El<T>;
     __shared__ T sRU[2][FB], sRL[2][FB], sCU[2][FB], sCL[2][FB];
     const size_t off = (size_t)blockIdx.z * (size_t)bstride;
@@ -126,41 +134,41 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     T* Ut = U + (size_t)o * ld + o;
     T* Lt = HAS_L ? L + (size_t)o * ld + o : nullptr;
 
-    T u[TM][TN], l[TM][TN];
-    load_tile<FB>(u, Ut, ld, m, m, vec, E::upad());
-    if (HAS_L) load_tile<FB>(l, Lt, ld, m, m, vec, E::lpad());
-    publish_row<FB, T, HAS_L>(u, l, 0, sRU[0], sRL[0]);
-    publish_col<FB, T, HAS_L>(u, l, 0, sCU[0], sCL[0]);
+    T u[S::TM][S::TN], l[S::TM][S::TN];
+    load_tile<S>(u, Ut, ld, m, m, vec, E::upad());
+    if (HAS_L) load_tile<S>(l, Lt, ld, m, m, vec, E::lpad());
+    publish_row<S, T, HAS_L>(u, l, 0, sRU[0], sRL[0]);
+    publish_col<S, T, HAS_L>(u, l, 0, sCU[0], sCL[0]);
     __syncthreads();
 
-    const int r0 = mt_row0<FB>();
+    const int r0 = S::row0();
     for (int k = 0; k < m; ++k) {
         const int b = k & 1;
-        T a[TM], al[TM], bb[TN], bl[TN];
+        T a[S::TM], al[S::TM], bb[S::TN], bl[S::TN];
 #pragma unroll
-        for (int r = 0; r < TM; ++r) {
+        for (int r = 0; r < S::TM; ++r) {
             a[r] = sCU[b][r0 + r];
             al[r] = HAS_L ? sCL[b][r0 + r] : T(0);
         }
 #pragma unroll
-        for (int c = 0; c < TN; ++c) {
-            bb[c] = sRU[b][mt_col<FB>(c)];
-            bl[c] = HAS_L ? sRL[b][mt_col<FB>(c)] : T(0);
+        for (int c = 0; c < S::TN; ++c) {
+            bb[c] = sRU[b][S::col(c)];
+            bl[c] = HAS_L ? sRL[b][S::col(c)] : T(0);
         }
         if (HAS_L) {
             const T lkk = sRL[b][k];
 #pragma unroll
-            for (int r = 0; r < TM; ++r) al[r] = E::mx(al[r], E::sub(lkk, a[r]));
+            for (int r = 0; r < S::TM; ++r) al[r] = E::mx(al[r], E::sub(lkk, a[r]));
         }
-        fw_update<T, HAS_L>(u, l, a, al, bb, bl);
+        fw_update<S, T, HAS_L>(u, l, a, al, bb, bl);
         if (k + 1 < m) {
-            publish_row<FB, T, HAS_L>(u, l, k + 1, sRU[b ^ 1], sRL[b ^ 1]);
-            publish_col<FB, T, HAS_L>(u, l, k + 1, sCU[b ^ 1], sCL[b ^ 1]);
+            publish_row<S, T, HAS_L>(u, l, k + 1, sRU[b ^ 1], sRL[b ^ 1]);
+            publish_col<S, T, HAS_L>(u, l, k + 1, sCU[b ^ 1], sCL[b ^ 1]);
         }
         __syncthreads();
     }
-    store_tile<FB>(u, Ut, ld, m, m, vec);
-    if (HAS_L) store_tile<FB>(l, Lt, ld, m, m, vec);
+    store_tile<S>(u, Ut, ld, m, m, vec);
+    if (HAS_L) store_tile<S>(l, Lt, ld, m, m, vec);
 }
 
 // ---------------------------------------------------------------- phase 2
@@ -183,19 +191,21 @@ constexpr int DPAD = 2;   // diagonal tile row stride FB + DPAD: even, so pairs 
 
 // Row panel: the owner of rows k, k+1 publishes (row k, row k+1 after step k).
 template <class T, bool HAS_L, int FB>
-__device__ __forceinline__ void p2_publish_rows(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
+__device__ __forceinline__ void p2_publish_rows(const T (&u)[P12<FB>::TM][P12<FB>::TN],
+                                                const T (&l)[P12<FB>::TM][P12<FB>::TN], int k,
                                                 const T* dU, const T* dL, T* sU, T* sL) {
+    using S = P12<FB>;
     using E = El<T>;
     constexpr int DS = FB + DPAD;
-    const int r0 = mt_row0<FB>();
+    const int r0 = S::row0();
 #pragma unroll
-    for (int rr = 0; rr < TM; rr += 2) {
+    for (int rr = 0; rr < S::TM; rr += 2) {
         if (r0 + rr != k) continue;
         const T a1 = dU[(k + 1) * DS + k];
         const T al1 = HAS_L ? dL[(k + 1) * DS + k] : T(0);
 #pragma unroll
-        for (int c = 0; c < TN; ++c) {
-            const int j = mt_col<FB>(c);
+        for (int c = 0; c < S::TN; ++c) {
+            const int j = S::col(c);
             sU[2 * j] = u[rr][c];
             sU[2 * j + 1] = E::mn(u[rr + 1][c], E::add(a1, u[rr][c]));
             if (HAS_L) {
@@ -210,20 +220,22 @@ __device__ __forceinline__ void p2_publish_rows(const T (&u)[TM][TN], const T (&
 // U'[i,k+1]) and the closure-raised column values (Lc_k[i], Lc_k+1[i]).
 // dU, dL: the diagonal tile, k-interleaved.
 template <class T, bool HAS_L, int FB>
-__device__ __forceinline__ void p2_publish_cols(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
+__device__ __forceinline__ void p2_publish_cols(const T (&u)[P12<FB>::TM][P12<FB>::TN],
+                                                const T (&l)[P12<FB>::TM][P12<FB>::TN], int k,
                                                 const T* dU, const T* dL, T* sU, T* sL) {
+    using S = P12<FB>;
     using E = El<T>;
-    const int r0 = mt_row0<FB>();
+    const int r0 = S::row0();
 #pragma unroll
-    for (int c = 0; c < TN; c += 2) {
-        if (mt_col<FB>(c) != k) continue;
+    for (int c = 0; c < S::TN; c += 2) {
+        if (S::col(c) != k) continue;
         const int kb = (k >> 1) * (2 * FB);
         const T ukk1 = dU[kb + 2 * (k + 1)];                        // D[k][k+1]
         const T lkk = HAS_L ? dL[kb + 2 * k] : T(0);                // D[k][k]
         const T lkk1 = HAS_L ? dL[kb + 2 * (k + 1)] : T(0);         // D[k][k+1]
         const T lk1k1 = HAS_L ? dL[kb + 2 * (k + 1) + 1] : T(0);    // D[k+1][k+1]
 #pragma unroll
-        for (int r = 0; r < TM; ++r) {
+        for (int r = 0; r < S::TM; ++r) {
             const T uk = u[r][c];
             const T u1 = E::mn(u[r][c + 1], E::add(uk, ukk1));
             sU[2 * (r0 + r)] = uk;
@@ -242,32 +254,33 @@ template <class T, bool HAS_L, int FB>
 __device__ __forceinline__ void p2_row_panel(T* U, T* L, size_t ld, int o, int op, int mk,
                                              int mp, bool vec, bool sym, T* dU, T* dL,
                                              T (*sU)[2 * FB], T (*sL)[2 * FB]) {
+    using S = P12<FB>;
     using E = El<T>;
     using LD = PairLoad<T>;
     using P = typename LD::P;
     constexpr bool NEG = std::is_same<T, int>::value;
     constexpr int DS = FB + DPAD;
-    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
+    const int r0 = S::row0(), cq = S::cq();
     T* Ut = U + (size_t)o * ld + op;
     T* Lt = HAS_L ? L + (size_t)o * ld + op : nullptr;
-    T u[TM][TN], l[TM][TN];
-    load_tile<FB>(u, Ut, ld, mk, mp, vec, E::upad());
-    if (HAS_L) load_tile<FB>(l, Lt, ld, mk, mp, vec, E::lpad());
+    T u[S::TM][S::TN], l[S::TM][S::TN];
+    load_tile<S>(u, Ut, ld, mk, mp, vec, E::upad());
+    if (HAS_L) load_tile<S>(l, Lt, ld, mk, mp, vec, E::lpad());
 
     p2_publish_rows<T, HAS_L, FB>(u, l, 0, dU, dL, sU[0], sL[0]);
     __syncthreads();
 #pragma unroll 1
     for (int k = 0; k < mk; k += 2) {
         const int b = (k >> 1) & 1;
-        P a[TM], al[TM], bb[TN], bl[TN];
+        P a[S::TM], al[S::TM], bb[S::TN], bl[S::TN];
 #pragma unroll
-        for (int r = 0; r < TM; ++r) {
+        for (int r = 0; r < S::TM; ++r) {
             a[r] = LD::ld2(dU + (r0 + r) * DS + k);
             if (HAS_L) al[r] = LD::ld2(dL + (r0 + r) * DS + k);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int jb = (h * (FB / 2) + cq) * 2;
+        for (int h = 0; h < S::QUADS; ++h) {
+            const int jb = (h * S::QSTRIDE + cq) * 2;
             LD::ld4(&sU[b][jb], bb[h * 4 + 0], bb[h * 4 + 1]);
             LD::ld4(&sU[b][jb + 4], bb[h * 4 + 2], bb[h * 4 + 3]);
             if (HAS_L) {
@@ -276,30 +289,30 @@ __device__ __forceinline__ void p2_row_panel(T* U, T* L, size_t ld, int o, int o
             }
         }
 #pragma unroll
-        for (int r = 0; r < TM; ++r)
+        for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-            for (int q = 0; q < TN; ++q) PairOps<T>::upper(u[r][q], a[r], bb[q]);
+            for (int q = 0; q < S::TN; ++q) PairOps<T>::upper(u[r][q], a[r], bb[q]);
         if (HAS_L) {
             if (NEG) {
 #pragma unroll
-                for (int r = 0; r < TM; ++r) a[r] = LD::neg(a[r]);
+                for (int r = 0; r < S::TM; ++r) a[r] = LD::neg(a[r]);
 #pragma unroll
-                for (int q = 0; q < TN; ++q) bb[q] = LD::neg(bb[q]);
+                for (int q = 0; q < S::TN; ++q) bb[q] = LD::neg(bb[q]);
             }
 #pragma unroll
-            for (int r = 0; r < TM; ++r)
+            for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-                for (int q = 0; q < TN; ++q) PairOps<T>::lower(l[r][q], a[r], al[r], bb[q], bl[q]);
+                for (int q = 0; q < S::TN; ++q) PairOps<T>::lower(l[r][q], a[r], al[r], bb[q], bl[q]);
         }
         if (k + 2 < mk) p2_publish_rows<T, HAS_L, FB>(u, l, k + 2, dU, dL, sU[b ^ 1], sL[b ^ 1]);
         __syncthreads();
     }
-    store_tile<FB>(u, Ut, ld, mk, mp, vec);
-    if (HAS_L) store_tile<FB>(l, Lt, ld, mk, mp, vec);
+    store_tile<S>(u, Ut, ld, mk, mp, vec);
+    if (HAS_L) store_tile<S>(l, Lt, ld, mk, mp, vec);
     if (sym) {
         // symmetric inputs: the column panel tile (P, K) is the transpose
-        store_tile_t<FB>(u, U + (size_t)op * ld + o, ld, mk, mp, vec);
-        if (HAS_L) store_tile_t<FB>(l, L + (size_t)op * ld + o, ld, mk, mp, vec);
+        store_tile_t<S>(u, U + (size_t)op * ld + o, ld, mk, mp, vec);
+        if (HAS_L) store_tile_t<S>(l, L + (size_t)op * ld + o, ld, mk, mp, vec);
     }
 }
 
@@ -307,32 +320,33 @@ template <class T, bool HAS_L, int FB>
 __device__ __forceinline__ void p2_col_panel(T* U, T* L, size_t ld, int o, int op, int mk,
                                              int mp, bool vec, T* dU, T* dL,
                                              T (*sU)[2 * FB], T (*sL)[2 * FB]) {
+    using S = P12<FB>;
     using E = El<T>;
     using LD = PairLoad<T>;
     using P = typename LD::P;
     constexpr bool NEG = std::is_same<T, int>::value;
-    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
+    const int r0 = S::row0(), cq = S::cq();
     T* Ut = U + (size_t)op * ld + o;
     T* Lt = HAS_L ? L + (size_t)op * ld + o : nullptr;
-    T u[TM][TN], l[TM][TN];
-    load_tile<FB>(u, Ut, ld, mp, mk, vec, E::upad());
-    if (HAS_L) load_tile<FB>(l, Lt, ld, mp, mk, vec, E::lpad());
+    T u[S::TM][S::TN], l[S::TM][S::TN];
+    load_tile<S>(u, Ut, ld, mp, mk, vec, E::upad());
+    if (HAS_L) load_tile<S>(l, Lt, ld, mp, mk, vec, E::lpad());
 
     p2_publish_cols<T, HAS_L, FB>(u, l, 0, dU, dL, sU[0], sL[0]);
     __syncthreads();
 #pragma unroll 1
     for (int k = 0; k < mk; k += 2) {
         const int b = (k >> 1) & 1;
-        P a[TM], al[TM], bb[TN], bl[TN];
+        P a[S::TM], al[S::TM], bb[S::TN], bl[S::TN];
 #pragma unroll
-        for (int r = 0; r < TM; ++r) {
+        for (int r = 0; r < S::TM; ++r) {
             a[r] = LD::ld2(&sU[b][2 * (r0 + r)]);
             if (HAS_L) al[r] = LD::ld2(&sL[b][2 * (r0 + r)]);
         }
         const int bo = (k >> 1) * (2 * FB);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int jb = bo + (h * (FB / 2) + cq) * 2;
+        for (int h = 0; h < S::QUADS; ++h) {
+            const int jb = bo + (h * S::QSTRIDE + cq) * 2;
             LD::ld4(dU + jb, bb[h * 4 + 0], bb[h * 4 + 1]);
             LD::ld4(dU + jb + 4, bb[h * 4 + 2], bb[h * 4 + 3]);
             if (HAS_L) {
@@ -341,34 +355,35 @@ __device__ __forceinline__ void p2_col_panel(T* U, T* L, size_t ld, int o, int o
             }
         }
 #pragma unroll
-        for (int r = 0; r < TM; ++r)
+        for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-            for (int q = 0; q < TN; ++q) PairOps<T>::upper(u[r][q], a[r], bb[q]);
+            for (int q = 0; q < S::TN; ++q) PairOps<T>::upper(u[r][q], a[r], bb[q]);
         if (HAS_L) {
             if (NEG) {
 #pragma unroll
-                for (int r = 0; r < TM; ++r) a[r] = LD::neg(a[r]);
+                for (int r = 0; r < S::TM; ++r) a[r] = LD::neg(a[r]);
 #pragma unroll
-                for (int q = 0; q < TN; ++q) bb[q] = LD::neg(bb[q]);
+                for (int q = 0; q < S::TN; ++q) bb[q] = LD::neg(bb[q]);
             }
 #pragma unroll
-            for (int r = 0; r < TM; ++r)
+            for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-                for (int q = 0; q < TN; ++q) PairOps<T>::lower(l[r][q], a[r], al[r], bb[q], bl[q]);
+                for (int q = 0; q < S::TN; ++q) PairOps<T>::lower(l[r][q], a[r], al[r], bb[q], bl[q]);
         }
         if (k + 2 < mk) p2_publish_cols<T, HAS_L, FB>(u, l, k + 2, dU, dL, sU[b ^ 1], sL[b ^ 1]);
         __syncthreads();
     }
-    store_tile<FB>(u, Ut, ld, mp, mk, vec);
-    if (HAS_L) store_tile<FB>(l, Lt, ld, mp, mk, vec);
+    store_tile<S>(u, Ut, ld, mp, mk, vec);
+    if (HAS_L) store_tile<S>(l, Lt, ld, mp, mk, vec);
 }
 
 template <class T, bool HAS_L, int FB>
-__global__ void __launch_bounds__(TileShape<FB>::NT)
+__global__ void __launch_bounds__(P12<FB>::NT)
 k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec,
          bool sym) {
+    using S = P12<FB>;
     using E = El<T>;
-    constexpr int NT = TileShape<FB>::NT;
+    constexpr int NT = P12<FB>::NT;
     constexpr int DS = FB + DPAD;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* dU = reinterpret_cast<T*>(smem_raw);
@@ -441,13 +456,14 @@ template <class T, bool HAS_L, int FB>
 __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_t ld, int oi,
                                          int oj, int ok, int mi, int mj, int mk, int c,
                                          bool vec) {
+    using S = P3S<FB>;
     using E = El<T>;
-    using S = P3Smem<T, HAS_L, FB>;
-    constexpr int NT = TileShape<FB>::NT;
+    using SM = P3Smem<T, HAS_L, FB>;
+    constexpr int NT = P3S<FB>::NT;
     T* AU = stage;
-    T* BU = stage + S::A_ELEMS;
-    T* AL = HAS_L ? BU + S::B_ELEMS : nullptr;
-    T* BL = HAS_L ? AL + S::A_ELEMS : nullptr;
+    T* BU = stage + SM::A_ELEMS;
+    T* AL = HAS_L ? BU + SM::B_ELEMS : nullptr;
+    T* BL = HAS_L ? AL + SM::A_ELEMS : nullptr;
     const int kc = c * BK;
     // column panel: FB rows x BK middle atoms, [i][k]
     if (vec) {
@@ -556,11 +572,12 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
 }
 
 template <class T, bool HAS_L, int FB>
-__global__ void __launch_bounds__(TileShape<FB>::NT)
+__global__ void __launch_bounds__(P3S<FB>::NT)
 k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K,
          int part, bool vec, bool sym) {
+    using S = P3S<FB>;
     using E = El<T>;
-    using S = P3Smem<T, HAS_L, FB>;
+    using SM = P3Smem<T, HAS_L, FB>;
     using LD = PairLoad<T>;
     using P = typename LD::P;
     constexpr bool NEG = std::is_same<T, int>::value;   // int lower bound adds negated values
@@ -576,37 +593,37 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     const int oi = I * FB, oj = J * FB, ok = K * FB;
     const int mi = min(FB, n - oi), mj = min(FB, n - oj), mk = min(FB, n - ok);
 
-    T u[TM][TN], l[TM][TN];
-    load_tile<FB>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
-    if (HAS_L) load_tile<FB>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
+    T u[S::TM][S::TN], l[S::TM][S::TN];
+    load_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
+    if (HAS_L) load_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
 
     const int nchunks = (mk + BK - 1) / BK;
     p3_stage<T, HAS_L, FB>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
     cp_async_commit();
-    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
+    const int r0 = S::row0(), cq = S::cq();
     for (int c = 0; c < nchunks; ++c) {
         if (c + 1 < nchunks)
-            p3_stage<T, HAS_L, FB>(sm + ((c + 1) & 1) * S::STAGE, U, L, ld, oi, oj, ok, mi, mj,
+            p3_stage<T, HAS_L, FB>(sm + ((c + 1) & 1) * SM::STAGE, U, L, ld, oi, oj, ok, mi, mj,
                                    mk, c + 1, vec);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
-        const T* AU = sm + (c & 1) * S::STAGE;
-        const T* BU = AU + S::A_ELEMS;
-        const T* AL = BU + S::B_ELEMS;
-        const T* BL = AL + S::A_ELEMS;
+        const T* AU = sm + (c & 1) * SM::STAGE;
+        const T* BU = AU + SM::A_ELEMS;
+        const T* AL = BU + SM::B_ELEMS;
+        const T* BL = AL + SM::A_ELEMS;
 #pragma unroll 1
         for (int kk = 0; kk < BK; kk += 2) {
-            P a[TM], al[TM], b[TN], bl[TN];
+            P a[S::TM], al[S::TM], b[S::TN], bl[S::TN];
 #pragma unroll
-            for (int r = 0; r < TM; ++r) {
+            for (int r = 0; r < S::TM; ++r) {
                 a[r] = LD::ld2(AU + (r0 + r) * AST + kk);
                 if (HAS_L) al[r] = LD::ld2(AL + (r0 + r) * AST + kk);
             }
             const int bo = (kk >> 1) * (2 * FB);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int jb = bo + (h * (FB / 2) + cq) * 2;
+            for (int h = 0; h < S::QUADS; ++h) {
+                const int jb = bo + (h * S::QSTRIDE + cq) * 2;
                 LD::ld4(BU + jb, b[h * 4 + 0], b[h * 4 + 1]);
                 LD::ld4(BU + jb + 4, b[h * 4 + 2], b[h * 4 + 3]);
                 if (HAS_L) {
@@ -615,30 +632,30 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
                 }
             }
 #pragma unroll
-            for (int r = 0; r < TM; ++r)
+            for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-                for (int q = 0; q < TN; ++q) PairOps<T>::upper(u[r][q], a[r], b[q]);
+                for (int q = 0; q < S::TN; ++q) PairOps<T>::upper(u[r][q], a[r], b[q]);
             if (HAS_L) {
                 if (NEG) {
 #pragma unroll
-                    for (int r = 0; r < TM; ++r) a[r] = LD::neg(a[r]);
+                    for (int r = 0; r < S::TM; ++r) a[r] = LD::neg(a[r]);
 #pragma unroll
-                    for (int q = 0; q < TN; ++q) b[q] = LD::neg(b[q]);
+                    for (int q = 0; q < S::TN; ++q) b[q] = LD::neg(b[q]);
                 }
 #pragma unroll
-                for (int r = 0; r < TM; ++r)
+                for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-                    for (int q = 0; q < TN; ++q)
+                    for (int q = 0; q < S::TN; ++q)
                         PairOps<T>::lower(l[r][q], a[r], al[r], b[q], bl[q]);
             }
         }
         __syncthreads();
     }
-    store_tile<FB>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
-    if (HAS_L) store_tile<FB>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
+    store_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
+    if (HAS_L) store_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
     if (sym && I != J) {
-        store_tile_t<FB>(u, U + (size_t)oj * ld + oi, ld, mi, mj, vec);
-        if (HAS_L) store_tile_t<FB>(l, L + (size_t)oj * ld + oi, ld, mi, mj, vec);
+        store_tile_t<S>(u, U + (size_t)oj * ld + oi, ld, mi, mj, vec);
+        if (HAS_L) store_tile_t<S>(l, L + (size_t)oj * ld + oi, ld, mi, mj, vec);
     }
 }
 
@@ -674,7 +691,8 @@ enum class Which { One, Two, Three };
 
 template <class T, bool HAS_L, int FB>
 static cudaError_t phase_t(Which w, const Mats& m, int K, int part, cudaStream_t s) {
-    constexpr int NT = TileShape<FB>::NT;
+    constexpr int NT12 = P12<FB>::NT;   // phases 1 and 2
+    constexpr int NT3 = P3S<FB>::NT;    // phase 3
     const int nb = (m.n + FB - 1) / FB;
     int tiles = 0;
     if (w == Which::Three) {
@@ -695,17 +713,17 @@ static cudaError_t phase_t(Which w, const Mats& m, int K, int part, cudaStream_t
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
         if (w == Which::One) {
             before_launch(s, PH_ONE);
-            k_phase1<T, HAS_L, FB><<<dim3(1, 1, nbz), NT, 0, s>>>(U, L, m.n, m.ld, m.bstride, K,
+            k_phase1<T, HAS_L, FB><<<dim3(1, 1, nbz), NT12, 0, s>>>(U, L, m.n, m.ld, m.bstride, K,
                                                                   m.vec);
             after_launch(s, PH_ONE);
         } else if (w == Which::Two) {
             before_launch(s, PH_TWO);
-            k_phase2<T, HAS_L, FB><<<dim3(nb - 1, m.sym ? 1 : 2, nbz), NT, p2_smem<T, HAS_L, FB>(),
+            k_phase2<T, HAS_L, FB><<<dim3(nb - 1, m.sym ? 1 : 2, nbz), NT12, p2_smem<T, HAS_L, FB>(),
                                      s>>>(U, L, m.n, m.ld, m.bstride, K, m.vec, m.sym);
             after_launch(s, PH_TWO);
         } else {
             before_launch(s, PH_THREE);
-            k_phase3<T, HAS_L, FB><<<dim3(tiles, 1, nbz), NT, P3Smem<T, HAS_L, FB>::BYTES, s>>>(
+            k_phase3<T, HAS_L, FB><<<dim3(tiles, 1, nbz), NT3, P3Smem<T, HAS_L, FB>::BYTES, s>>>(
                 U, L, m.n, m.ld, m.bstride, K, part, m.vec, m.sym);
             after_launch(s, PH_THREE);
         }

@@ -8,15 +8,8 @@ namespace bs {
 
 // Floyd-Warshall block (tile) sizes of the three-phase schedule: 128 for large
 // matrices, 64 for small ones (a quarter of the serial work per block round).
-// Every blocked kernel runs (FB/8)^2 threads (256 or 64), each owning an 8 x 8
-// micro-tile of U (and of L).
 constexpr int FB_LARGE = 128;
 constexpr int FB_SMALL = 64;
-constexpr int TM = 8;
-constexpr int TN = 8;
-template <int FB> struct TileShape {
-    static constexpr int NT = (FB / 8) * (FB / 8);
-};
 
 // One batch of matrices as the kernels see it.
 struct Mats {

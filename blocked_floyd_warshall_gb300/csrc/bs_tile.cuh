@@ -35,27 +35,38 @@ template <> struct El<int> {
     static __device__ __forceinline__ int mx(int a, int b) { return max(a, b); }
 };
 
-// Micro-tile coordinates of this thread inside an FB x FB tile (FB/8 x FB/8
-// threads): rows 8*ty .. 8*ty+7, columns 4*tx+q and FB/2+4*tx+q.
-template <int FB> __device__ __forceinline__ int mt_row0() { return (threadIdx.x / (FB / 8)) * TM; }
-template <int FB> __device__ __forceinline__ int mt_cq() { return (threadIdx.x % (FB / 8)) * 4; }
-template <int FB> __device__ __forceinline__ int mt_col(int c) {
-    return (c >> 2) * (FB / 2) + mt_cq<FB>() + (c & 3);
-}
+// Micro-tile geometry: an FB x FB tile covered by (FB/TM) x (FB/TN) threads,
+// each owning TM x TN cells: rows TM*ty .. TM*ty+TM-1 and TN/4 column quads,
+// quad h covering columns h*FB/(TN/4) + 4*tx .. +3 (ty = tid / (FB/TN),
+// tx = tid % (FB/TN)).  Rows 2m, 2m+1 always share a thread (TM even), and so
+// do columns 2m, 2m+1 (same quad).
+template <int FB_, int TM_, int TN_>
+struct Shape {
+    static constexpr int FB = FB_;
+    static constexpr int TM = TM_;
+    static constexpr int TN = TN_;
+    static constexpr int QUADS = TN / 4;
+    static constexpr int TX = FB / TN;              // threads per row group
+    static constexpr int NT = (FB / TM) * TX;       // threads per CTA
+    static constexpr int QSTRIDE = FB / QUADS;      // column distance between quads
+    static __device__ __forceinline__ int row0() { return (int)(threadIdx.x / TX) * TM; }
+    static __device__ __forceinline__ int cq() { return (int)(threadIdx.x % TX) * 4; }
+    static __device__ __forceinline__ int col(int c) { return (c >> 2) * QSTRIDE + cq() + (c & 3); }
+};
 
-// Load the thread's 8 x 8 cells of the tile at `M` (tile origin; mr x mc cells
+// Load the thread's cells of the tile at `M` (tile origin; mr x mc cells
 // valid).  Cells outside get `pad`.
-template <int FB, class T>
-__device__ __forceinline__ void load_tile(T (&x)[TM][TN], const T* M, size_t ld, int mr,
+template <class S, class T>
+__device__ __forceinline__ void load_tile(T (&x)[S::TM][S::TN], const T* M, size_t ld, int mr,
                                           int mc, bool vec, T pad) {
     using V4 = typename El<T>::V4;
-    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
+    const int r0 = S::row0(), cq = S::cq();
 #pragma unroll
-    for (int r = 0; r < TM; ++r) {
+    for (int r = 0; r < S::TM; ++r) {
         const int i = r0 + r;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int j = h * (FB / 2) + cq;
+        for (int h = 0; h < S::QUADS; ++h) {
+            const int j = h * S::QSTRIDE + cq;
             if (vec && i < mr && j + 4 <= mc) {
                 const V4 v = *reinterpret_cast<const V4*>(M + (size_t)i * ld + j);
                 x[r][h * 4 + 0] = v.x;
@@ -72,18 +83,18 @@ __device__ __forceinline__ void load_tile(T (&x)[TM][TN], const T* M, size_t ld,
 }
 
 // Store the thread's cells that lie inside the mr x mc block.
-template <int FB, class T>
-__device__ __forceinline__ void store_tile(const T (&x)[TM][TN], T* M, size_t ld, int mr,
+template <class S, class T>
+__device__ __forceinline__ void store_tile(const T (&x)[S::TM][S::TN], T* M, size_t ld, int mr,
                                            int mc, bool vec) {
     using V4 = typename El<T>::V4;
-    const int r0 = mt_row0<FB>(), cq = mt_cq<FB>();
+    const int r0 = S::row0(), cq = S::cq();
 #pragma unroll
-    for (int r = 0; r < TM; ++r) {
+    for (int r = 0; r < S::TM; ++r) {
         const int i = r0 + r;
         if (i >= mr) continue;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int j = h * (FB / 2) + cq;
+        for (int h = 0; h < S::QUADS; ++h) {
+            const int j = h * S::QSTRIDE + cq;
             if (vec && j + 4 <= mc) {
                 V4 v;
                 v.x = x[r][h * 4 + 0];
@@ -102,23 +113,25 @@ __device__ __forceinline__ void store_tile(const T (&x)[TM][TN], T* M, size_t ld
 
 // Store the transpose of the thread's cells: cell (i, j) of an mr x mc tile
 // goes to MT[j*ld + i], MT being the origin of the mirrored tile.  For a fixed
-// column the thread's 8 rows are 8 consecutive elements (one 32-byte sector).
-template <int FB, class T>
-__device__ __forceinline__ void store_tile_t(const T (&x)[TM][TN], T* MT, size_t ld, int mr,
+// column the thread's rows are consecutive elements (one 32-byte sector for
+// 8 rows).
+template <class S, class T>
+__device__ __forceinline__ void store_tile_t(const T (&x)[S::TM][S::TN], T* MT, size_t ld, int mr,
                                              int mc, bool vec) {
     using V4 = typename El<T>::V4;
-    const int r0 = mt_row0<FB>();
+    const int r0 = S::row0();
 #pragma unroll
-    for (int c = 0; c < TN; ++c) {
-        const int j = mt_col<FB>(c);
+    for (int c = 0; c < S::TN; ++c) {
+        const int j = S::col(c);
         if (j >= mc) continue;
         T* row = MT + (size_t)j * ld + r0;
-        if (vec && r0 + TM <= mr) {
-            *reinterpret_cast<V4*>(row) = V4{x[0][c], x[1][c], x[2][c], x[3][c]};
-            *reinterpret_cast<V4*>(row + 4) = V4{x[4][c], x[5][c], x[6][c], x[7][c]};
+        if (vec && r0 + S::TM <= mr) {
+#pragma unroll
+            for (int r = 0; r < S::TM; r += 4)
+                *reinterpret_cast<V4*>(row + r) = V4{x[r][c], x[r + 1][c], x[r + 2][c], x[r + 3][c]};
         } else {
 #pragma unroll
-            for (int r = 0; r < TM; ++r)
+            for (int r = 0; r < S::TM; ++r)
                 if (r0 + r < mr) row[r] = x[r][c];
         }
     }
@@ -130,51 +143,51 @@ __device__ __forceinline__ void store_tile_t(const T (&x)[TM][TN], T* MT, size_t
 // (round-invariant) upper values:
 //   U[i,j] = min(U[i,j], U[i,k] + U[k,j])
 //   L[i,j] = max(L[i,j], L[k,j] - U[i,k], Lcol[i] - U[k,j])
-template <class T, bool HAS_L>
-__device__ __forceinline__ void fw_update(T (&u)[TM][TN], T (&l)[TM][TN], const T (&a)[TM],
-                                          const T (&al)[TM], const T (&b)[TN],
-                                          const T (&bl)[TN]) {
+template <class S, class T, bool HAS_L>
+__device__ __forceinline__ void fw_update(T (&u)[S::TM][S::TN], T (&l)[S::TM][S::TN],
+                                          const T (&a)[S::TM], const T (&al)[S::TM],
+                                          const T (&b)[S::TN], const T (&bl)[S::TN]) {
 #pragma unroll
-    for (int r = 0; r < TM; ++r)
+    for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-        for (int c = 0; c < TN; ++c) u[r][c] = El<T>::mn(u[r][c], El<T>::add(a[r], b[c]));
+        for (int c = 0; c < S::TN; ++c) u[r][c] = El<T>::mn(u[r][c], El<T>::add(a[r], b[c]));
     if (HAS_L) {
 #pragma unroll
-        for (int r = 0; r < TM; ++r)
+        for (int r = 0; r < S::TM; ++r)
 #pragma unroll
-            for (int c = 0; c < TN; ++c)
+            for (int c = 0; c < S::TN; ++c)
                 l[r][c] = El<T>::mx(l[r][c], El<T>::mx(El<T>::sub(bl[c], a[r]),
                                                        El<T>::sub(al[r], b[c])));
     }
 }
 
 // Row k of the tile (U and L) into shared vectors, by the threads that own it.
-template <int FB, class T, bool HAS_L>
-__device__ __forceinline__ void publish_row(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
-                                            T* dU, T* dL) {
-    const int r0 = mt_row0<FB>();
+template <class S, class T, bool HAS_L>
+__device__ __forceinline__ void publish_row(const T (&u)[S::TM][S::TN], const T (&l)[S::TM][S::TN],
+                                            int k, T* dU, T* dL) {
+    const int r0 = S::row0();
 #pragma unroll
-    for (int r = 0; r < TM; ++r) {
+    for (int r = 0; r < S::TM; ++r) {
         if (r0 + r == k) {
 #pragma unroll
-            for (int c = 0; c < TN; ++c) {
-                dU[mt_col<FB>(c)] = u[r][c];
-                if (HAS_L) dL[mt_col<FB>(c)] = l[r][c];
+            for (int c = 0; c < S::TN; ++c) {
+                dU[S::col(c)] = u[r][c];
+                if (HAS_L) dL[S::col(c)] = l[r][c];
             }
         }
     }
 }
 
 // Column k of the tile (U and L) into shared vectors, by the threads that own it.
-template <int FB, class T, bool HAS_L>
-__device__ __forceinline__ void publish_col(const T (&u)[TM][TN], const T (&l)[TM][TN], int k,
-                                            T* dU, T* dL) {
-    const int r0 = mt_row0<FB>();
+template <class S, class T, bool HAS_L>
+__device__ __forceinline__ void publish_col(const T (&u)[S::TM][S::TN], const T (&l)[S::TM][S::TN],
+                                            int k, T* dU, T* dL) {
+    const int r0 = S::row0();
 #pragma unroll
-    for (int c = 0; c < TN; ++c) {
-        if (mt_col<FB>(c) == k) {
+    for (int c = 0; c < S::TN; ++c) {
+        if (S::col(c) == k) {
 #pragma unroll
-            for (int r = 0; r < TM; ++r) {
+            for (int r = 0; r < S::TM; ++r) {
                 dU[r0 + r] = u[r][c];
                 if (HAS_L) dL[r0 + r] = l[r][c];
             }

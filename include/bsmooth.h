@@ -82,10 +82,16 @@ enum {
     BS_RULE_LITERAL = 1 << 3, /* printed rule; BS_PERK only, else BS_ERR_ARG */
     BS_VALIDATE = 1 << 4,     /* check the preconditions first (synchronises) */
     /* Blocked-mode schedule knobs; every setting gives identical results. */
-    BS_TILE_64 = 1 << 5,      /* force 64 x 64 tiles (default: chosen from n) */
+    BS_TILE_64 = 1 << 5,      /* force 64 x 64 tiles (default: 64 for n <= 3072,
+                                 else 128) */
     BS_TILE_128 = 1 << 6,     /* force 128 x 128 tiles; both tile bits: BS_ERR_ARG */
     BS_NO_LOOKAHEAD = 1 << 7, /* run the three phases of each block round in
                                  sequence on `stream` only (see below) */
+    BS_FORCE_LOOKAHEAD = 1 << 9, /* use the look-ahead schedule even where the
+                                    size rule would not (it is on by default only
+                                    when a round's remaining phase-3 work is at
+                                    least 2^21 cells); with BS_NO_LOOKAHEAD:
+                                    BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the
                                  diagonal are computed, each mirrored into its

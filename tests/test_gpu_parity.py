@@ -38,8 +38,8 @@ SIZES_BLOCKED = [1, 2, 3, 5, 31, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 
 # blocked-mode schedules: automatic, forced tile sizes, with and without look-ahead
 SCHEDULES = {
     "auto": 0,
-    "t64": bsm.BS_TILE_64,
-    "t128": bsm.BS_TILE_128,
+    "t64": bsm.BS_TILE_64 | bsm.BS_FORCE_LOOKAHEAD,
+    "t128": bsm.BS_TILE_128 | bsm.BS_FORCE_LOOKAHEAD,
     "t64_serial": bsm.BS_TILE_64 | bsm.BS_NO_LOOKAHEAD,
     "t128_serial": bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD,
     "sym": bsm.BS_SYMMETRIC,
@@ -217,6 +217,17 @@ def test_chain_configs(idx, algo):
         assert oracle.count_infeasible(Uo, Lo) == 0
 
 
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_mid_size_default_schedule(dtype):
+    """n = 2000 (ragged against 64-wide tiles) on the default schedule, which
+    at this size is 64-wide tiles with look-ahead: full matrix vs the oracle."""
+    Uq, Lq = W.random_bounds(2000, 2024, p_known=0.1, p_bad=0.001)
+    U0, L0 = as_dtype(Uq, Lq, dtype)
+    Uo, Lo = oracle.smooth(U0, L0)
+    Ug, Lg, ok = gpu_bounds(U0, L0)
+    assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
 @pytest.fixture(scope="module")
 def globule4096():
     m = W.make_config(2)
@@ -380,16 +391,21 @@ def test_empty_and_launch_counting():
                          flags=bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD)
     assert bsm.bs_launch_count() - before == 3 * 3        # three phases x three block rounds
     before = bsm.bs_launch_count()
-    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_TILE_64)
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)),
+                         flags=bsm.BS_TILE_64 | bsm.BS_FORCE_LOOKAHEAD)
     # 5 block rounds: 5 x (phase 1, phase 2); phase 3 split in two for rounds 0..3
     assert bsm.bs_launch_count() - before == 5 + 5 + 4 * 2 + 1
+    before = bsm.bs_launch_count()
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_TILE_64)
+    # this size is below the look-ahead rule: three launches per round
+    assert bsm.bs_launch_count() - before == 5 * 3
 
 
 def test_profile_records_every_launch():
     Uq, Lq = W.random_bounds(300, 2, p_bad=0.01)
     U, L = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
     bsm.bs_profile_begin()
-    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_TILE_128)
+    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_TILE_128 | bsm.BS_FORCE_LOOKAHEAD)
     p = bsm.bs_profile_end()
     assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 5]   # rounds 0, 1: phase 3 split
     assert p["phase3"]["ms"] > 0
