@@ -89,13 +89,13 @@ def load_peaks():
 
 
 def kernel_hash():
-    """Hash of the CUDA sources: ties a committed ncu traffic figure to the code."""
+    """Hash of the phase-3 kernel's sources (the blocked kernels and their
+    device helpers): ties a committed ncu traffic figure to the code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blocked_floyd_warshall_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in ("phase3.cu", "pairops.cuh", "bs_tile.cuh", "bs_internal.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 

@@ -39,6 +39,7 @@ cudaError_t launch_cross(bool is_int, const Mats& m, int k, cudaStream_t s);
 
 // Blocked mode, block round K.
 cudaError_t blocked_setup(bool is_int);   // once per device: shared-memory limits
+cudaError_t phase3_setup(bool is_int);
 cudaError_t launch_phase1(bool is_int, const Mats& m, int K, cudaStream_t s);
 cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
 // Phase 3 of block round K over the tiles `part` selects (P3_* below).

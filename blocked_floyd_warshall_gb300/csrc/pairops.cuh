@@ -1,0 +1,115 @@
+// Helpers shared by the blocked kernels: cp.async staging, the micro-tile
+// shapes of each phase, the paired middle-atom instructions, and the loop over
+// batch chunks of a launch.
+#pragma once
+
+#include <type_traits>
+
+#include "bs_tile.cuh"
+
+namespace bs {
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Micro-tile shapes.  Phases 1 and 2 advance one (or two) middle atoms per
+// barrier, so they want more threads with fewer cells each: 4 x 4 cells on
+// 64-wide tiles (256 threads); on 128-wide tiles phase 2 runs 8 x 4 (512
+// threads) and phase 1 8 x 8 (256 threads), the faster shape for each measured
+// on the GB300.  Phase 3 has no barrier per step and wants many cells per
+// thread: 8 x 8 (64 or 256 threads).
+template <int FB> using P1S = Shape<FB, (FB == FB_SMALL ? 4 : 8), (FB == FB_SMALL ? 4 : 8)>;
+template <int FB> using P12 = Shape<FB, (FB == FB_SMALL ? 4 : 8), 4>;
+template <int FB> using P3S = Shape<FB, 8, 8>;
+
+// ---------------------------------------------------------------- paired middle atoms
+
+// Cell updates for a pair of middle atoms (k, k+1).
+//   a, al : (U[i,k], U[i,k+1]), (L[i,k], L[i,k+1])   -- row i of the thread
+//   b, bl : (U[k,j], U[k+1,j]), (L[k,j], L[k+1,j])   -- column j of the thread
+template <class T> struct PairOps;
+
+template <> struct PairOps<float> {
+    using P = unsigned long long;   // two fp32 lanes: low = k, high = k+1
+    static __device__ __forceinline__ void upper(float& u, P a, P b) {
+        asm("{\n\t.reg .b64 s;\n\t.reg .f32 s0, s1;\n\t"
+            "add.rn.f32x2 s, %1, %2;\n\t"
+            "mov.b64 {s0, s1}, s;\n\t"
+            "min.f32 %0, %0, s0, s1;\n\t}"
+            : "+f"(u) : "l"(a), "l"(b));
+    }
+    // L = max(L, L[k,j] - U[i,k], L[i,k] - U[k,j]) over both k
+    static __device__ __forceinline__ void lower(float& l, P a, P al, P b, P bl) {
+        asm("{\n\t.reg .b64 d1, d2;\n\t.reg .f32 x0, x1, y0, y1;\n\t"
+            "sub.rn.f32x2 d1, %1, %3;\n\t"
+            "sub.rn.f32x2 d2, %2, %4;\n\t"
+            "mov.b64 {x0, x1}, d1;\n\t"
+            "mov.b64 {y0, y1}, d2;\n\t"
+            "max.f32 %0, %0, x0, x1;\n\t"
+            "max.f32 %0, %0, y0, y1;\n\t}"
+            : "+f"(l) : "l"(bl), "l"(al), "l"(a), "l"(b));
+    }
+};
+
+template <> struct PairOps<int> {
+    using P = int2;
+    static __device__ __forceinline__ void upper(int& u, P a, P b) {
+        u = __viaddmin_s32(a.x, b.x, u);
+        u = __viaddmin_s32(a.y, b.y, u);
+    }
+    // na, nb: negated a, b
+    static __device__ __forceinline__ void lower(int& l, P na, P al, P nb, P bl) {
+        l = __viaddmax_s32(bl.x, na.x, l);
+        l = __viaddmax_s32(bl.y, na.y, l);
+        l = __viaddmax_s32(al.x, nb.x, l);
+        l = __viaddmax_s32(al.y, nb.y, l);
+    }
+};
+
+template <class T> struct PairLoad;
+template <> struct PairLoad<float> {
+    using P = unsigned long long;
+    static __device__ __forceinline__ P ld2(const float* p) {
+        return *reinterpret_cast<const unsigned long long*>(p);
+    }
+    static __device__ __forceinline__ void ld4(const float* p, P& x, P& y) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
+        x = v.x;
+        y = v.y;
+    }
+    static __device__ __forceinline__ P neg(P x) { return x; }
+};
+template <> struct PairLoad<int> {
+    using P = int2;
+    static __device__ __forceinline__ P ld2(const int* p) { return *reinterpret_cast<const int2*>(p); }
+    static __device__ __forceinline__ void ld4(const int* p, P& x, P& y) {
+        const int4 v = *reinterpret_cast<const int4*>(p);
+        x = make_int2(v.x, v.y);
+        y = make_int2(v.z, v.w);
+    }
+    static __device__ __forceinline__ P neg(P x) { return make_int2(-x.x, -x.y); }
+};
+
+// Launch `launch(first, count)` over the batch in chunks the grid's z dimension
+// can hold; returns the first launch error.
+template <class F>
+cudaError_t for_batch_chunks(const Mats& m, F launch) {
+    for (int b0 = 0; b0 < m.batch; b0 += 65535) {
+        const int nbz = m.batch - b0 < 65535 ? m.batch - b0 : 65535;
+        launch(b0, nbz);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace bs
