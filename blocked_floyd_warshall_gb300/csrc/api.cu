@@ -152,12 +152,15 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
         }
         e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT, s);
         if (e == cudaSuccess) e = cudaEventRecord(c.fork, s);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(c.side, c.fork, 0);
+        if (e != cudaSuccess) break;
+        // from here on the side stream is forked: always join it back
+        e = cudaStreamWaitEvent(c.side, c.fork, 0);
         if (e == cudaSuccess) e = bs::launch_phase1(is_int, m, K + 1, c.side);
         if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K + 1, c.side);
-        if (e == cudaSuccess) e = cudaEventRecord(c.join, c.side);
+        cudaError_t j = cudaEventRecord(c.join, c.side);
         if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, bs::P3_REST, s);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c.join, 0);
+        if (j == cudaSuccess) j = cudaStreamWaitEvent(s, c.join, 0);
+        if (e == cudaSuccess) e = j;
     }
     release_side(d, c);
     return e;

@@ -40,7 +40,10 @@
  * (unless BS_NO_LOOKAHEAD) phases 1 and 2 of block round K+1 run on an
  * internal stream of the library, forked from and joined back into `stream`
  * with events inside the call, while the rest of round K's phase 3 runs on
- * `stream`; all work still completes in `stream` order.
+ * `stream`; all work still completes in `stream` order.  The smoothing calls
+ * can be captured into a CUDA graph (stream capture on `stream`) once the
+ * library has run one smoothing of the same kind on the device, which sets up
+ * its per-device state; the look-ahead fork and join are captured with it.
  *
  * Memory.  The caller owns U, L and the mask.  Smoothing allocates nothing.
  * bs_check_feasible and BS_VALIDATE use one small internal device buffer per

@@ -373,6 +373,34 @@ def test_symmetric_flag_checks():
                          flags=bsm.BS_SYMMETRIC | bsm.BS_VALIDATE)
 
 
+@pytest.mark.parametrize("sched", ["t64", "t128", "sym", "perk"])
+def test_cuda_graph_capture_and_replay(sched):
+    """A smoothing captured into a CUDA graph (look-ahead fork and join
+    included) replays to the same result, twice, on fresh inputs."""
+    t = torch()
+    flags = bsm.BS_PERK if sched == "perk" else SCHEDULES[sched]
+    n = 300
+    Uq, Lq = W.random_bounds(n, 9300, p_bad=0.02)
+    U0, L0 = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
+    Uo, Lo = oracle.smooth(W.to_f32(Uq), W.to_f32(Lq))
+    U, L = U0.clone(), L0.clone()
+    bsm.bs_smooth_bounds(U, L, flags=flags)          # first call on the device: set-up
+    t.cuda.synchronize()
+    s = t.cuda.Stream()
+    g = t.cuda.CUDAGraph()
+    U.copy_(U0)
+    L.copy_(L0)
+    t.cuda.synchronize()
+    with t.cuda.graph(g, stream=s):
+        bsm.bs_smooth_bounds(U, L, flags=flags)
+    for _ in range(2):
+        U.copy_(U0)
+        L.copy_(L0)
+        g.replay()
+        t.cuda.synchronize()
+        assert same_bits(host(U), Uo) and same_bits(host(L), Lo)
+
+
 def test_literal_rule_rejected_in_blocked_mode():
     U, L = dev(np.zeros((4, 4), np.float32)), dev(np.zeros((4, 4), np.float32))
     with pytest.raises(bsm.BSError) as e:
