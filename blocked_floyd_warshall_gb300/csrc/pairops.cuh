@@ -1,6 +1,5 @@
-// Helpers shared by the blocked kernels: cp.async staging, the micro-tile
-// shapes of each phase, the paired middle-atom instructions, and the loop over
-// batch chunks of a launch.
+// Helpers shared by the blocked kernels: cp.async staging, the paired
+// middle-atom instructions, and the loop over batch chunks of a launch.
 #pragma once
 
 #include <type_traits>
@@ -20,16 +19,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-
-// Micro-tile shapes.  Phases 1 and 2 advance one (or two) middle atoms per
-// barrier, so they want more threads with fewer cells each: 4 x 4 cells on
-// 64-wide tiles (256 threads); on 128-wide tiles phase 2 runs 8 x 4 (512
-// threads) and phase 1 8 x 8 (256 threads), the faster shape for each measured
-// on the GB300.  Phase 3 has no barrier per step and wants many cells per
-// thread: 8 x 8 (64 or 256 threads).
-template <int FB> using P1S = Shape<FB, (FB == FB_SMALL ? 4 : 8), (FB == FB_SMALL ? 4 : 8)>;
-template <int FB> using P12 = Shape<FB, (FB == FB_SMALL ? 4 : 8), 4>;
-template <int FB> using P3S = Shape<FB, 8, 8>;
 
 // ---------------------------------------------------------------- paired middle atoms
 

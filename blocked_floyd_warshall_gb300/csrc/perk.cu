@@ -4,7 +4,8 @@
 //
 // Round k reads only row k and column k.  Round-synchronous semantics without
 // a second matrix: k_round updates every cell OUTSIDE row k and column k, so
-// nothing it reads is written during the launch; k_cross then updates row k
+// nothing it reads changes during the launch (the 16-byte store that covers
+// column k writes that lane back unchanged); k_cross then updates row k
 // and column k, whose new values depend only on themselves, L[k,k] and U
 // (all unchanged by round k: U[i,k] + U[k,k] = U[i,k] because U[k,k] = 0).
 //   cell (i,k): L[i,k] <- max(L[i,k], L[k,k] - U[i,k])

@@ -28,6 +28,14 @@
 
 namespace bs {
 
+// Micro-tile shapes.  Phases 1 and 2 advance one (phase 2: two) middle atoms
+// per barrier, so their per-step latency, not their throughput, sets their
+// time: 4 x 4 cells per thread on 64-wide tiles (256 threads); on 128-wide
+// tiles phase 1 runs 8 x 8 (256 threads) and phase 2 8 x 4 (512 threads), the
+// faster shape for each measured on the GB300.
+template <int FB> using P1S = Shape<FB, (FB == FB_SMALL ? 4 : 8), (FB == FB_SMALL ? 4 : 8)>;
+template <int FB> using P2S = Shape<FB, (FB == FB_SMALL ? 4 : 8), 4>;
+
 // ---------------------------------------------------------------- phase 1
 
 template <class T, bool HAS_L, int FB>
@@ -101,10 +109,10 @@ constexpr int DPAD = 2;   // diagonal tile row stride FB + DPAD: even, so pairs 
 
 // Row panel: the owner of rows k, k+1 publishes (row k, row k+1 after step k).
 template <class T, bool HAS_L, int FB>
-__device__ __forceinline__ void p2_publish_rows(const T (&u)[P12<FB>::TM][P12<FB>::TN],
-                                                const T (&l)[P12<FB>::TM][P12<FB>::TN], int k,
+__device__ __forceinline__ void p2_publish_rows(const T (&u)[P2S<FB>::TM][P2S<FB>::TN],
+                                                const T (&l)[P2S<FB>::TM][P2S<FB>::TN], int k,
                                                 const T* dU, const T* dL, T* sU, T* sL) {
-    using S = P12<FB>;
+    using S = P2S<FB>;
     using E = El<T>;
     constexpr int DS = FB + DPAD;
     const int r0 = S::row0();
@@ -130,10 +138,10 @@ __device__ __forceinline__ void p2_publish_rows(const T (&u)[P12<FB>::TM][P12<FB
 // U'[i,k+1]) and the closure-raised column values (Lc_k[i], Lc_k+1[i]).
 // dU, dL: the diagonal tile, k-interleaved.
 template <class T, bool HAS_L, int FB>
-__device__ __forceinline__ void p2_publish_cols(const T (&u)[P12<FB>::TM][P12<FB>::TN],
-                                                const T (&l)[P12<FB>::TM][P12<FB>::TN], int k,
+__device__ __forceinline__ void p2_publish_cols(const T (&u)[P2S<FB>::TM][P2S<FB>::TN],
+                                                const T (&l)[P2S<FB>::TM][P2S<FB>::TN], int k,
                                                 const T* dU, const T* dL, T* sU, T* sL) {
-    using S = P12<FB>;
+    using S = P2S<FB>;
     using E = El<T>;
     const int r0 = S::row0();
 #pragma unroll
@@ -164,7 +172,7 @@ template <class T, bool HAS_L, int FB>
 __device__ __forceinline__ void p2_row_panel(T* U, T* L, size_t ld, int o, int op, int mk,
                                              int mp, bool vec, bool sym, T* dU, T* dL,
                                              T (*sU)[2 * FB], T (*sL)[2 * FB]) {
-    using S = P12<FB>;
+    using S = P2S<FB>;
     using E = El<T>;
     using LD = PairLoad<T>;
     using P = typename LD::P;
@@ -230,7 +238,7 @@ template <class T, bool HAS_L, int FB>
 __device__ __forceinline__ void p2_col_panel(T* U, T* L, size_t ld, int o, int op, int mk,
                                              int mp, bool vec, T* dU, T* dL,
                                              T (*sU)[2 * FB], T (*sL)[2 * FB]) {
-    using S = P12<FB>;
+    using S = P2S<FB>;
     using E = El<T>;
     using LD = PairLoad<T>;
     using P = typename LD::P;
@@ -288,12 +296,12 @@ __device__ __forceinline__ void p2_col_panel(T* U, T* L, size_t ld, int o, int o
 }
 
 template <class T, bool HAS_L, int FB>
-__global__ void __launch_bounds__(P12<FB>::NT)
+__global__ void __launch_bounds__(P2S<FB>::NT)
 k_phase2(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec,
          bool sym) {
-    using S = P12<FB>;
+    using S = P2S<FB>;
     using E = El<T>;
-    constexpr int NT = P12<FB>::NT;
+    constexpr int NT = P2S<FB>::NT;
     constexpr int DS = FB + DPAD;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* dU = reinterpret_cast<T*>(smem_raw);
@@ -373,7 +381,7 @@ static cudaError_t phase2_t(const Mats& m, int K, cudaStream_t s) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
         before_launch(s, PH_TWO);
-        k_phase2<T, HAS_L, FB><<<dim3(nb - 1, m.sym ? 1 : 2, nbz), P12<FB>::NT,
+        k_phase2<T, HAS_L, FB><<<dim3(nb - 1, m.sym ? 1 : 2, nbz), P2S<FB>::NT,
                                  p2_smem<T, HAS_L, FB>(), s>>>(U, L, m.n, m.ld, m.bstride, K,
                                                               m.vec, m.sym);
         after_launch(s, PH_TWO);

@@ -4,6 +4,10 @@
 
 namespace bs {
 
+// Micro-tile shape: no barrier per step, so many cells per thread (fewest
+// shared-memory loads per cell update): 8 x 8 (64 or 256 threads).
+template <int FB> using P3S = Shape<FB, 8, 8>;
+
 // ---------------------------------------------------------------- phase 3
 //
 // Phase 3 updates tile (I,J) from the finished column panel (I,K) and row

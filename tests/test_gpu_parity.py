@@ -202,6 +202,97 @@ def test_fp32_off_grid_within_tolerance(n, p_bad, sched):
     assert np.max(np.abs(Uf.astype(np.float64) - Uo)) <= np.max(Uo) * (n - 1) * 2.0 ** -24
 
 
+# ------------------------------------------------------------------ edge cases
+
+
+def edge_cases():
+    """Degenerate inputs the method admits (each pair: U, L as Q10 int32)."""
+    cases = {}
+    n = 150
+    # int32 at the precondition ceiling: unknown U = 2^30 - 1, long known bonds
+    U, L = W.random_bounds(n, 9400, p_known=0.05, p_bad=0.01)
+    U = np.where(U == W.sentinel_q(n), (1 << 30) - 1, U).astype(np.int32)
+    big = np.random.default_rng(1).random((n, n)) < 0.02
+    U = np.where(big & (U < (1 << 29)), U + (1 << 28), U).astype(np.int32)
+    U = np.minimum(U, U.T)
+    np.fill_diagonal(U, 0)
+    cases["int32_ceiling"] = (U, L)
+    # zero-length bonds: distinct atoms at the same place
+    U, L = W.random_bounds(n, 9401, p_known=0.3)
+    z = np.random.default_rng(2).random((n, n)) < 0.01
+    z = z | z.T
+    U = np.where(z, 0, U).astype(np.int32)
+    L = np.where(z, 0, L).astype(np.int32)
+    cases["zero_bonds"] = (U, L)
+    # two disconnected molecules: no path between the halves
+    U, L = W.blank_bounds(n)
+    h = n // 2
+    Ua, La = W.random_bounds(h, 9402, p_known=0.3)
+    Ub, Lb = W.random_bounds(n - h, 9403, p_known=0.3)
+    U[:h, :h], L[:h, :h] = Ua, La
+    U[h:, h:], L[h:, h:] = Ub, Lb
+    cases["disconnected"] = (U, L)
+    # nothing known
+    cases["all_unknown"] = W.blank_bounds(n)
+    return cases
+
+
+@pytest.mark.parametrize("case", sorted(edge_cases()))
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
+def test_edge_cases(case, algo):
+    Uq, Lq = edge_cases()[case]
+    flags = bsm.BS_PERK if algo == "perk" else SCHEDULES[algo]
+    for U0, L0 in ((Uq, Lq), (W.to_f32(Uq), W.to_f32(Lq))):
+        if case == "int32_ceiling" and U0.dtype == np.float32:
+            continue                      # above 2^24 units the fp32 grid is not exact
+        Uo, Lo = oracle.smooth(U0, L0)
+        Ug, Lg, ok = gpu_bounds(U0, L0, flags)
+        assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
+    if case == "all_unknown":
+        np.testing.assert_array_equal(Uo, Uq.astype(Uo.dtype) / (1 if Uo.dtype == np.int32 else 1024))
+
+
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
+def test_infinite_upper_bounds(algo):
+    """fp32 U may be +inf for unknown pairs; inf + x = inf never wins."""
+    Uq, Lq = W.random_bounds(200, 9500, p_known=0.1, p_bad=0.01)
+    Uq[190:, :] = Lq[190:, :] = 0
+    Uq[:, 190:] = Lq[:, 190:] = 0
+    Uq[190:, :] = W.sentinel_q(200)              # atoms 190.. are constrained by nothing
+    Uq[:, 190:] = W.sentinel_q(200)
+    Lq[190:, :] = 1024
+    Lq[:, 190:] = 1024
+    np.fill_diagonal(Uq, 0)
+    np.fill_diagonal(Lq, 0)
+    U0, L0 = W.to_f32(Uq), W.to_f32(Lq)
+    U0 = np.where(Uq == W.sentinel_q(200), np.float32(np.inf), U0).astype(np.float32)
+    Uo, Lo = oracle.smooth(U0, L0)
+    assert np.isinf(Uo).any()
+    Ug, Lg, ok = gpu_bounds(U0, L0, bsm.BS_PERK if algo == "perk" else SCHEDULES[algo])
+    assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
+def test_batch_beyond_grid_limit():
+    """More molecules than a grid's z dimension holds (65535): launches are
+    split in chunks; every molecule still matches a single-molecule call."""
+    t = torch()
+    B, n = 70000, 4
+    rng = np.random.default_rng(9600)
+    base = [W.random_bounds(n, 9600 + s, p_known=0.8, p_bad=0.1) for s in range(7)]
+    pick = rng.integers(0, 7, B)
+    Uq = np.stack([base[p][0] for p in pick])
+    Lq = np.stack([base[p][1] for p in pick])
+    U, L = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
+    bsm.bs_smooth_bounds_batched(U, L)
+    Ug, Lg = host(U), host(L)
+    ref = [oracle.smooth(W.to_f32(u), W.to_f32(l)) for u, l in base]
+    for b in (0, 1, 65534, 65535, 65536, B - 1) + tuple(rng.integers(0, B, 50)):
+        assert same_bits(Ug[b], ref[pick[b]][0]) and same_bits(Lg[b], ref[pick[b]][1])
+    counts = bsm.bs_check_feasible_noalloc(U[:4096], L[:4096])
+    assert counts == [oracle.count_infeasible(*ref[p]) for p in pick[:4096]]
+    del t
+
+
 # ------------------------------------------------------------------ benchmark molecules
 
 
