@@ -24,11 +24,19 @@ template <int FB> using P3S = Shape<FB, 8, 8>;
 // round-to-nearest fp32 add.  int32 uses the add-then-min/max forms
 // (__viaddmin_s32 / __viaddmax_s32).
 
-constexpr int BK = 16;        // middle atoms staged per pipeline stage
-constexpr int AST = BK + 4;   // column-panel row stride (elements); rows stay 16-byte aligned
+// Middle atoms staged per pipeline stage: 32 on 128-wide tiles (half the
+// barriers of 16; measured 5 % faster), 16 on 64-wide tiles (keeps four CTAs
+// per SM within shared memory).  The column panel's row stride BK + 4 keeps its
+// rows 16-byte aligned.
+template <int FB> struct P3K {
+    static constexpr int BK = FB == FB_LARGE ? 32 : 16;
+    static constexpr int AST = BK + 4;
+};
 
 template <class T, bool HAS_L, int FB>
 struct P3Smem {
+    static constexpr int BK = P3K<FB>::BK;
+    static constexpr int AST = P3K<FB>::AST;
     // one stage: column panel A[i][k] (FB x AST) and row panel B[k/2][j][k%2]
     static constexpr int A_ELEMS = FB * AST;
     static constexpr int B_ELEMS = BK * FB;
@@ -51,6 +59,7 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
     using E = El<T>;
     using SM = P3Smem<T, HAS_L, FB>;
     constexpr int NT = P3S<FB>::NT;
+    constexpr int BK = P3K<FB>::BK, AST = P3K<FB>::AST;
     T* AU = stage;
     T* BU = stage + SM::A_ELEMS;
     T* AL = HAS_L ? BU + SM::B_ELEMS : nullptr;
@@ -170,6 +179,7 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     using E = El<T>;
     using SM = P3Smem<T, HAS_L, FB>;
     using LD = PairLoad<T>;
+    constexpr int BK = P3K<FB>::BK, AST = P3K<FB>::AST;
     using P = typename LD::P;
     constexpr bool NEG = std::is_same<T, int>::value;   // int lower bound adds negated values
     extern __shared__ __align__(16) unsigned char smem_raw[];
