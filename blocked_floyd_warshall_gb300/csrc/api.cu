@@ -12,16 +12,17 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// A side stream and two events for the look-ahead schedule.  A call holds
+// A side stream and three events for the look-ahead schedule.  A call holds
 // one exclusively while it enqueues, so concurrent callers never share events.
 struct SideCtx {
     cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr;   // recorded on the caller's stream
-    cudaEvent_t join = nullptr;   // recorded on the side stream
+    cudaEvent_t main_done[2] = {nullptr, nullptr};   // on the caller's stream, by round parity
+    cudaEvent_t side_done = nullptr;                 // on the side stream
 };
 
 struct DeviceState {
     bool ready = false;                   // kernel attributes set
+    int sms = 0;                          // multiprocessor count
     unsigned long long* scratch = nullptr;  // [0] count, [1] validation flags
     std::vector<SideCtx> free_side;       // idle look-ahead contexts
 };
@@ -51,7 +52,8 @@ cudaError_t device_state(DeviceState** out) {
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState& d = g_dev[dev];
     if (!d.ready) {
-        e = bs::blocked_setup(false);
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = bs::blocked_setup(false);
         if (e == cudaSuccess) e = bs::blocked_setup(true);
         if (e != cudaSuccess) return e;
         d.ready = true;
@@ -91,11 +93,11 @@ cudaError_t acquire_side(DeviceState* d, SideCtx* out) {
     int lo = 0, hi = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, hi);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming);
+    for (cudaEvent_t* ev : {&c.main_done[0], &c.main_done[1], &c.side_done})
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {
-        if (c.join) cudaEventDestroy(c.join);
-        if (c.fork) cudaEventDestroy(c.fork);
+        for (cudaEvent_t ev : {c.main_done[0], c.main_done[1], c.side_done})
+            if (ev) cudaEventDestroy(ev);
         if (c.side) cudaStreamDestroy(c.side);
         return e;
     }
@@ -119,10 +121,17 @@ int choose_tile(int n, int batch, int mode) {
 
 // The blocked schedule.  Without look-ahead: for each block round K, phase 1,
 // phase 2, phase 3 on `s`.  With look-ahead (nb >= 3), phase 3 of round K is
-// split: the tiles of block-row/column K+1 first, then phases 1 and 2 of round
-// K+1 on the side stream while the remaining tiles of round K run on `s`.
-// The split is exact: those remaining tiles neither read nor write anything
-// phases 1 and 2 of round K+1 touch.
+// split into NEXT(K), the tiles of block-row/column K+1, and REST(K), the
+// others, and two streams run
+//   side: NEXT(K), phase 1 and phase 2 of round K+1   (highest priority)
+//   s   : REST(K)
+// concurrently.  NEXT(K) waits for REST(K-1) (it rewrites tiles REST(K-1)
+// reads as panels), REST(K) for phase 2 of round K.  REST(K) touches no tile
+// the side stream reads or writes in the meantime: it reads block-row and
+// -column K, which phase 2 of round K+1 does not write except tiles (K,K+1)
+// and (K+1,K), which REST(K) does not read; it writes tiles outside
+// block-rows and -columns K and K+1.  NEXT(K)'s short wave thus overlaps
+// REST(K) instead of running alone.
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
                         bool force, DeviceState* d) {
     const int nb = (m.n + m.fb - 1) / m.fb;
@@ -145,23 +154,33 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
     SideCtx c;
     e = acquire_side(d, &c);
     if (e != cudaSuccess) return e;
-    for (int K = 0; K < nb && e == cudaSuccess; ++K) {
-        if (K + 1 == nb) {
-            e = bs::launch_phase3(is_int, m, K, bs::P3_ALL, s);
-            break;
+    // main_done[1] stands for "REST(-1)": everything enqueued on s so far.
+    e = cudaEventRecord(c.main_done[1], s);
+    bool forked = false;   // side work enqueued that s has not yet waited for
+    for (int K = 0; K + 1 < nb && e == cudaSuccess; ++K) {
+        if (forked) {
+            e = cudaStreamWaitEvent(s, c.side_done, 0);   // phase 2 of round K
+            forked = false;
         }
-        e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT, s);
-        if (e == cudaSuccess) e = cudaEventRecord(c.fork, s);
+        if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, bs::P3_REST, s);
+        if (e == cudaSuccess) e = cudaEventRecord(c.main_done[K & 1], s);
         if (e != cudaSuccess) break;
-        // from here on the side stream is forked: always join it back
-        e = cudaStreamWaitEvent(c.side, c.fork, 0);
+        // side: after REST(K-1), NEXT(K) then phases 1 and 2 of round K+1
+        e = cudaStreamWaitEvent(c.side, c.main_done[(K + 1) & 1], 0);
+        if (e != cudaSuccess) break;
+        forked = true;
+        e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT, c.side);
         if (e == cudaSuccess) e = bs::launch_phase1(is_int, m, K + 1, c.side);
         if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K + 1, c.side);
-        cudaError_t j = cudaEventRecord(c.join, c.side);
-        if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, bs::P3_REST, s);
-        if (j == cudaSuccess) j = cudaStreamWaitEvent(s, c.join, 0);
+        cudaError_t r = cudaEventRecord(c.side_done, c.side);
+        if (e == cudaSuccess) e = r;
+    }
+    // always join the side stream back, on success or failure
+    if (forked) {
+        cudaError_t j = cudaStreamWaitEvent(s, c.side_done, 0);
         if (e == cudaSuccess) e = j;
     }
+    if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, nb - 1, bs::P3_ALL, s);
     release_side(d, c);
     return e;
 }
@@ -198,6 +217,7 @@ bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
              (batch <= 1 || bstride % 4 == 0);
     m->fb = choose_tile(n, batch, mode);
     m->sym = (mode & BS_SYMMETRIC) != 0;
+    m->sms = 1;
     return BS_OK;
 }
 
@@ -230,6 +250,7 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
     const bool is_int = (mode & BS_DTYPE_MASK) == BS_INT32_Q10;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return BS_ERR_CUDA;
+    m.sms = d->sms;
     if (mode & BS_VALIDATE) {
         st = validate(m, is_int, s);
         if (st != BS_OK) return st;

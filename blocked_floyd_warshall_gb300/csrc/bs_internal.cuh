@@ -22,6 +22,7 @@ struct Mats {
     bool vec;             // 16-byte vector IO allowed (ld % 4 == 0, bases 16B-aligned)
     int fb;               // blocked mode: tile size FB_LARGE or FB_SMALL
     bool sym;             // blocked mode: inputs symmetric, compute half and mirror
+    int sms;              // multiprocessors of the device
 };
 
 enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3 };
@@ -44,7 +45,7 @@ cudaError_t launch_phase1(bool is_int, const Mats& m, int K, cudaStream_t s);
 cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
 // Phase 3 of block round K over the tiles `part` selects (P3_* below).
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s);
-enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2 };
+enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2, P3_PANELS = 3 };
 
 // Feasibility count and precondition checks.  `count` and `flags` are device
 // words the caller has zeroed on `s`.

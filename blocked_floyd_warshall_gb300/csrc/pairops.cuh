@@ -76,6 +76,10 @@ template <> struct PairLoad<float> {
         y = v.y;
     }
     static __device__ __forceinline__ P neg(P x) { return x; }
+    static __device__ __forceinline__ P mk(float lo, float hi) {
+        return (unsigned long long)__float_as_uint(lo) |
+               ((unsigned long long)__float_as_uint(hi) << 32);
+    }
 };
 template <> struct PairLoad<int> {
     using P = int2;
@@ -86,6 +90,7 @@ template <> struct PairLoad<int> {
         y = make_int2(v.z, v.w);
     }
     static __device__ __forceinline__ P neg(P x) { return make_int2(-x.x, -x.y); }
+    static __device__ __forceinline__ P mk(int lo, int hi) { return make_int2(lo, hi); }
 };
 
 // Launch `launch(first, count)` over the batch in chunks the grid's z dimension

@@ -1,17 +1,24 @@
-// Phase 3 of the three-phase blocked Floyd-Warshall: the bulk tile update.
-// (The schedule as a whole is described at the top of phase12.cu.)
+// Phases 2 and 3 of the three-phase blocked Floyd-Warshall: the panel and
+// bulk tile updates, one kernel.  (The schedule as a whole, and why the panels
+// are the same product as the bulk tiles, is described at the top of
+// phase1.cu.)
 #include "pairops.cuh"
 
 namespace bs {
 
 // Micro-tile shape: no barrier per step, so many cells per thread (fewest
-// shared-memory loads per cell update): 8 x 8 (64 or 256 threads).
-template <int FB> using P3S = Shape<FB, 8, 8>;
+// shared-memory loads per cell update): 8 x 8 (64 or 256 threads).  When a
+// launch has too few tiles to fill the GPU, each CTA is latency-bound; the
+// wide form of the 64-wide tile then spreads it over 256 threads (4 x 4 cells
+// each), four times the warps per tile.
+template <int FB, bool WIDE> using P3S = Shape<FB, (WIDE ? 4 : 8), (WIDE ? 4 : 8)>;
 
 // ---------------------------------------------------------------- phase 3
 //
-// Phase 3 updates tile (I,J) from the finished column panel (I,K) and row
-// panel (K,J).  Both are streamed through shared memory in chunks of BK
+// The kernel updates tile (I,J) from the column operand (I,K) and the row
+// operand (K,J): in phase 3 the finished panels; in phase 2 the finished
+// diagonal tile (K,K) and the panel tile itself, read before the CTA writes it
+// (no other CTA touches it).  Both are streamed through shared memory in chunks of BK
 // middle atoms (two stages, cp.async).  The inner loop takes the middle atoms
 // two at a time: a thread holds, per row r, the pair (U[i,k], U[i,k+1]) in one
 // 64-bit register (the column panel is stored [i][k], so the pair is one
@@ -51,14 +58,12 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
 }
 
 // Stage k-chunk `c` of both panels into shared memory stage `stage`.
-template <class T, bool HAS_L, int FB>
+template <class T, bool HAS_L, int FB, int NT>
 __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_t ld, int oi,
                                          int oj, int ok, int mi, int mj, int mk, int c,
                                          bool vec) {
-    using S = P3S<FB>;
     using E = El<T>;
     using SM = P3Smem<T, HAS_L, FB>;
-    constexpr int NT = P3S<FB>::NT;
     constexpr int BK = P3K<FB>::BK, AST = P3K<FB>::AST;
     T* AU = stage;
     T* BU = stage + SM::A_ELEMS;
@@ -111,13 +116,15 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
     }
 }
 
-// Which tiles a phase-3 launch covers (block round K, nb tile rows):
-//   P3_ALL  : every tile outside block-row K and block-column K;
-//   P3_NEXT : those in block-row K+1 or block-column K+1 (the tiles the next
-//             block round's phases 1 and 2 read and write);
-//   P3_REST : the others.
+// Which tiles a launch covers (block round K, nb tile rows):
+//   P3_ALL    : every tile outside block-row K and block-column K;
+//   P3_NEXT   : those in block-row K+1 or block-column K+1 (the tiles the next
+//               block round's phases 1 and 2 read and write);
+//   P3_REST   : the others;
+//   P3_PANELS : phase 2, the row panel (K,J) then the column panel (I,K).
 // With symmetric inputs only tiles with I <= J are computed (each off-diagonal
-// one is also stored transposed): (nb-1)nb/2, nb-1 and (nb-2)(nb-1)/2 tiles.
+// one is also stored transposed): (nb-1)nb/2, nb-1 and (nb-2)(nb-1)/2 tiles;
+// phase 2 computes the row panel and stores it transposed as the column panel.
 
 // t -> (a, b), a <= b, enumerating the upper triangle column by column.
 __device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
@@ -130,6 +137,17 @@ __device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
 
 __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K, int& I,
                                         int& J) {
+    if (part == P3_PANELS) {
+        if (t < nb - 1) {
+            I = K;
+            J = t + (t >= K);
+        } else {
+            const int u = t - (nb - 1);
+            I = u + (u >= K);
+            J = K;
+        }
+        return;
+    }
     if (!sym) {
         if (part == P3_ALL) {
             const int ti = t / (nb - 1), tj = t % (nb - 1);
@@ -171,11 +189,11 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
     }
 }
 
-template <class T, bool HAS_L, int FB>
-__global__ void __launch_bounds__(P3S<FB>::NT)
+template <class T, bool HAS_L, int FB, bool WIDE>
+__global__ void __launch_bounds__(P3S<FB, WIDE>::NT)
 k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K,
          int part, bool vec, bool sym) {
-    using S = P3S<FB>;
+    using S = P3S<FB, WIDE>;
     using E = El<T>;
     using SM = P3Smem<T, HAS_L, FB>;
     using LD = PairLoad<T>;
@@ -199,13 +217,13 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     if (HAS_L) load_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
 
     const int nchunks = (mk + BK - 1) / BK;
-    p3_stage<T, HAS_L, FB>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
+    p3_stage<T, HAS_L, FB, S::NT>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
     cp_async_commit();
     const int r0 = S::row0(), cq = S::cq();
     for (int c = 0; c < nchunks; ++c) {
         if (c + 1 < nchunks)
-            p3_stage<T, HAS_L, FB>(sm + ((c + 1) & 1) * SM::STAGE, U, L, ld, oi, oj, ok, mi, mj,
-                                   mk, c + 1, vec);
+            p3_stage<T, HAS_L, FB, S::NT>(sm + ((c + 1) & 1) * SM::STAGE, U, L, ld, oi, oj, ok,
+                                          mi, mj, mk, c + 1, vec);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
@@ -269,10 +287,12 @@ static cudaError_t setup3() {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     };
-    set(k_phase3<T, true, FB_LARGE>, P3Smem<T, true, FB_LARGE>::BYTES);
-    set(k_phase3<T, false, FB_LARGE>, P3Smem<T, false, FB_LARGE>::BYTES);
-    set(k_phase3<T, true, FB_SMALL>, P3Smem<T, true, FB_SMALL>::BYTES);
-    set(k_phase3<T, false, FB_SMALL>, P3Smem<T, false, FB_SMALL>::BYTES);
+    set(k_phase3<T, true, FB_LARGE, false>, P3Smem<T, true, FB_LARGE>::BYTES);
+    set(k_phase3<T, false, FB_LARGE, false>, P3Smem<T, false, FB_LARGE>::BYTES);
+    set(k_phase3<T, true, FB_SMALL, false>, P3Smem<T, true, FB_SMALL>::BYTES);
+    set(k_phase3<T, false, FB_SMALL, false>, P3Smem<T, false, FB_SMALL>::BYTES);
+    set(k_phase3<T, true, FB_SMALL, true>, P3Smem<T, true, FB_SMALL>::BYTES);
+    set(k_phase3<T, false, FB_SMALL, true>, P3Smem<T, false, FB_SMALL>::BYTES);
     return e;
 }
 
@@ -281,6 +301,7 @@ cudaError_t phase3_setup(bool is_int) { return is_int ? setup3<int>() : setup3<f
 // Tiles a phase-3 launch covers (see p3_tile).
 static int p3_tiles(bool sym, int part, int nb, int K) {
     if (nb < 2) return 0;
+    if (part == P3_PANELS) return sym ? nb - 1 : 2 * (nb - 1);
     if (sym)
         return part == P3_ALL ? (nb - 1) * nb / 2
                : part == P3_NEXT ? (K + 1 < nb ? nb - 1 : 0)
@@ -290,7 +311,7 @@ static int p3_tiles(bool sym, int part, int nb, int K) {
                              : (K + 1 < nb ? (nb - 2) * (nb - 2) : 0);
 }
 
-template <class T, bool HAS_L, int FB>
+template <class T, bool HAS_L, int FB, bool WIDE>
 static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {
     const int nb = (m.n + FB - 1) / FB;
     const int tiles = p3_tiles(m.sym, part, nb, K);
@@ -298,22 +319,32 @@ static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {
     return for_batch_chunks(m, [&](int b0, int nbz) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
-        before_launch(s, PH_THREE);
-        k_phase3<T, HAS_L, FB><<<dim3(tiles, 1, nbz), P3S<FB>::NT, P3Smem<T, HAS_L, FB>::BYTES, s>>>(
+        const Phase ph = part == P3_PANELS ? PH_TWO : PH_THREE;
+        before_launch(s, ph);
+        k_phase3<T, HAS_L, FB, WIDE><<<dim3(tiles, 1, nbz), P3S<FB, WIDE>::NT,
+                                       P3Smem<T, HAS_L, FB>::BYTES, s>>>(
             U, L, m.n, m.ld, m.bstride, K, part, m.vec, m.sym);
-        after_launch(s, PH_THREE);
+        after_launch(s, ph);
     });
 }
 
+// The wide form for 64-wide tiles when the launch has at most two CTAs per SM.
 template <class T, bool HAS_L>
 static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
-    return m.fb == FB_SMALL ? phase3_t<T, HAS_L, FB_SMALL>(m, K, part, s)
-                            : phase3_t<T, HAS_L, FB_LARGE>(m, K, part, s);
+    if (m.fb == FB_LARGE) return phase3_t<T, HAS_L, FB_LARGE, false>(m, K, part, s);
+    const int nb = (m.n + FB_SMALL - 1) / FB_SMALL;
+    const double ctas = (double)p3_tiles(m.sym, part, nb, K) * m.batch;
+    return ctas <= 2.0 * m.sms ? phase3_t<T, HAS_L, FB_SMALL, true>(m, K, part, s)
+                               : phase3_t<T, HAS_L, FB_SMALL, false>(m, K, part, s);
 }
 
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s) {
     if (is_int) return m.L ? phase3_fb<int, true>(m, K, part, s) : phase3_fb<int, false>(m, K, part, s);
     return m.L ? phase3_fb<float, true>(m, K, part, s) : phase3_fb<float, false>(m, K, part, s);
+}
+
+cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s) {
+    return launch_phase3(is_int, m, K, P3_PANELS, s);
 }
 
 }  // namespace bs
