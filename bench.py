@@ -49,13 +49,14 @@ def make_workload(name):
     return globule_bounds(wl["box"], wl["seed"], wl["p_long"])
 
 
-def tile_size(n, flags=0):
+def tile_size(n, flags=0, batch=1):
     """Tile size the library picks (mirrors its rule; forced by the tile bits)."""
     if flags & (1 << 5):
         return 64
     if flags & (1 << 6):
         return 128
-    return 64 if n <= 3072 else 128
+    nb = (n + 127) // 128
+    return 128 if (nb - 1) ** 2 * batch >= 768 else 64
 
 
 def phase_cells(n, fb, sym=False):
@@ -76,6 +77,21 @@ def phase_cells(n, fb, sym=False):
         else:
             p3 += rest * rest * mk
     return p1, p2, p3
+
+
+def next_cells(n, fb):
+    """Cell updates of the look-ahead launches of one blocked smoothing: the
+    tiles of block row and column K+1 (outside row and column K) in block
+    rounds K < nb - 1.  They run on the library's side stream; the rest of
+    phase 3 runs on the caller's stream."""
+    nb = (n + fb - 1) // fb
+    sizes = [min(fb, n - K * fb) for K in range(nb)]
+    cells = 0
+    for K in range(nb - 1):
+        mk, s1 = sizes[K], sizes[K + 1]
+        other = n - mk - s1
+        cells += mk * s1 * (2 * other + s1)
+    return cells
 
 
 def load_peaks():
@@ -99,10 +115,10 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(n, fb=128):
-    """DRAM bytes of phase 3 per smoothing step from the committed ncu summary
-    (bytes per cell update x the step's phase-3 cell updates), if the summary
-    was taken on the current kernel source; else None."""
+def committed_traffic(cells):
+    """DRAM bytes of phase-3 launches covering `cells` cell updates, from the
+    committed ncu summary (bytes per cell update x cells), if the summary was
+    taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "phase3_traffic.json")
     if not os.path.exists(p):
         return None
@@ -113,7 +129,7 @@ def committed_traffic(n, fb=128):
     per_cell_k = d.get("dram_bytes_per_cell_k")
     if per_cell_k is None:
         return None
-    return per_cell_k * float(phase_cells(n, fb)[2])
+    return per_cell_k * float(cells)
 
 
 # ------------------------------------------------------------------ clocks
@@ -365,13 +381,16 @@ def main():
     peaks = load_peaks()
     fmax = peaks["sm_max_mhz"] * 1e6
     alu_peak_ops = sms * FP32_LANES_PER_SM * fmax            # ALU ops/s
+    # phase 3 on the caller's stream (the rest of each block round, and the
+    # last round whole): these launches never overlap one another
     p3 = prof["phase3"]
     fb = tile_size(n)
     p3_cells_step = phase_cells(n, fb)[2]
-    p3_ops_step = p3_cells_step * OPS_PER_CELL
+    main_cells_step = p3_cells_step - (next_cells(n, fb) if prof["phase3_next"]["launches"] else 0)
+    p3_ops_step = main_cells_step * OPS_PER_CELL
     p3_s_step = p3["ms"] * 1e-3 / args.steps
     p3_achieved = p3_ops_step / p3_s_step if p3["launches"] else None
-    traffic = committed_traffic(n, fb)
+    traffic = committed_traffic(main_cells_step)
     clocks = clk.summary()
 
     line = {
@@ -393,15 +412,18 @@ def main():
             "peak": alu_peak_ops / 1e12, "unit": "Tops/s",
             "frac": (p3_achieved / alu_peak_ops) if p3_achieved else None,
             "traffic": traffic,
-            "traffic_basis": "DRAM bytes of all phase-3 launches of one smoothing step",
+            "traffic_basis": "DRAM bytes of the same launches in one smoothing step (ncu bytes "
+                             "per cell update, profiles/phase3_traffic.json, x their cell updates)",
             "ops_per_step": p3_ops_step,
+            "cells_share_of_phase3": main_cells_step / p3_cells_step,
             "ms_per_step": p3_s_step * 1e3,
             "launches_per_step": p3["launches"] / args.steps,
-            "achieved_basis": "6 ops x phase-3 cell updates of one step / summed device time of "
-                              "that step's phase-3 launches (each launch timed with CUDA events "
-                              "on its stream; phases 1-2 of the next round run concurrently on a "
-                              "side stream, so this understates the kernel alone)",
-            "share_of_step": p3["ms"] / max(1e-9, sum(prof[k]["ms"] for k in bsm.PHASES)),
+            "achieved_basis": "6 ops x cell updates of the step's phase-3 launches on the caller's "
+                              "stream (all but the next block row and column of each round) / "
+                              "their summed device time, each launch timed with CUDA events on "
+                              "that stream; the look-ahead stream's kernels share the GPU with "
+                              "them meanwhile, so this understates the kernel alone",
+            "share_of_step": p3["ms"] / args.steps / (total_ms / args.steps),
             "peak_basis": "SMs x 128 FP32 lanes x max SM clock, 6 ALU ops per cell update (%s)"
                           % peaks["source"],
         },
@@ -495,7 +517,7 @@ def sweep(args):
                     "ms_median": ms, "ms_best": min(times), "cell_updates_per_s": rate,
                     "fp32_alu_frac": rate * OPS_PER_CELL / alu}
             if algo == "sym":
-                executed = batch * float(sum(phase_cells(n, tile_size(n, flags), sym=True)))
+                executed = batch * float(sum(phase_cells(n, tile_size(n, flags, batch), sym=True)))
                 line["executed_cell_updates"] = executed
                 line["fp32_alu_frac_executed"] = executed / (ms * 1e-3) * OPS_PER_CELL / alu
             if algo == "perk":

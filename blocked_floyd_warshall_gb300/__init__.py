@@ -48,7 +48,7 @@ BS_NO_LOOKAHEAD = 1 << 7
 BS_SYMMETRIC = 1 << 8
 BS_FORCE_LOOKAHEAD = 1 << 9
 
-PHASES = ("round", "phase1", "phase2", "phase3")
+PHASES = ("round", "phase1", "phase2", "phase3", "phase3_next")
 
 PROBES = {"fadd": 0, "fmnmx": 1, "fmnmx3": 2, "fadd2": 3, "fadd2+fmnmx3": 4,
           "iadd": 5, "imnmx": 6, "viaddmin": 7, "vimnmx3": 8}
@@ -61,7 +61,7 @@ class BSError(RuntimeError):
 
 
 class _Profile(ctypes.Structure):
-    _fields_ = [("ms", ctypes.c_double * 4), ("launches", ctypes.c_longlong * 4),
+    _fields_ = [("ms", ctypes.c_double * 5), ("launches", ctypes.c_longlong * 5),
                 ("overflow", ctypes.c_int)]
 
 

@@ -110,13 +110,17 @@ void release_side(DeviceState* d, const SideCtx& c) {
     d->free_side.push_back(c);
 }
 
-// Tile size for the blocked schedule: 64 x 64 tiles for small matrices, where
-// the serial phases 1 and 2 dominate, 128 x 128 otherwise.
+// Tile size for the blocked schedule: 128 x 128 tiles (the faster phase-3
+// kernel) once a block round's phase 3 at that size holds at least 768 tiles
+// over the batch (about five per SM), else 64 x 64 (twice the block rounds,
+// but more tiles to spread and an eighth of the phase-1 work per round).
+// Measured on the GB300: n = 3000 is faster with 64, n = 4096 and 256
+// molecules of n = 512 with 128.
 int choose_tile(int n, int batch, int mode) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
     if (mode & BS_TILE_128) return bs::FB_LARGE;
-    (void)batch;
-    return n <= 3072 ? bs::FB_SMALL : bs::FB_LARGE;
+    const double nb = (double)((n + bs::FB_LARGE - 1) / bs::FB_LARGE);
+    return (nb - 1) * (nb - 1) * batch >= 768.0 ? bs::FB_LARGE : bs::FB_SMALL;
 }
 
 // The blocked schedule.  Without look-ahead: for each block round K, phase 1,
@@ -391,7 +395,7 @@ bs_status bs_profile_end(bs_profile* out) {
         float ms = 0.f;
         cudaError_t e = cudaEventSynchronize(r.b);
         if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
-        if (e == cudaSuccess && r.phase >= 0 && r.phase < 4) {
+        if (e == cudaSuccess && r.phase >= 0 && r.phase < BS_PROFILE_PHASES) {
             p.ms[r.phase] += ms;
             p.launches[r.phase] += 1;
         } else if (first == cudaSuccess) {

@@ -25,7 +25,8 @@ struct Mats {
     int sms;              // multiprocessors of the device
 };
 
-enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3 };
+// profile categories (the index of bs_profile's arrays)
+enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3, PH_NEXT = 4 };
 
 // Launch bookkeeping (api.cu): counts launches and, when profiling, records an
 // event pair around each launch on `s`.

@@ -319,7 +319,7 @@ static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {
     return for_batch_chunks(m, [&](int b0, int nbz) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
-        const Phase ph = part == P3_PANELS ? PH_TWO : PH_THREE;
+        const Phase ph = part == P3_PANELS ? PH_TWO : part == P3_NEXT ? PH_NEXT : PH_THREE;
         before_launch(s, ph);
         k_phase3<T, HAS_L, FB, WIDE><<<dim3(tiles, 1, nbz), P3S<FB, WIDE>::NT,
                                        P3Smem<T, HAS_L, FB>::BYTES, s>>>(

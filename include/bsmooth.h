@@ -169,14 +169,18 @@ bs_status bs_check_feasible_noalloc(const void *U, const void *L, int n, int ld,
 long long bs_launch_count(void);
 
 /* Per-phase device time.  After bs_profile_begin(), every smoothing call
- * records a CUDA event pair around each of its kernel launches on the
- * caller's stream.  bs_profile_end() waits for those events, writes the summed
- * milliseconds and launch counts per phase (index: 0 per-round kernels,
- * 1 phase 1, 2 phase 2, 3 phase 3) and stops recording.  At most 1<<16 launches
- * are recorded per session; more set *overflow to 1. */
+ * records a CUDA event pair around each of its kernel launches, on the stream
+ * the kernel runs on (the caller's, or the library's look-ahead stream).
+ * bs_profile_end() waits for those events, writes the summed milliseconds and
+ * launch counts per phase and stops recording.  Index: 0 per-round kernels,
+ * 1 phase 1, 2 phase 2, 3 phase 3 on the caller's stream, 4 phase 3 of the
+ * next block row and column on the look-ahead stream (these overlap index 3
+ * in time).  At most 1<<16 launches are recorded per session; more set
+ * *overflow to 1. */
+#define BS_PROFILE_PHASES 5
 typedef struct {
-    double ms[4];
-    long long launches[4];
+    double ms[BS_PROFILE_PHASES];
+    long long launches[BS_PROFILE_PHASES];
     int overflow;
 } bs_profile;
 
