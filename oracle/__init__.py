@@ -55,6 +55,8 @@ def _load():
             f.restype = c_int
         lib.oracle_closure_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp]
         lib.oracle_closure_rows.restype = c_int
+        lib.oracle_smooth_track_f64.argtypes = [vp, vp, vp, vp, vp, i64, i64]
+        lib.oracle_smooth_track_f64.restype = c_int
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = c_int
         for name in ("oracle_count_infeasible_f32", "oracle_count_infeasible_i32"):
@@ -105,6 +107,29 @@ def smooth(U: np.ndarray, L: np.ndarray | None = None, *, rule: int = RULE_CLOSU
     if rc != 0:
         raise ValueError("oracle_smooth: bad arguments (rc=%d)" % rc)
     return U, L
+
+
+def smooth_track(U0: np.ndarray, L0: np.ndarray):
+    """fp64 closure-rule smoothing that also returns each cell's path
+    provenance (see oracle_smooth_track_f64 in oracle.c).
+
+    Returns (U, L, HU, HL, ML): the smoothed bounds (float64), the fewest edges
+    of a shortest upper-bound path and of a best lower-bound path (int32), and
+    the sum of |edge weight| along that lower-bound path (float64).
+    """
+    lib = _load()
+    U = np.array(U0, dtype=np.float64, order="C")
+    L = np.array(L0, dtype=np.float64, order="C")
+    if U.ndim != 2 or U.shape[0] != U.shape[1] or L.shape != U.shape:
+        raise ValueError("U and L must be n x n")
+    n = U.shape[0]
+    HU = np.empty((n, n), np.int32)
+    HL = np.empty((n, n), np.int32)
+    ML = np.empty((n, n), np.float64)
+    rc = lib.oracle_smooth_track_f64(_ptr(U), _ptr(L), _ptr(HU), _ptr(HL), _ptr(ML), n, n)
+    if rc != 0:
+        raise ValueError("oracle_smooth_track_f64: bad arguments (rc=%d)" % rc)
+    return U, L, HU, HL, ML
 
 
 def smooth_upper(U: np.ndarray, **kw) -> np.ndarray:

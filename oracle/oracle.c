@@ -41,6 +41,12 @@
  * oracle_closure_rows() gives single rows of the fixed point at any size by a
  * different route (Dijkstra on the bound graph) for sampled checks of large
  * matrices.
+ *
+ * oracle_smooth_track_f64() is the fp64 closure-rule smoothing that also keeps,
+ * for every cell, which path its value is the length of: the number of edges
+ * and, for the lower bound, the sum of the magnitudes of the edge weights.
+ * Rounding bounds for fp32 results off the 1/1024 grid are stated in those
+ * terms (see that function).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -218,4 +224,113 @@ int oracle_closure_rows(const double *U0, const double *L0, int64_t n, int64_t l
         free(done); free(t);
     }
     return bad ? 1 : 0;
+}
+
+/*
+ * fp64 closure-rule smoothing with path provenance.
+ *
+ * Same rounds as oracle_smooth_f64 (ORACLE_RULE_CLOSURE, copies of row and
+ * column k taken at the start of round k), and in addition, per cell:
+ *   HU[i,j]  edges of a path i -> j whose upper-bound length is U[i,j];
+ *   HL[i,j]  edges of a path i' -> j'' (one -l edge, u edges before and after
+ *            it) whose length is -L[i,j];
+ *   ML[i,j]  the sum of |edge weight| along that path.
+ * A candidate formed through k combines the provenance of its two parts
+ * (edges add, magnitudes add; a u part contributes its own length, since u
+ * weights are >= 0).  Among candidates of equal length the one with fewer
+ * edges is kept, so HU and HL are the fewest edges over all shortest paths
+ * (lexicographic Floyd-Warshall).  Start: HU = 1 off the diagonal, 0 on it
+ * (the empty path); HL = 1 and ML = L0 everywhere (the single -l edge).
+ *
+ * Why these numbers bound rounding: every value a schedule computes is a
+ * rounded sum or difference of two computed values, and rounding is monotone,
+ * so the computed upper bound is at most the rounded length of a shortest
+ * path, summed in some order, and the computed lower bound at least that of
+ * the best lower-bound path.  A sum of h terms rounded in any order is within
+ * (h-1) u / (1 - (h-1) u) of the exact sum times the sum of the terms'
+ * magnitudes (u = unit roundoff).  U, L: n x n fp64 (row stride ld), updated
+ * in place; HU, HL: int32; ML: fp64, all with stride ld.
+ */
+int oracle_smooth_track_f64(double *U, double *L, int32_t *HU, int32_t *HL, double *ML,
+                            int64_t n, int64_t ld)
+{
+    if (n < 0 || ld < n) return 1;
+    if (n == 0) return 0;
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < n; ++j) {
+            HU[i * ld + j] = i == j ? 0 : 1;
+            HL[i * ld + j] = 1;
+            ML[i * ld + j] = L[i * ld + j];
+        }
+    size_t bytes = sizeof(double) * (size_t)n, ibytes = sizeof(int32_t) * (size_t)n;
+    double *urow = malloc(bytes), *ucol = malloc(bytes), *lrow = malloc(bytes),
+           *lcol = malloc(bytes), *mrow = malloc(bytes), *mcol = malloc(bytes);
+    int32_t *hurow = malloc(ibytes), *hucol = malloc(ibytes), *hlrow = malloc(ibytes),
+            *hlcol = malloc(ibytes);
+    int rc = 0;
+    if (!urow || !ucol || !lrow || !lcol || !mrow || !mcol || !hurow || !hucol || !hlrow ||
+        !hlcol) {
+        rc = 2;
+        goto out;
+    }
+    for (int64_t k = 0; k < n; ++k) {
+        for (int64_t j = 0; j < n; ++j) {
+            urow[j] = U[k * ld + j];
+            hurow[j] = HU[k * ld + j];
+            lrow[j] = L[k * ld + j];
+            hlrow[j] = HL[k * ld + j];
+            mrow[j] = ML[k * ld + j];
+        }
+        const double lkk = L[k * ld + k];
+        const int32_t hlkk = HL[k * ld + k];
+        const double mkk = ML[k * ld + k];
+        for (int64_t i = 0; i < n; ++i) {
+            ucol[i] = U[i * ld + k];
+            hucol[i] = HU[i * ld + k];
+            /* the column value, raised through the pair (k, k) */
+            double lc = L[i * ld + k], mc = ML[i * ld + k];
+            int32_t hc = HL[i * ld + k];
+            const double r = lkk - ucol[i];
+            const int32_t hr = hlkk + hucol[i];
+            if (r > lc || (r == lc && hr < hc)) {
+                lc = r;
+                hc = hr;
+                mc = mkk + ucol[i];
+            }
+            lcol[i] = lc;
+            hlcol[i] = hc;
+            mcol[i] = mc;
+        }
+        _Pragma("omp parallel for schedule(static)")
+        for (int64_t i = 0; i < n; ++i) {
+            for (int64_t j = 0; j < n; ++j) {
+                const int64_t c = i * ld + j;
+                const double s = ucol[i] + urow[j];
+                const int32_t hs = hucol[i] + hurow[j];
+                if (s < U[c] || (s == U[c] && hs < HU[c])) {
+                    U[c] = s;
+                    HU[c] = hs;
+                }
+                /* l_kj - u_ik, then lc_i - u_kj */
+                const double a = lrow[j] - ucol[i];
+                const int32_t ha = hlrow[j] + hucol[i];
+                const double b = lcol[i] - urow[j];
+                const int32_t hb = hlcol[i] + hurow[j];
+                if (a > L[c] || (a == L[c] && ha < HL[c])) {
+                    L[c] = a;
+                    HL[c] = ha;
+                    ML[c] = mrow[j] + ucol[i];
+                }
+                if (b > L[c] || (b == L[c] && hb < HL[c])) {
+                    L[c] = b;
+                    HL[c] = hb;
+                    ML[c] = mcol[i] + urow[j];
+                }
+            }
+        }
+    }
+out:
+    free(urow); free(ucol); free(lrow); free(lcol); free(mrow); free(mcol);
+    free(hurow); free(hucol); free(hlrow); free(hlcol);
+    return rc;
 }

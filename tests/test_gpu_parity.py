@@ -202,6 +202,42 @@ def test_fp32_off_grid_within_tolerance(n, p_bad, sched):
     assert np.max(np.abs(Uf.astype(np.float64) - Uo)) <= np.max(Uo) * (n - 1) * 2.0 ** -24
 
 
+def gamma(m):
+    """Relative rounding bound of a sum of m + 1 fp32 terms, any order."""
+    u = 2.0 ** -24
+    m = np.maximum(m, 0).astype(np.float64)
+    return m * u / (1 - m * u)
+
+
+@pytest.mark.parametrize("n,p_bad,seed", [(300, 0.0, 1), (300, 0.02, 2), (700, 0.01, 3),
+                                          (517, 0.005, 4)])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "sym", "perk"])
+def test_fp32_off_grid_per_cell_bound(n, p_bad, seed, sched):
+    """Off the 1/1024 grid, every fp32 cell against the fp64 oracle, with a
+    bound from the cell's own path (oracle provenance: edges h and summed
+    |weight| M of a best path).  Every computed value is a rounded sum or
+    difference of computed values and rounding is monotone, so
+      U: U64 (1 - g(n-2)) <= Ug <= U64 (1 + g(hU - 1))
+      L: L64 - g(hL - 1) M <= Lg <= L64 + g(n) (2 max L0 + 1)
+    with g(m) = m u / (1 - m u), u = 2^-24 (the second L bound: a path that
+    wins has no more u weight than twice its l weight).  Slack 1e-12 relative
+    covers the oracle's own fp64 rounding."""
+    U0, L0 = off_grid(n, 8000 + seed, p_bad)
+    U64, L64, HU, HL, ML = oracle.smooth_track(U0.astype(np.float64), L0.astype(np.float64))
+    flags = bsm.BS_PERK if sched == "perk" else SCHEDULES[sched]
+    Ug, Lg, ok = gpu_bounds(U0, L0, flags)
+    assert ok
+    Ug, Lg = Ug.astype(np.float64), Lg.astype(np.float64)
+    eps = 1e-12
+    assert np.all(Ug <= U64 * (1 + gamma(HU - 1)) * (1 + eps))
+    assert np.all(Ug >= U64 * (1 - gamma(np.full_like(HU, n - 2))) * (1 - eps))
+    assert np.all(Lg >= L64 - gamma(HL - 1) * ML * (1 + eps) - eps * ML)
+    top = gamma(np.array(n)) * (2 * float(L0.max()) + 1)
+    assert np.all(Lg <= L64 + top * (1 + eps))
+    # the per-cell bound lies inside the stated gate (1e-4 A or 1e-5 relative)
+    assert np.all((gamma(HU - 1) <= 1e-5) | (gamma(HU - 1) * U64 <= 1e-4))
+
+
 # ------------------------------------------------------------------ edge cases
 
 
