@@ -39,20 +39,20 @@ namespace bs {
 // Phase 1 computes the closure of tile (K,K) by the same blocked scheme one
 // level down, on the tile held in shared memory: for each SB-wide sub-block s
 // of its middle atoms,
-//   (a) one warp closes sub-block (s,s), k serially, exchanging row and column
-//       k by warp shuffles (no barrier per middle atom);
+//   (a) two warps close sub-block (s,s), k serially, exchanging row and
+//       column k through shared memory with a two-warp barrier per middle
+//       atom; for s > 0 this runs during (c) of s-1, on the two warps (c)
+//       leaves idle;
 //   (b) the sub-panels in sub-block row s and sub-block column s take the
 //       product with the closed sub-block (each cell computed into registers,
 //       written after a barrier, so every operand is the value from before);
 //   (c) every other cell takes the product of its sub-panels, paired middle
 //       atoms as in phase 3.
 // (b) and (c) are the update of the other phases, X[i,j] against T[i,k] and
-// T[k,j] over the sub-block's middle atoms k.  Four barriers per sub-block
+// T[k,j] over the sub-block's middle atoms k.  Three barriers per sub-block
 // instead of one per middle atom.
 
 constexpr int SB = 16;          // sub-block width
-constexpr int CPL = SB * SB / 32;  // (a): cells per lane
-constexpr int LPR = SB / CPL;      // (a): lanes per sub-block row
 constexpr int HALVES = SB / 8;     // (b): 8-cell units per sub-panel line
 
 // (c) micro-tile: 4 x 4 cells on 64-wide tiles (256 threads), 8 x 4 on 128-wide
@@ -71,59 +71,137 @@ struct P1Smem {
     static constexpr size_t BYTES = MATS * (TILE + RP + DI) * sizeof(T);   // tU tL | rU rL | dU dL
 };
 
-// (a): closure of the SB x SB sub-block at (sb, sb), one warp.  Lane
-// LPR*i + h holds row i, columns CPL*h .. CPL*h + CPL-1.  Step k: row k comes
-// from lanes LPR*k + h, column k of row i from lane LPR*i + k/CPL; all
-// shuffles precede the updates, so each step reads the values from before it
-// (round-synchronous), and the lower-bound column is raised by the closure
-// rule, Lc = max(L[i,k], L[k,k] - U[i,k]).  The closed sub-block is written
-// back row-major and k-interleaved (dU, dL) for the column sub-panel.
-template <class T, bool HAS_L, int TS>
-__device__ __forceinline__ void p1_sub_closure(T* tU, T* tL, T* dU, T* dL, int sb) {
-    using E = El<T>;
-    constexpr unsigned FULL = 0xffffffffu;
-    const int lane = threadIdx.x & 31;
-    const int i = lane / LPR, h = lane % LPR;
-    T* pu = tU + (sb + i) * TS + sb + CPL * h;
-    T* pl = HAS_L ? tL + (sb + i) * TS + sb + CPL * h : nullptr;
-    T u[CPL], l[CPL];
+// (a): closure of the SB x SB sub-block at (sb, sb) by two warps (AT
+// threads), in registers: thread t holds row t/4, columns 4(t%4) .. +3 of the
+// block.  Step k reads row k and column k from a double-buffered exchange in
+// shared memory that the holders of row and column k filled after step k-1,
+// so each step uses the values from before it (round-synchronous); one
+// two-warp barrier per step.  The lower-bound column is raised by the closure
+// rule, Lc = max(L[i,k], L[k,k] - U[i,k]).  xr, xc: [2 buffers][U, L][SB].
+constexpr int AT = 64;
+static_assert(SB * SB == AT * 4, "(a): four cells per thread");
+
+__device__ __forceinline__ void p1_pair_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+
+template <class T, bool HAS_L>
+__device__ __forceinline__ void p1_publish(const T (&u)[4], const T (&l)[4], int t, int k, T* xr,
+                                           T* xc) {
+    const int i = t >> 2, c0 = (t & 3) * 4;
+    T* r = xr + (k & 1) * 2 * SB;
+    T* c = xc + (k & 1) * 2 * SB;
+    if (i == k) {
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-        u[c] = pu[c];
-        l[c] = HAS_L ? pl[c] : T(0);
+        for (int q = 0; q < 4; ++q) {
+            r[c0 + q] = u[q];
+            if (HAS_L) r[SB + c0 + q] = l[q];
+        }
     }
+    if (c0 == (k & ~3)) {
+        const int q = k & 3;
+        c[i] = q == 0 ? u[0] : q == 1 ? u[1] : q == 2 ? u[2] : u[3];
+        if (HAS_L) c[SB + i] = q == 0 ? l[0] : q == 1 ? l[1] : q == 2 ? l[2] : l[3];
+    }
+}
+
+template <class T, bool HAS_L>
+__device__ __forceinline__ void p1_block_close(T (&u)[4], T (&l)[4], int t, T* xr, T* xc) {
+    using E = El<T>;
+    const int i = t >> 2, c0 = (t & 3) * 4;
+    p1_publish<T, HAS_L>(u, l, t, 0, xr, xc);
+    p1_pair_sync();
 #pragma unroll
     for (int k = 0; k < SB; ++k) {
-        const int own = LPR * i + k / CPL;   // holder of (i, k)
-        const int row = LPR * k + h;         // holder of (k, my columns)
-        const T uik = __shfl_sync(FULL, u[k % CPL], own);
-        T ukj[CPL], lkj[CPL];
+        const T* r = xr + (k & 1) * 2 * SB;
+        const T* c = xc + (k & 1) * 2 * SB;
+        const T uik = c[i];
+        T ukj[4], lkj[4];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) ukj[c] = __shfl_sync(FULL, u[c], row);
-        T lc = T(0);
-        if (HAS_L) {
-            const T lik = __shfl_sync(FULL, l[k % CPL], own);
-            const T lkk = __shfl_sync(FULL, l[k % CPL], LPR * k + k / CPL);
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) lkj[c] = __shfl_sync(FULL, l[c], row);
-            lc = E::mx(lik, E::sub(lkk, uik));
+        for (int q = 0; q < 4; ++q) {
+            ukj[q] = r[c0 + q];
+            lkj[q] = HAS_L ? r[SB + c0 + q] : T(0);
         }
+        T lc = T(0);
+        if (HAS_L) lc = E::mx(c[SB + i], E::sub(r[SB + k], uik));
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) u[c] = E::mn(u[c], E::add(uik, ukj[c]));
+        for (int q = 0; q < 4; ++q) u[q] = E::mn(u[q], E::add(uik, ukj[q]));
         if (HAS_L) {
 #pragma unroll
-            for (int c = 0; c < CPL; ++c)
-                l[c] = E::mx(l[c], E::mx(E::sub(lkj[c], uik), E::sub(lc, ukj[c])));
+            for (int q = 0; q < 4; ++q)
+                l[q] = E::mx(l[q], E::mx(E::sub(lkj[q], uik), E::sub(lc, ukj[q])));
+        }
+        if (k + 1 < SB) {
+            p1_publish<T, HAS_L>(u, l, t, k + 1, xr, xc);
+            p1_pair_sync();
         }
     }
+}
+
+// The block (sb, sb) to or from the (a) threads' registers.  The store also
+// writes the closed block k-interleaved (dU, dL) for the column sub-panel.
+template <class T, bool HAS_L, int TS>
+__device__ __forceinline__ void p1_block_load(const T* tU, const T* tL, int sb, int t, T (&u)[4],
+                                              T (&l)[4]) {
+    const int o = (sb + (t >> 2)) * TS + sb + (t & 3) * 4;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-        pu[c] = u[c];
-        const int d = (i >> 1) * (2 * SB) + 2 * (CPL * h + c) + (i & 1);
-        dU[d] = u[c];
+    for (int q = 0; q < 4; ++q) {
+        u[q] = tU[o + q];
+        l[q] = HAS_L ? tL[o + q] : T(0);
+    }
+}
+
+template <class T, bool HAS_L, int TS>
+__device__ __forceinline__ void p1_block_store(T* tU, T* tL, T* dU, T* dL, int sb, int t,
+                                               const T (&u)[4], const T (&l)[4]) {
+    const int i = t >> 2, c0 = (t & 3) * 4;
+    const int o = (sb + i) * TS + sb + c0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        tU[o + q] = u[q];
+        const int d = (i >> 1) * (2 * SB) + 2 * (c0 + q) + (i & 1);
+        dU[d] = u[q];
         if (HAS_L) {
-            pl[c] = l[c];
-            dL[d] = l[c];
+            tL[o + q] = l[q];
+            dL[d] = l[q];
+        }
+    }
+}
+
+// Step (c) of sub-block sp for the cells of block (sb, sb), in the (a)
+// layout: the product of the column sub-panel T[i][sp + k] (row-major tile)
+// with the row sub-panel T[sp + k][j] (its k-interleaved copy rU, rL), middle
+// atoms in pairs as in phase 3.
+template <class T, bool HAS_L, int FB, int TS>
+__device__ __forceinline__ void p1_block_product(T (&u)[4], T (&l)[4], const T* tU, const T* tL,
+                                                 const T* rU, const T* rL, int sb, int sp,
+                                                 int t) {
+    using LD = PairLoad<T>;
+    using P = typename LD::P;
+    constexpr bool NEG = std::is_same<T, int>::value;
+    const int row = (sb + (t >> 2)) * TS + sp;
+    const int j0 = sb + (t & 3) * 4;
+#pragma unroll 2
+    for (int kk = 0; kk < SB; kk += 2) {
+        P a = LD::ld2(tU + row + kk);
+        P al = a;
+        if (HAS_L) al = LD::ld2(tL + row + kk);
+        P b[4], bl[4];
+        const int jb = (kk >> 1) * (2 * FB) + 2 * j0;
+        LD::ld4(rU + jb, b[0], b[1]);
+        LD::ld4(rU + jb + 4, b[2], b[3]);
+        if (HAS_L) {
+            LD::ld4(rL + jb, bl[0], bl[1]);
+            LD::ld4(rL + jb + 4, bl[2], bl[3]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) PairOps<T>::upper(u[q], a, b[q]);
+        if (HAS_L) {
+            if (NEG) {
+                a = LD::neg(a);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) b[q] = LD::neg(b[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) PairOps<T>::lower(l[q], a, al, b[q], bl[q]);
         }
     }
 }
@@ -188,10 +266,17 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
 
     const int r0 = S::row0(), cq = S::cq();
     const int warp = threadIdx.x >> 5;
+    // (a) of the first sub-block; each later one runs inside (c) of the
+    // previous sub-block, on a warp that (c) leaves idle
+    __shared__ __align__(16) T xr[2 * 2 * SB], xc[2 * 2 * SB];   // (a) exchange
+    if (threadIdx.x < AT) {
+        T u[4], l[4];
+        p1_block_load<T, HAS_L, TS>(tU, tL, 0, threadIdx.x, u, l);
+        p1_block_close<T, HAS_L>(u, l, threadIdx.x, xr, xc);
+        p1_block_store<T, HAS_L, TS>(tU, tL, dU, dL, 0, threadIdx.x, u, l);
+    }
+    __syncthreads();
     for (int sb = 0; sb < m; sb += SB) {
-        // (a)
-        if (warp == 0) p1_sub_closure<T, HAS_L, TS>(tU, tL, dU, dL, sb);
-        __syncthreads();
 
         // (b): thread t < HALVES*W: row-panel cells (sb + 8hh + q, p), q < 8;
         //      t < 2*HALVES*W: column-panel cells (p, sb + 8hh + q), q < 8.
@@ -285,9 +370,23 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
         __syncthreads();
 
         // (c): threads whose rows lie in sub-block row s skip (whole warps);
-        // those whose columns lie in sub-block column s compute but do not store.
-        if ((r0 / SB) != (sb / SB)) {
-            const bool keep = (cq / SB) != (sb / SB);
+        // those whose columns lie in sub-block column s compute but do not
+        // store.  The skipping warps take block (s+1, s+1) instead: its (c)
+        // step, then its closure (a), so that the next sub-block's (a)
+        // overlaps this (c); the others leave that block alone.
+        const int nsb = sb + SB;
+        if (warp >> 1 == sb / SB) {
+            if (nsb < m) {
+                const int t = threadIdx.x - AT * (sb / SB);
+                T u[4], l[4];
+                p1_block_load<T, HAS_L, TS>(tU, tL, nsb, t, u, l);
+                p1_block_product<T, HAS_L, FB, TS>(u, l, tU, tL, rU, rL, nsb, sb, t);
+                p1_block_close<T, HAS_L>(u, l, t, xr, xc);
+                p1_block_store<T, HAS_L, TS>(tU, tL, dU, dL, nsb, t, u, l);
+            }
+        } else if ((r0 / SB) != (sb / SB)) {
+            const bool keep = (cq / SB) != (sb / SB) &&
+                              !(nsb < m && r0 / SB == nsb / SB && cq / SB == nsb / SB);
             T u[S::TM][S::TN], l[S::TM][S::TN];
 #pragma unroll
             for (int r = 0; r < S::TM; ++r)

@@ -278,6 +278,196 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     }
 }
 
+// ---------------------------------------------------------------- strips
+//
+// When a launch has fewer 64-wide tiles than a fraction of the SMs (small n:
+// a block round of n = 256 has 9 bulk tiles and 6 panel tiles), each tile is
+// split among SPLIT CTAs, each computing one strip of it, so that more SMs
+// share the round's critical path.  A strip is the 64 rows x 64/SPLIT columns
+// of the tile, or for a column panel 64/SPLIT rows x 64 columns: a CTA then
+// reads of its own tile (the panel operand of phase 2) only the lines it
+// writes itself, and no two CTAs touch the same cell.  Same update as
+// k_phase3: middle atoms in pairs, operands staged per 16 middle atoms with
+// cp.async.  256 threads, each 64/(16 SPLIT) rows x 4 columns.
+
+constexpr int SFB = FB_SMALL;      // strips only split 64-wide tiles
+constexpr int SBK = P3K<SFB>::BK;  // 16
+constexpr int SAST = SBK + 4;
+constexpr int SNT = 256;
+
+// One buffer per 16-middle-atom chunk (four): a strip's CTA is latency-bound,
+// so every chunk is put in flight at once instead of two at a time.
+template <class T, bool HAS_L>
+struct StripSmem {
+    static constexpr int A_ELEMS = SFB * SAST;   // A[i][k], up to 64 rows
+    static constexpr int B_ELEMS = SBK * SFB;    // B[k/2][j][k%2], up to 64 columns
+    static constexpr int STAGE = (HAS_L ? 2 : 1) * (A_ELEMS + B_ELEMS);
+    static constexpr int STAGES = SFB / SBK;
+    static constexpr size_t BYTES = STAGES * STAGE * sizeof(T);
+};
+
+// Stage chunk c of the column operand (rows gi .. gi+ri-1 of the global
+// matrix, middle atoms ok + c*SBK ..) and of the row operand (columns
+// gj .. gj+cj-1); rs x cs is the strip's full extent, cells beyond the valid
+// ri x cj (and middle atoms beyond mk) get pads.
+template <class T, bool HAS_L>
+__device__ __forceinline__ void strip_stage(T* stage, const T* U, const T* L, size_t ld, int gi,
+                                            int gj, int ok, int rs, int cs, int ri, int cj,
+                                            int mk, int c, bool vec) {
+    using E = El<T>;
+    using SM = StripSmem<T, HAS_L>;
+    T* AU = stage;
+    T* BU = stage + SM::A_ELEMS;
+    T* AL = HAS_L ? BU + SM::B_ELEMS : nullptr;
+    T* BL = HAS_L ? AL + SM::A_ELEMS : nullptr;
+    const int kc = c * SBK;
+    for (int p = threadIdx.x; p < rs * (SBK / 4); p += SNT) {
+        const int i = p / (SBK / 4), kq = (p % (SBK / 4)) * 4;
+        const size_t g = (size_t)(gi + i) * ld + ok + kc + kq;
+        if (vec && i < ri && kc + kq + 4 <= mk) {
+            cp_async16(AU + i * SAST + kq, U + g);
+            if (HAS_L) cp_async16(AL + i * SAST + kq, L + g);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool in = i < ri && kc + kq + q < mk;
+                AU[i * SAST + kq + q] = in ? U[g + q] : E::upad();
+                if (HAS_L) AL[i * SAST + kq + q] = in ? L[g + q] : E::lpad();
+            }
+        }
+    }
+    for (int p = threadIdx.x; p < SBK * cs; p += SNT) {
+        const int k = p / cs, j = p % cs;
+        const int d = (k >> 1) * (2 * SFB) + j * 2 + (k & 1);
+        const size_t g = (size_t)(ok + kc + k) * ld + gj + j;
+        if (kc + k < mk && j < cj) {
+            cp_async4(BU + d, U + g);
+            if (HAS_L) cp_async4(BL + d, L + g);
+        } else {
+            BU[d] = E::upad();
+            if (HAS_L) BL[d] = E::lpad();
+        }
+    }
+}
+
+template <class T, bool HAS_L, int SPLIT>
+__global__ void __launch_bounds__(SNT)
+k_strip(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, int part,
+        bool vec, bool sym) {
+    using E = El<T>;
+    using SM = StripSmem<T, HAS_L>;
+    using LD = PairLoad<T>;
+    using P = typename LD::P;
+    constexpr int W = SFB / SPLIT;    // strip width
+    constexpr int TMS = W / 16;       // rows per thread: 64 * W cells over 256 threads, 4 columns each
+    constexpr bool NEG = std::is_same<T, int>::value;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* sm = reinterpret_cast<T*>(smem_raw);
+
+    const size_t off = (size_t)blockIdx.z * (size_t)bstride;
+    U += off;
+    if (HAS_L) L += off;
+    const int nb = (n + SFB - 1) / SFB;
+    int I, J;
+    p3_tile(part, sym, blockIdx.x, nb, K, I, J);
+    const int oi = I * SFB, oj = J * SFB, ok = K * SFB;
+    const int mi = min(SFB, n - oi), mj = min(SFB, n - oj), mk = min(SFB, n - ok);
+    // the strip: rows r0 .. r0+rs-1, columns c0 .. c0+cs-1 of the tile
+    const bool rows_split = part == P3_PANELS && J == K && I != K;   // column panel
+    const int s = blockIdx.y;
+    const int r0 = rows_split ? s * W : 0, c0 = rows_split ? 0 : s * W;
+    const int rs = rows_split ? W : SFB, cs = rows_split ? SFB : W;
+    const int ri = max(0, min(rs, mi - r0)), cj = max(0, min(cs, mj - c0));
+    const int qx = cs / 4;                       // column quads
+    const int tx = threadIdx.x % qx, ty = threadIdx.x / qx;
+    const int lr = ty * TMS, lc = tx * 4;        // the thread's cells, strip-relative
+    T* Us = U + (size_t)(oi + r0) * ld + oj + c0;
+    T* Ls = HAS_L ? L + (size_t)(oi + r0) * ld + oj + c0 : nullptr;
+
+    T u[TMS][4], l[TMS][4];
+#pragma unroll
+    for (int r = 0; r < TMS; ++r) {
+        const int i = lr + r;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const bool in = i < ri && lc + q < cj;
+            u[r][q] = in ? Us[(size_t)i * ld + lc + q] : E::upad();
+            l[r][q] = HAS_L && in ? Ls[(size_t)i * ld + lc + q] : E::lpad();
+        }
+    }
+
+    const int nchunks = (mk + SBK - 1) / SBK;   // 1 .. SM::STAGES
+    for (int c = 0; c < SM::STAGES; ++c) {
+        if (c < nchunks)
+            strip_stage<T, HAS_L>(sm + c * SM::STAGE, U, L, ld, oi + r0, oj + c0, ok, rs, cs, ri,
+                                  cj, mk, c, vec);
+        cp_async_commit();   // one group per buffer, empty past the last chunk
+    }
+    static_assert(SM::STAGES == 4, "the waits below count four groups");
+    for (int c = 0; c < nchunks; ++c) {
+        // chunk c landed once at most 3 - c younger groups are still pending
+        if (c == 0) cp_async_wait<3>();
+        else if (c == 1) cp_async_wait<2>();
+        else if (c == 2) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncthreads();
+        const T* AU = sm + c * SM::STAGE;
+        const T* BU = AU + SM::A_ELEMS;
+        const T* AL = BU + SM::B_ELEMS;
+        const T* BL = AL + SM::A_ELEMS;
+#pragma unroll 2
+        for (int kk = 0; kk < SBK; kk += 2) {
+            P a[TMS], al[TMS], b[4], bl[4];
+#pragma unroll
+            for (int r = 0; r < TMS; ++r) {
+                a[r] = LD::ld2(AU + (lr + r) * SAST + kk);
+                if (HAS_L) al[r] = LD::ld2(AL + (lr + r) * SAST + kk);
+            }
+            const int jb = (kk >> 1) * (2 * SFB) + lc * 2;
+            LD::ld4(BU + jb, b[0], b[1]);
+            LD::ld4(BU + jb + 4, b[2], b[3]);
+            if (HAS_L) {
+                LD::ld4(BL + jb, bl[0], bl[1]);
+                LD::ld4(BL + jb + 4, bl[2], bl[3]);
+            }
+#pragma unroll
+            for (int r = 0; r < TMS; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) PairOps<T>::upper(u[r][q], a[r], b[q]);
+            if (HAS_L) {
+                if (NEG) {
+#pragma unroll
+                    for (int r = 0; r < TMS; ++r) a[r] = LD::neg(a[r]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) b[q] = LD::neg(b[q]);
+                }
+#pragma unroll
+                for (int r = 0; r < TMS; ++r)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) PairOps<T>::lower(l[r][q], a[r], al[r], b[q], bl[q]);
+            }
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < TMS; ++r) {
+        const int i = lr + r;
+        if (i >= ri) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (lc + q >= cj) continue;
+            Us[(size_t)i * ld + lc + q] = u[r][q];
+            if (HAS_L) Ls[(size_t)i * ld + lc + q] = l[r][q];
+            if (sym && I != J) {
+                // the mirrored cell of tile (J, I)
+                const size_t t = (size_t)(oj + c0 + lc + q) * ld + oi + r0 + i;
+                U[t] = u[r][q];
+                if (HAS_L) L[t] = l[r][q];
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- launchers
 
 template <class T>
@@ -293,6 +483,10 @@ static cudaError_t setup3() {
     set(k_phase3<T, false, FB_SMALL, false>, P3Smem<T, false, FB_SMALL>::BYTES);
     set(k_phase3<T, true, FB_SMALL, true>, P3Smem<T, true, FB_SMALL>::BYTES);
     set(k_phase3<T, false, FB_SMALL, true>, P3Smem<T, false, FB_SMALL>::BYTES);
+    set(k_strip<T, true, 2>, StripSmem<T, true>::BYTES);
+    set(k_strip<T, true, 4>, StripSmem<T, true>::BYTES);
+    set(k_strip<T, false, 2>, StripSmem<T, false>::BYTES);
+    set(k_strip<T, false, 4>, StripSmem<T, false>::BYTES);
     return e;
 }
 
@@ -328,12 +522,32 @@ static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {
     });
 }
 
-// The wide form for 64-wide tiles when the launch has at most two CTAs per SM.
+template <class T, bool HAS_L, int SPLIT>
+static cudaError_t strip_t(const Mats& m, int K, int part, cudaStream_t s) {
+    const int nb = (m.n + SFB - 1) / SFB;
+    const int tiles = p3_tiles(m.sym, part, nb, K);
+    if (tiles <= 0) return cudaSuccess;
+    return for_batch_chunks(m, [&](int b0, int nbz) {
+        T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
+        T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
+        const Phase ph = part == P3_PANELS ? PH_TWO : part == P3_NEXT ? PH_NEXT : PH_THREE;
+        before_launch(s, ph);
+        k_strip<T, HAS_L, SPLIT><<<dim3(tiles, SPLIT, nbz), SNT, StripSmem<T, HAS_L>::BYTES, s>>>(
+            U, L, m.n, m.ld, m.bstride, K, part, m.vec, m.sym);
+        after_launch(s, ph);
+    });
+}
+
+// 64-wide tiles: with at most a quarter (half) of an SM's worth of tiles per
+// SM, four (two) strips per tile; with at most two tiles per SM the wide form;
+// else the 8 x 8 form.
 template <class T, bool HAS_L>
 static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
     if (m.fb == FB_LARGE) return phase3_t<T, HAS_L, FB_LARGE, false>(m, K, part, s);
     const int nb = (m.n + FB_SMALL - 1) / FB_SMALL;
     const double ctas = (double)p3_tiles(m.sym, part, nb, K) * m.batch;
+    if (4.0 * ctas <= m.sms) return strip_t<T, HAS_L, 4>(m, K, part, s);
+    if (2.0 * ctas <= m.sms) return strip_t<T, HAS_L, 2>(m, K, part, s);
     return ctas <= 2.0 * m.sms ? phase3_t<T, HAS_L, FB_SMALL, true>(m, K, part, s)
                                : phase3_t<T, HAS_L, FB_SMALL, false>(m, K, part, s);
 }
