@@ -454,13 +454,14 @@ def main():
 
 SCHEDULE_FLAGS = {"auto": 0, "t64": (1 << 5) | (1 << 9), "t128": (1 << 6) | (1 << 9),
                   "t64_serial": (1 << 5) | (1 << 7), "t128_serial": (1 << 6) | (1 << 7),
-                  "perk": 1 << 2, "sym": 1 << 8}
+                  "perk": 1 << 2, "sym": 1 << 8,
+                  "graph": 0}   # "graph": the auto schedule captured once, replayed
 ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial", "sym")
 SWEEP = (
     # (config, dtype, schedules, description); config None: random bounds of size n
-    (0, "f32", ALL_SCHEDULES, "chain n=256"),
-    (1, "f32", ALL_SCHEDULES, "chain n=1000"),
-    (("random", 2048), "f32", ALL_SCHEDULES, "random bounds n=2048"),
+    (0, "f32", ALL_SCHEDULES + ("graph",), "chain n=256"),
+    (1, "f32", ALL_SCHEDULES + ("graph",), "chain n=1000"),
+    (("random", 2048), "f32", ALL_SCHEDULES + ("graph",), "random bounds n=2048"),
     (("random", 3000), "f32", ("auto", "t64", "t128", "t128_serial"), "random bounds n=3000"),
     (2, "f32", ALL_SCHEDULES + ("perk",), "globule n=4096"),
     (2, "i32", ("auto",), "globule n=4096"),
@@ -497,15 +498,42 @@ def sweep(args):
             flags = SCHEDULE_FLAGS[algo]
             reps = max(3, min(args.steps, 20)) if n < 16384 else max(3, min(args.steps, 5))
             times = []
-            for r in range(args.warmup + reps):
-                U, L = dU0.clone(), dL0.clone()
-                torch.cuda.synchronize()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
+
+            def call(U, L):
                 if batch > 1:
                     bsm.bs_smooth_bounds_batched(U, L, flags=flags)
                 else:
                     bsm.bs_smooth_bounds(U, L, flags=flags)
+            if algo == "graph":
+                # one call captured in a CUDA graph, replayed: the launch
+                # sequence is submitted at once.  Each replay redoes the full
+                # smoothing of the same matrices (the work does not depend
+                # on the values).
+                U, L = dU0.clone(), dL0.clone()
+                call(U, L)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    call(U, L)
+                for r in range(args.warmup + reps):
+                    torch.cuda.synchronize()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    g.replay()
+                    b.record()
+                    torch.cuda.synchronize()
+                    if r >= args.warmup:
+                        times.append(a.elapsed_time(b))
+                Uo, Lo = dU0.clone(), dL0.clone()
+                call(Uo, Lo)
+                assert torch.equal(U, Uo) and torch.equal(L, Lo)
+                del g
+            for r in range(0 if algo == "graph" else args.warmup + reps):
+                U, L = dU0.clone(), dL0.clone()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                call(U, L)
                 b.record()
                 torch.cuda.synchronize()
                 if r >= args.warmup:

@@ -137,16 +137,11 @@ int choose_tile(int n, int batch, int mode) {
 // block-rows and -columns K and K+1.  NEXT(K)'s short wave thus overlaps
 // REST(K) instead of running alone.
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
-                        bool force, DeviceState* d) {
+                        DeviceState* d) {
     const int nb = (m.n + m.fb - 1) / m.fb;
     cudaError_t e = bs::launch_phase1(is_int, m, 0, s);
     if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, 0, s);
     if (e != cudaSuccess) return e;
-    // Look-ahead pays only when the rest of a round's phase 3 is large enough to
-    // hide phases 1 and 2 of the next round; with a wave or two of tiles, the
-    // serial phase 1 running beside them only gets slower.
-    const double rest_cells = (double)(nb - 2) * (nb - 2) * m.fb * m.fb * m.batch;
-    if (rest_cells < 2097152.0 && !force) lookahead = false;
     if (!lookahead || nb < 3) {
         for (int K = 0; K < nb && e == cudaSuccess; ++K) {
             e = bs::launch_phase3(is_int, m, K, bs::P3_ALL, s);
@@ -266,8 +261,7 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
             if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
         }
     } else {
-        e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0,
-                        (mode & BS_FORCE_LOOKAHEAD) != 0, d);
+        e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0, d);
     }
     return cuda_status(e);
 }

@@ -99,11 +99,34 @@ template <class F>
 cudaError_t for_batch_chunks(const Mats& m, F launch) {
     for (int b0 = 0; b0 < m.batch; b0 += 65535) {
         const int nbz = m.batch - b0 < 65535 ? m.batch - b0 : 65535;
-        launch(b0, nbz);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch(b0, nbz);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// Launch on `s` carrying the stream's priority as a launch attribute, so that
+// a launch captured into a CUDA graph keeps it (a graph's kernel nodes do not
+// inherit the priority of the stream they were captured from).  The
+// look-ahead stream's kernels depend on it.
+template <class... KArgs, class... Args>
+cudaError_t launch_prio(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t s, Args... args) {
+    int prio = 0;
+    cudaError_t e = cudaStreamGetPriority(s, &prio);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributePriority;
+    attr[0].val.priority = prio;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = prio != 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 }  // namespace bs

@@ -490,9 +490,11 @@ static cudaError_t phase1_t(const Mats& m, int K, cudaStream_t s) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
         before_launch(s, PH_ONE);
-        k_phase1<T, HAS_L, FB><<<dim3(1, 1, nbz), P1S<FB>::NT, P1Smem<T, HAS_L, FB>::BYTES, s>>>(
-            U, L, m.n, m.ld, m.bstride, K, m.vec);
+        const cudaError_t e = launch_prio(k_phase1<T, HAS_L, FB>, dim3(1, 1, nbz), dim3(P1S<FB>::NT),
+                                          P1Smem<T, HAS_L, FB>::BYTES, s, U, L, m.n, m.ld,
+                                          m.bstride, K, m.vec);
         after_launch(s, PH_ONE);
+        return e;
     });
 }
 

@@ -515,10 +515,11 @@ static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
         const Phase ph = part == P3_PANELS ? PH_TWO : part == P3_NEXT ? PH_NEXT : PH_THREE;
         before_launch(s, ph);
-        k_phase3<T, HAS_L, FB, WIDE><<<dim3(tiles, 1, nbz), P3S<FB, WIDE>::NT,
-                                       P3Smem<T, HAS_L, FB>::BYTES, s>>>(
-            U, L, m.n, m.ld, m.bstride, K, part, m.vec, m.sym);
+        const cudaError_t e = launch_prio(k_phase3<T, HAS_L, FB, WIDE>, dim3(tiles, 1, nbz),
+                                          dim3(P3S<FB, WIDE>::NT), P3Smem<T, HAS_L, FB>::BYTES, s,
+                                          U, L, m.n, m.ld, m.bstride, K, part, m.vec, m.sym);
         after_launch(s, ph);
+        return e;
     });
 }
 
@@ -532,21 +533,26 @@ static cudaError_t strip_t(const Mats& m, int K, int part, cudaStream_t s) {
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
         const Phase ph = part == P3_PANELS ? PH_TWO : part == P3_NEXT ? PH_NEXT : PH_THREE;
         before_launch(s, ph);
-        k_strip<T, HAS_L, SPLIT><<<dim3(tiles, SPLIT, nbz), SNT, StripSmem<T, HAS_L>::BYTES, s>>>(
-            U, L, m.n, m.ld, m.bstride, K, part, m.vec, m.sym);
+        const cudaError_t e = launch_prio(k_strip<T, HAS_L, SPLIT>, dim3(tiles, SPLIT, nbz),
+                                          dim3(SNT), StripSmem<T, HAS_L>::BYTES, s, U, L, m.n,
+                                          m.ld, m.bstride, K, part, m.vec, m.sym);
         after_launch(s, ph);
+        return e;
     });
 }
 
-// 64-wide tiles: with at most a quarter (half) of an SM's worth of tiles per
-// SM, four (two) strips per tile; with at most two tiles per SM the wide form;
-// else the 8 x 8 form.
+// 64-wide tiles: with at most half a tile per SM, four strips per tile; with
+// at most one, two strips; with at most two tiles per SM the wide form; else
+// the 8 x 8 form.  (Measured on the GB300: n = 2048, where the next block row
+// and column and the panels, 61 and 62 tiles, run on the look-ahead critical
+// path, is 12 % faster with four strips than with two; n = 1000's 225 bulk
+// tiles are 8 % slower as strips than in the wide form.)
 template <class T, bool HAS_L>
 static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
     if (m.fb == FB_LARGE) return phase3_t<T, HAS_L, FB_LARGE, false>(m, K, part, s);
     const int nb = (m.n + FB_SMALL - 1) / FB_SMALL;
     const double ctas = (double)p3_tiles(m.sym, part, nb, K) * m.batch;
-    if (4.0 * ctas <= m.sms) return strip_t<T, HAS_L, 4>(m, K, part, s);
+    if (4.0 * ctas <= 2.0 * m.sms) return strip_t<T, HAS_L, 4>(m, K, part, s);
     if (2.0 * ctas <= m.sms) return strip_t<T, HAS_L, 2>(m, K, part, s);
     return ctas <= 2.0 * m.sms ? phase3_t<T, HAS_L, FB_SMALL, true>(m, K, part, s)
                                : phase3_t<T, HAS_L, FB_SMALL, false>(m, K, part, s);

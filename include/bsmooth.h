@@ -37,13 +37,18 @@
  * default stream) of the calling thread's current device, which must hold
  * the matrices.  Smoothing calls return before the GPU finishes.
  * bs_check_feasible synchronises `stream` before it returns.  In blocked mode
- * (unless BS_NO_LOOKAHEAD) phases 1 and 2 of block round K+1 run on an
- * internal stream of the library, forked from and joined back into `stream`
- * with events inside the call, while the rest of round K's phase 3 runs on
- * `stream`; all work still completes in `stream` order.  The smoothing calls
- * can be captured into a CUDA graph (stream capture on `stream`) once the
- * library has run one smoothing of the same kind on the device, which sets up
- * its per-device state; the look-ahead fork and join are captured with it.
+ * with three or more block rows (unless BS_NO_LOOKAHEAD) the tiles of block
+ * row and column K+1 and phases 1 and 2 of block round K+1 run on an internal
+ * high-priority stream of the library, forked from and joined back into
+ * `stream` with events inside the call, while the rest of round K's phase 3
+ * runs on `stream`; all work still completes in `stream` order.  The
+ * smoothing calls can be captured into a CUDA graph (stream capture on
+ * `stream`) once the library has run one smoothing of the same kind on the
+ * device, which sets up its per-device state; the look-ahead fork and join
+ * are captured with it, and the internal stream's priority is kept on its
+ * kernels as a launch attribute.  Replaying a captured call saves the
+ * per-launch host overhead, which matters for small n (n = 256: about a
+ * quarter of the call).
  *
  * Memory.  The caller owns U, L and the mask.  Smoothing allocates nothing.
  * bs_check_feasible and BS_VALIDATE use one small internal device buffer per
@@ -90,11 +95,11 @@ enum {
     BS_TILE_128 = 1 << 6,     /* force 128 x 128 tiles; both tile bits: BS_ERR_ARG */
     BS_NO_LOOKAHEAD = 1 << 7, /* run the three phases of each block round in
                                  sequence on `stream` only (see below) */
-    BS_FORCE_LOOKAHEAD = 1 << 9, /* use the look-ahead schedule even where the
-                                    size rule would not (it is on by default only
-                                    when a round's remaining phase-3 work is at
-                                    least 2^21 cells); with BS_NO_LOOKAHEAD:
-                                    BS_ERR_ARG */
+    BS_FORCE_LOOKAHEAD = 1 << 9, /* use the look-ahead schedule; it is the
+                                    default whenever the matrix has three or more
+                                    block rows, so this bit changes nothing and is
+                                    kept for callers that set it; with
+                                    BS_NO_LOOKAHEAD: BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the
                                  diagonal are computed, each mirrored into its

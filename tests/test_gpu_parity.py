@@ -403,6 +403,25 @@ def test_batched_chains(sched):
     del n
 
 
+@pytest.mark.parametrize("n,B", [(200, 3), (300, 4), (257, 12), (130, 40)])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+@pytest.mark.parametrize("sched", ["auto", "sym"])
+def test_batched_small_molecules(n, B, dtype, sched):
+    """Small batches of small molecules: the launches take the strip forms
+    (four or two CTAs per tile) or the 256-thread form depending on the
+    tiles per SM; every molecule against the oracle."""
+    mols = [W.random_bounds(n, 8100 + 7 * B + b, p_bad=0.01) for b in range(B)]
+    Uq = np.stack([m[0] for m in mols])
+    Lq = np.stack([m[1] for m in mols])
+    U0, L0 = (W.to_f32(Uq), W.to_f32(Lq)) if dtype == "f32" else (Uq, Lq)
+    U, L = dev(U0), dev(L0)
+    bsm.bs_smooth_bounds_batched(U, L, flags=SCHEDULES[sched])
+    Ug, Lg = host(U), host(L)
+    for b in range(B):
+        Uo, Lo = oracle.smooth(U0[b], L0[b])
+        assert same_bits(Ug[b], Uo) and same_bits(Lg[b], Lo)
+
+
 def test_batched_per_round_and_strided():
     """Per-round mode and a batch stride larger than one molecule."""
     B, n, ld = 5, 70, 72
@@ -552,7 +571,11 @@ def test_empty_and_launch_counting():
     assert bsm.bs_launch_count() - before == 5 + 5 + 4 * 2 + 1
     before = bsm.bs_launch_count()
     bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_TILE_64)
-    # this size is below the look-ahead rule: three launches per round
+    # look-ahead is the default from three block rounds on: the same launches
+    assert bsm.bs_launch_count() - before == 5 + 5 + 4 * 2 + 1
+    before = bsm.bs_launch_count()
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)),
+                         flags=bsm.BS_TILE_64 | bsm.BS_NO_LOOKAHEAD)
     assert bsm.bs_launch_count() - before == 5 * 3
 
 
