@@ -37,6 +37,9 @@ WORKLOADS = {
     # profiling size: inputs 4x larger than L2, a few GB on the device
     "globule8192": dict(box=(32, 16, 16), seed=1005, p_long=0.005,
                         desc="lattice globule n=8192 (profiling size), fp32 U+L, blocked"),
+    # the small molecules of the benchmark set, for launch lists
+    "chain256": dict(config=0, desc="random-walk chain n=256, fp32 U+L, blocked"),
+    "chain1000": dict(config=1, desc="random-walk chain n=1000, fp32 U+L, blocked"),
 }
 
 
