@@ -18,6 +18,7 @@ struct SideCtx {
     cudaStream_t side = nullptr;
     cudaEvent_t main_done[2] = {nullptr, nullptr};   // on the caller's stream, by round parity
     cudaEvent_t side_done = nullptr;                 // on the side stream
+    cudaEvent_t next_done = nullptr;                 // on the side stream, after NEXT(K)
 };
 
 struct DeviceState {
@@ -93,10 +94,10 @@ cudaError_t acquire_side(DeviceState* d, SideCtx* out) {
     int lo = 0, hi = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, hi);
-    for (cudaEvent_t* ev : {&c.main_done[0], &c.main_done[1], &c.side_done})
+    for (cudaEvent_t* ev : {&c.main_done[0], &c.main_done[1], &c.side_done, &c.next_done})
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {
-        for (cudaEvent_t ev : {c.main_done[0], c.main_done[1], c.side_done})
+        for (cudaEvent_t ev : {c.main_done[0], c.main_done[1], c.side_done, c.next_done})
             if (ev) cudaEventDestroy(ev);
         if (c.side) cudaStreamDestroy(c.side);
         return e;
@@ -135,7 +136,7 @@ int choose_tile(int n, int batch, int mode) {
 // -column K, which phase 2 of round K+1 does not write except tiles (K,K+1)
 // and (K+1,K), which REST(K) does not read; it writes tiles outside
 // block-rows and -columns K and K+1.  NEXT(K)'s short wave thus overlaps
-// REST(K) instead of running alone.
+// REST(K) instead of running alone (except with few rest tiles, see below).
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
                         DeviceState* d) {
     const int nb = (m.n + m.fb - 1) / m.fb;
@@ -153,26 +154,40 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
     SideCtx c;
     e = acquire_side(d, &c);
     if (e != cudaSuccess) return e;
+    // With fewer rest-of-round tiles than two per SM, REST(K) would fill the
+    // SMs the moment it is ready and phase 1 of round K+1, on the critical
+    // path, would wait for one of its CTAs to finish; REST(K) then waits for
+    // NEXT(K) instead (which follows phase 2 of round K on the side stream),
+    // so phase 1 is dispatched first.
+    const bool tight = (double)(nb - 2) * (nb - 2) * m.batch < 2.0 * m.sms;
     // main_done[1] stands for "REST(-1)": everything enqueued on s so far.
     e = cudaEventRecord(c.main_done[1], s);
     bool forked = false;   // side work enqueued that s has not yet waited for
+    auto rest = [&](int K, cudaEvent_t after) {
+        cudaError_t r = cudaSuccess;
+        if (after) r = cudaStreamWaitEvent(s, after, 0);
+        if (r == cudaSuccess) r = bs::launch_phase3(is_int, m, K, bs::P3_REST, s);
+        if (r == cudaSuccess) r = cudaEventRecord(c.main_done[K & 1], s);
+        return r;
+    };
     for (int K = 0; K + 1 < nb && e == cudaSuccess; ++K) {
-        if (forked) {
-            e = cudaStreamWaitEvent(s, c.side_done, 0);   // phase 2 of round K
+        if (!tight) {
+            // REST(K) after phase 2 of round K
+            e = rest(K, forked ? c.side_done : nullptr);
             forked = false;
+            if (e != cudaSuccess) break;
         }
-        if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, bs::P3_REST, s);
-        if (e == cudaSuccess) e = cudaEventRecord(c.main_done[K & 1], s);
-        if (e != cudaSuccess) break;
         // side: after REST(K-1), NEXT(K) then phases 1 and 2 of round K+1
         e = cudaStreamWaitEvent(c.side, c.main_done[(K + 1) & 1], 0);
         if (e != cudaSuccess) break;
         forked = true;
         e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT, c.side);
+        if (e == cudaSuccess && tight) e = cudaEventRecord(c.next_done, c.side);
         if (e == cudaSuccess) e = bs::launch_phase1(is_int, m, K + 1, c.side);
         if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K + 1, c.side);
         cudaError_t r = cudaEventRecord(c.side_done, c.side);
         if (e == cudaSuccess) e = r;
+        if (e == cudaSuccess && tight) e = rest(K, c.next_done);
     }
     // always join the side stream back, on success or failure
     if (forked) {
