@@ -492,11 +492,54 @@ def upper_bellman_holds(U0q, Ug, block=32):
     return True
 
 
+def lower_bellman_holds(U0q, L0q, Ug, Lg, block=32):
+    """Every cell of the smoothed lower bound against the shortest-path
+    equations of the doubled bound graph (-L[i,j] is the distance from i's
+    first copy to j's second), given the smoothed U:
+      L[i,j] = max(L0[i,j], max_k L[k,j] - U0[i,k], max_b L0[i,b] - U[b,j])
+    over the known neighbours k, b of i.  Pairs left out cannot win here:
+    an unknown pair's term L0[i,b] - U[b,j] <= 1 A <= L0[i,j] (every
+    off-diagonal L0 is at least the unknown value, asserted), and an unknown
+    u edge leaves L[k,j] - U0[i,k] < 0 since L <= U < U0 there.  For fixed U
+    the equations are a shortest-path problem with positive weights, so
+    their solution is unique.  Plain PyTorch float64 on Q10 values."""
+    t = torch()
+    n = U0q.shape[0]
+    sent = W.sentinel_q(n)
+    off = ~np.eye(n, dtype=bool)
+    unknown_l = int(L0q[off & (U0q >= sent)].max())
+    assert int(L0q[off].min()) >= unknown_l
+    known = (U0q < sent) & off
+    kmax = int(known.sum(1).max())
+    nbr = np.zeros((n, kmax), np.int64)
+    wu = np.full((n, kmax), np.inf)       # U0[i, k]
+    wl = np.full((n, kmax), -np.inf)      # L0[i, b]
+    for i in range(n):
+        ks = np.nonzero(known[i])[0]
+        nbr[i, :len(ks)] = ks
+        wu[i, :len(ks)] = U0q[i, ks]
+        wl[i, :len(ks)] = L0q[i, ks]
+    nbr_d = t.from_numpy(nbr).cuda()
+    wu_d, wl_d = t.from_numpy(wu).cuda(), t.from_numpy(wl).cuda()
+    Ud = Ug.to(t.float64) * 1024
+    Ld = Lg.to(t.float64) * 1024
+    L0d = t.from_numpy(L0q.astype(np.float64)).cuda()
+    for i0 in range(0, n, block):
+        i1 = min(n, i0 + block)
+        nb = nbr_d[i0:i1]
+        via_u = (Ld[nb] - wu_d[i0:i1, :, None]).max(dim=1).values
+        via_l = (wl_d[i0:i1, :, None] - Ud[nb]).max(dim=1).values
+        rhs = t.maximum(L0d[i0:i1], t.maximum(via_u, via_l))
+        if not bool((rhs == Ld[i0:i1]).all()):
+            return False
+    return True
+
+
 @pytest.mark.parametrize("sched", ["auto", "sym"])
 def test_globule_16384_sampled_rows(globule16384, sched):
     """n = 16384, fp32, blocked, as timed by the benchmark: 64 sampled rows
-    of U and L against the oracle's shortest-path rows, every cell of U
-    against the shortest-path equations, plus properties of every cell."""
+    of U and L against the oracle's shortest-path rows, every cell of U and
+    of L against the shortest-path equations, plus properties of every cell."""
     m, rows, Ur, Lr = globule16384
     t = torch()
     U, L = dev(W.to_f32(m["U"])), dev(W.to_f32(m["L"]))
@@ -505,8 +548,9 @@ def test_globule_16384_sampled_rows(globule16384, sched):
     Ug = U[t.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64) * 1024
     Lg = L[t.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64) * 1024
     assert np.array_equal(Ug, Ur) and np.array_equal(Lg, Lr)
-    # every cell of U: the shortest-path equations of the bound graph
+    # every cell of U and L: the shortest-path equations of the bound graph
     assert upper_bellman_holds(m["U"], U)
+    assert lower_bellman_holds(m["U"], m["L"], U, L)
     # every cell: symmetric, consistent (no flags), diagonal zero
     assert bool((U == U.T).all()) and bool((L == L.T).all())
     assert bsm.bs_check_feasible(U, L) == 0
