@@ -403,6 +403,17 @@ def main():
     U, L = copies[0]
     if wl.get("consistent", True):
         assert bsm.bs_check_feasible(U, L) == 0
+    # the feasibility pass (HBM-bound: reads 8 n^2 bytes), timed on its own
+    fz = []
+    for r in range(4):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bsm.bs_check_feasible(U, L)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if r:
+            fz.append(a.elapsed_time(b))
+    feas_ms = statistics.median(fz)
 
     peaks = load_peaks()
     fmax = peaks["sm_max_mhz"] * 1e6
@@ -456,6 +467,10 @@ def main():
         "phases_ms_per_step": {k: prof[k]["ms"] / args.steps for k in bsm.PHASES},
         "gpu_launches": launches,
         "clocks": clocks,
+        "feasible": {"ms": feas_ms, "gbs": 8.0 * n * n / (feas_ms * 1e-3) / 1e9,
+                     "frac_of_hbm": 8.0 * n * n / (feas_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "basis": "bs_check_feasible on the smoothed matrices: 8 n^2 bytes read / "
+                              "event time of the call (launch, counter reset, 8-byte readback)"},
     }
     if args.mode == "perk":
         # per-round mode: every round reads and writes all of U and L, 16 bytes

@@ -4,22 +4,48 @@
 
 namespace bs {
 
+// One pass over both matrices.  With 16-byte rows (vec) each thread compares
+// four cells per step through 16-byte loads (and writes the mask as 4 bytes);
+// otherwise one cell.  The count is reduced per warp, then per CTA, then one
+// atomic per CTA.
 template <class T>
 __global__ void __launch_bounds__(256)
 k_feasible(const T* __restrict__ U, const T* __restrict__ L, int n, int ld, long long bstride,
-           unsigned char* __restrict__ mask, unsigned long long* __restrict__ count) {
+           bool vec, unsigned char* __restrict__ mask, unsigned long long* __restrict__ count) {
+    using V4 = typename El<T>::V4;
     const size_t off = (size_t)blockIdx.z * (size_t)bstride;
     U += off;
     L += off;
     if (mask) mask += off;
     unsigned int c = 0;
+    const int stride = gridDim.x * blockDim.x;
+    const int j0 = blockIdx.x * blockDim.x + threadIdx.x;
     for (int i = blockIdx.y; i < n; i += gridDim.y) {
         const T* Ui = U + (size_t)i * ld;
         const T* Li = L + (size_t)i * ld;
-        for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
-            const bool bad = Li[j] > Ui[j];
-            c += bad;
-            if (mask) mask[(size_t)i * ld + j] = bad ? 1 : 0;
+        if (vec) {
+            const int nq = n / 4;
+            for (int q = j0; q < nq; q += stride) {
+                const V4 u = reinterpret_cast<const V4*>(Ui)[q];
+                const V4 l = reinterpret_cast<const V4*>(Li)[q];
+                const unsigned b0 = l.x > u.x, b1 = l.y > u.y, b2 = l.z > u.z, b3 = l.w > u.w;
+                c += b0 + b1 + b2 + b3;
+                if (mask)
+                    reinterpret_cast<uchar4*>(mask + (size_t)i * ld)[q] =
+                        make_uchar4((unsigned char)b0, (unsigned char)b1, (unsigned char)b2,
+                                    (unsigned char)b3);
+            }
+            for (int j = 4 * nq + j0; j < n; j += stride) {   // the last n % 4 cells
+                const bool bad = Li[j] > Ui[j];
+                c += bad;
+                if (mask) mask[(size_t)i * ld + j] = bad ? 1 : 0;
+            }
+        } else {
+            for (int j = j0; j < n; j += stride) {
+                const bool bad = Li[j] > Ui[j];
+                c += bad;
+                if (mask) mask[(size_t)i * ld + j] = bad ? 1 : 0;
+            }
         }
     }
     c = __reduce_add_sync(0xffffffffu, c);
@@ -85,9 +111,11 @@ static cudaError_t feasible_t(const Mats& m, unsigned char* mask, unsigned long 
         const int nbz = m.batch - b0 < 65535 ? m.batch - b0 : 65535;
         const size_t o = (size_t)b0 * m.bstride;
         before_launch(s, PH_ROUND);
+        // 16-byte loads need 16-byte rows (m.vec) and, for the mask, 4-byte rows
+        const bool vec = m.vec && (!mask || reinterpret_cast<uintptr_t>(mask) % 4 == 0);
         k_feasible<T><<<pass_grid(m.n, nbz), 256, 0, s>>>(
             static_cast<const T*>(m.U) + o, static_cast<const T*>(m.L) + o, m.n, m.ld,
-            m.bstride, mask ? mask + o : nullptr, count);
+            m.bstride, vec, mask ? mask + o : nullptr, count);
         after_launch(s, PH_ROUND);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -129,16 +129,18 @@ def test_upper_only(n, dtype, algo):
     assert ok and same_bits(Ug, Uo)
 
 
-@pytest.mark.parametrize("n", [1, 64, 131])
+@pytest.mark.parametrize("n,pad", [(1, 4), (64, 4), (131, 4), (131, 1), (131, 5), (257, 3)])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-def test_feasibility_count_and_mask(n, dtype):
+def test_feasibility_count_and_mask(n, pad, dtype):
+    """Rows of 16-byte multiples take the 4-cell path (with a tail when n is
+    not a multiple of 4); others the 1-cell path.  Padding columns untouched."""
     Uq, Lq = W.random_bounds(n, 6000 + n, p_known=0.4, p_bad=0.05)
     U0, L0 = as_dtype(Uq, Lq, dtype)
     Uo, Lo = oracle.smooth(U0, L0)
-    ld = n + 4
+    ld = n + pad
     t = torch()
-    U = dev(np.pad(Uo, ((0, 0), (0, 4))))
-    L = dev(np.pad(Lo, ((0, 0), (0, 4))))
+    U = dev(np.pad(Uo, ((0, 0), (0, pad))))
+    L = dev(np.pad(Lo, ((0, 0), (0, pad))))
     mask = t.full((n, ld), 7, dtype=t.uint8, device="cuda")
     cnt = bsm.bs_check_feasible(U, L, n, ld, None, None, mask)
     assert cnt == oracle.count_infeasible(Uo, Lo)
