@@ -7,7 +7,8 @@
 namespace bs {
 
 // Floyd-Warshall block (tile) sizes of the three-phase schedule: 128 for large
-// matrices, 64 for small ones (a quarter of the serial work per block round).
+// matrices, 64 for small ones (an eighth of the serial phase-1 work per block
+// round, and four times the tiles to spread over the SMs).
 constexpr int FB_LARGE = 128;
 constexpr int FB_SMALL = 64;
 

@@ -2,7 +2,7 @@
 //
 // The matrix is cut into FB x FB tiles; block round K processes the middle
 // atoms k of tile-row K in order, in three launches:
-//   phase 1: tile (K,K), k serially, one CTA (this file);
+//   phase 1: tile (K,K), its closure over block K, one CTA (this file);
 //   phase 2: row panel (K,J) and column panel (I,K) against the finished
 //            diagonal tile (phase3.cu);
 //   phase 3: every other tile (I,J), against the finished panels (phase3.cu).
@@ -29,9 +29,8 @@
 // inequalities, the same as the round-by-round schedule (exactly in int32; in
 // fp32 exactly for values on the 1/1024 grid below 2^14).
 //
-// Inside phase 1 each step k is round-synchronous: every thread keeps its
-// cells in registers and row and column k are published to shared memory,
-// double-buffered, one barrier per middle atom.
+// Phase 1 itself applies the same blocked scheme one level down (below); only
+// its 16-wide sub-blocks are closed step by step, each step round-synchronous.
 #include "pairops.cuh"
 
 namespace bs {
