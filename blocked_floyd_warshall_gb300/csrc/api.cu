@@ -271,10 +271,10 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
     }
     cudaError_t e = cudaSuccess;
     if (perk) {
-        for (int k = 0; k < n && e == cudaSuccess; ++k) {
-            e = bs::launch_round(is_int, m, k, literal, s);
-            if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
-        }
+        // each round's launch also applies the row/column k update of the round
+        // before it (perk.cu); the last round's has its own launch
+        for (int k = 0; k < n && e == cudaSuccess; ++k) e = bs::launch_round(is_int, m, k, literal, s);
+        if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, n - 1, s);
     } else {
         e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0, d);
     }
