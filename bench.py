@@ -60,7 +60,7 @@ def tile_size(n, flags=0, batch=1):
     if flags & (1 << 6):
         return 128
     nb = (n + 127) // 128
-    return 128 if (nb - 1) ** 2 * batch >= 768 else 64
+    return 128 if (nb - 1) ** 2 * batch >= 3000 else 64
 
 
 def phase_cells(n, fb, sym=False):

@@ -111,17 +111,19 @@ void release_side(DeviceState* d, const SideCtx& c) {
     d->free_side.push_back(c);
 }
 
-// Tile size for the blocked schedule: 128 x 128 tiles (the faster phase-3
-// kernel) once a block round's phase 3 at that size holds at least 768 tiles
-// over the batch (about five per SM), else 64 x 64 (twice the block rounds,
-// but more tiles to spread and an eighth of the phase-1 work per round).
-// Measured on the GB300: n = 3000 is faster with 64, n = 4096 and 256
-// molecules of n = 512 with 128.
+// Tile size for the blocked schedule: 64 x 64 unless a block round's phase 3
+// at 128 holds at least 3000 tiles over the batch (single matrices from about
+// n = 7100 on), then 128 x 128.  With the 128-thread form of the 64-wide
+// product, 64-wide tiles are as fast as 128-wide ones on large matrices
+// (n = 8192 and 16384 measured equal on the GB300) and faster below them
+// (n = 3000: 5.9 against 7.4 ms; n = 4096: 13.8 against 14.0; 256 molecules
+// of n = 512: 6.6 against 6.8), where the smaller tiles spread further; 128
+// halves the block rounds of the largest matrices.
 int choose_tile(int n, int batch, int mode) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
     if (mode & BS_TILE_128) return bs::FB_LARGE;
     const double nb = (double)((n + bs::FB_LARGE - 1) / bs::FB_LARGE);
-    return (nb - 1) * (nb - 1) * batch >= 768.0 ? bs::FB_LARGE : bs::FB_SMALL;
+    return (nb - 1) * (nb - 1) * batch >= 3000.0 ? bs::FB_LARGE : bs::FB_SMALL;
 }
 
 // The blocked schedule.  Without look-ahead: for each block round K, phase 1,
