@@ -54,13 +54,14 @@ def make_workload(name):
 
 
 def tile_size(n, flags=0, batch=1):
-    """Tile size the library picks (mirrors its rule; forced by the tile bits)."""
+    """Tile size the library picks (mirrors its rule; forced by the tile bits;
+    flags bit 0 set: int32)."""
     if flags & (1 << 5):
         return 64
     if flags & (1 << 6):
         return 128
     nb = (n + 127) // 128
-    return 128 if (nb - 1) ** 2 * batch >= 3000 else 64
+    return 128 if (nb - 1) ** 2 * batch >= (768 if flags & 1 else 3000) else 64
 
 
 def phase_cells(n, fb, sym=False):

@@ -119,11 +119,14 @@ void release_side(DeviceState* d, const SideCtx& c) {
 // (n = 3000: 5.9 against 7.4 ms; n = 4096: 13.8 against 14.0; 256 molecules
 // of n = 512: 6.6 against 6.8), where the smaller tiles spread further; 128
 // halves the block rounds of the largest matrices.
+// The int32 product on 64-wide tiles does not gain as much (n = 4096: 14.6
+// against 14.1 ms with 128), so int32 keeps 128 from 768 tiles on.
 int choose_tile(int n, int batch, int mode) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
     if (mode & BS_TILE_128) return bs::FB_LARGE;
     const double nb = (double)((n + bs::FB_LARGE - 1) / bs::FB_LARGE);
-    return (nb - 1) * (nb - 1) * batch >= 3000.0 ? bs::FB_LARGE : bs::FB_SMALL;
+    const double from = (mode & BS_DTYPE_MASK) == BS_INT32_Q10 ? 768.0 : 3000.0;
+    return (nb - 1) * (nb - 1) * batch >= from ? bs::FB_LARGE : bs::FB_SMALL;
 }
 
 // The blocked schedule.  Without look-ahead: for each block round K, phase 1,
