@@ -284,9 +284,10 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
 
 // ---------------------------------------------------------------- strips
 //
-// When a launch has fewer 64-wide tiles than a fraction of the SMs (small n:
-// a block round of n = 256 has 9 bulk tiles and 6 panel tiles), each tile is
-// split among SPLIT CTAs, each computing one strip of it, so that more SMs
+// When a launch has fewer 64-wide tiles than half the SMs (small n: a block
+// round of n = 256 has 9 bulk tiles and 6 panel tiles), each tile is split
+// among SPLIT = 4 CTAs (the template also takes 2), each computing one strip
+// of it, so that more SMs
 // share the round's critical path.  A strip is the 64 rows x 64/SPLIT columns
 // of the tile, or for a column panel 64/SPLIT rows x 64 columns: a CTA then
 // reads of its own tile (the panel operand of phase 2) only the lines it
@@ -487,9 +488,7 @@ static cudaError_t setup3() {
     set(k_phase3<T, false, FB_SMALL, false>, P3Smem<T, false, FB_SMALL>::BYTES);
     set(k_phase3<T, true, FB_SMALL, true>, P3Smem<T, true, FB_SMALL>::BYTES);
     set(k_phase3<T, false, FB_SMALL, true>, P3Smem<T, false, FB_SMALL>::BYTES);
-    set(k_strip<T, true, 2>, StripSmem<T, true>::BYTES);
     set(k_strip<T, true, 4>, StripSmem<T, true>::BYTES);
-    set(k_strip<T, false, 2>, StripSmem<T, false>::BYTES);
     set(k_strip<T, false, 4>, StripSmem<T, false>::BYTES);
     return e;
 }
@@ -545,20 +544,20 @@ static cudaError_t strip_t(const Mats& m, int K, int part, cudaStream_t s) {
     });
 }
 
-// 64-wide tiles: with at most half a tile per SM, four strips per tile; with
-// at most one, two strips; with at most two tiles per SM the wide form; else
-// the 8 x 8 form.  (Measured on the GB300: n = 2048, where the next block row
-// and column and the panels, 61 and 62 tiles, run on the look-ahead critical
-// path, is 12 % faster with four strips than with two; n = 1000's 225 bulk
-// tiles are 8 % slower as strips than in the wide form.)
+// 64-wide tiles, by tiles per SM in the launch: up to half, four strips per
+// tile; up to one, the wide form (a tile per SM, latency-bound); more, the
+// 8 x 4 form, four CTAs per SM.  (Measured on the GB300: n = 2048, where the
+// next block row and column and the panels, 61 and 62 tiles, run on the
+// look-ahead critical path, is 12 % faster with four strips than with two;
+// n = 1000's 196 and 225 bulk tiles are 6 % faster in the 8 x 4 form than in
+// the wide form and 8 % slower as strips.)
 template <class T, bool HAS_L>
 static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
     if (m.fb == FB_LARGE) return phase3_t<T, HAS_L, FB_LARGE, false>(m, K, part, s);
     const int nb = (m.n + FB_SMALL - 1) / FB_SMALL;
     const double ctas = (double)p3_tiles(m.sym, part, nb, K) * m.batch;
-    if (4.0 * ctas <= 2.0 * m.sms) return strip_t<T, HAS_L, 4>(m, K, part, s);
-    if (2.0 * ctas <= m.sms) return strip_t<T, HAS_L, 2>(m, K, part, s);
-    return ctas <= 2.0 * m.sms ? phase3_t<T, HAS_L, FB_SMALL, true>(m, K, part, s)
+    if (2.0 * ctas <= m.sms) return strip_t<T, HAS_L, 4>(m, K, part, s);
+    return ctas <= 1.0 * m.sms ? phase3_t<T, HAS_L, FB_SMALL, true>(m, K, part, s)
                                : phase3_t<T, HAS_L, FB_SMALL, false>(m, K, part, s);
 }
 
