@@ -633,6 +633,44 @@ def test_cuda_graph_capture_and_replay(sched):
         assert same_bits(host(U), Uo) and same_bits(host(L), Lo)
 
 
+@pytest.mark.parametrize("n", [700, 2000])
+def test_concurrent_calls_on_own_streams(n):
+    """Three host threads smooth three molecules at once, each on its own
+    stream (each call takes its own look-ahead stream and events); then work
+    queued on each caller's stream after the call sees the finished result
+    (the look-ahead stream is joined back into the caller's stream)."""
+    import threading
+    t = torch()
+    mols = [W.random_bounds(n, 9500 + b, p_bad=0.01) for b in range(3)]
+    want = [oracle.smooth(W.to_f32(u), W.to_f32(l)) for u, l in mols]
+    bsm.bs_smooth_bounds(dev(W.to_f32(mols[0][0])), dev(W.to_f32(mols[0][1])))   # set-up
+    t.cuda.synchronize()
+    streams = [t.cuda.Stream() for _ in mols]
+    bufs = [(dev(W.to_f32(u)), dev(W.to_f32(l))) for u, l in mols]
+    outs = [(t.empty_like(u), t.empty_like(l)) for u, l in bufs]
+    errors = []
+
+    def work(b):
+        try:
+            with t.cuda.stream(streams[b]):
+                U, L = bufs[b]
+                bsm.bs_smooth_bounds(U, L, stream=streams[b])
+                outs[b][0].copy_(U)          # queued after the call on the same stream
+                outs[b][1].copy_(L)
+        except Exception as e:               # reported below, in the test thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(b,)) for b in range(len(mols))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for b, s in enumerate(streams):
+        s.synchronize()
+        assert same_bits(host(outs[b][0]), want[b][0]) and same_bits(host(outs[b][1]), want[b][1])
+
+
 def test_literal_rule_rejected_in_blocked_mode():
     U, L = dev(np.zeros((4, 4), np.float32)), dev(np.zeros((4, 4), np.float32))
     with pytest.raises(bsm.BSError) as e:
