@@ -510,7 +510,8 @@ def main():
 SCHEDULE_FLAGS = {"auto": 0, "t64": (1 << 5) | (1 << 9), "t128": (1 << 6) | (1 << 9),
                   "t64_serial": (1 << 5) | (1 << 7), "t128_serial": (1 << 6) | (1 << 7),
                   "perk": 1 << 2, "sym": 1 << 8,
-                  "graph": 0}   # "graph": the auto schedule captured once, replayed
+                  "graph": 0,   # "graph": the auto schedule captured once, replayed
+                  "upper": 0}   # "upper": bs_smooth_upper, U alone
 ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial", "sym")
 SWEEP = (
     # (config, dtype, schedules, description); config None: random bounds of size n
@@ -518,10 +519,10 @@ SWEEP = (
     (1, "f32", ALL_SCHEDULES + ("graph",), "chain n=1000"),
     (("random", 2048), "f32", ALL_SCHEDULES + ("graph",), "random bounds n=2048"),
     (("random", 3000), "f32", ("auto", "t64", "t128", "t128_serial"), "random bounds n=3000"),
-    (2, "f32", ALL_SCHEDULES + ("perk",), "globule n=4096"),
+    (2, "f32", ALL_SCHEDULES + ("perk", "upper"), "globule n=4096"),
     (2, "i32", ("auto",), "globule n=4096"),
     (3, "f32", ALL_SCHEDULES, "256 chains n=512, batched"),
-    (4, "f32", ("auto", "t128_serial", "sym"), "globule n=16384"),
+    (4, "f32", ("auto", "t128_serial", "sym", "upper"), "globule n=16384"),
 )
 
 
@@ -555,7 +556,9 @@ def sweep(args):
             times = []
 
             def call(U, L):
-                if batch > 1:
+                if algo == "upper":
+                    bsm.bs_smooth_upper(U, flags=flags)
+                elif batch > 1:
                     bsm.bs_smooth_bounds_batched(U, L, flags=flags)
                 else:
                     bsm.bs_smooth_bounds(U, L, flags=flags)
@@ -603,6 +606,9 @@ def sweep(args):
                 executed = batch * float(sum(phase_cells(n, tile_size(n, flags, batch), sym=True)))
                 line["executed_cell_updates"] = executed
                 line["fp32_alu_frac_executed"] = executed / (ms * 1e-3) * OPS_PER_CELL / alu
+            if algo == "upper":
+                # U alone: an add and a min per cell update
+                line["fp32_alu_frac_upper"] = rate * 2 / alu
             if algo == "perk":
                 gbs = rate * 16 / 1e9
                 line["hbm_gbs_algorithmic"] = gbs
