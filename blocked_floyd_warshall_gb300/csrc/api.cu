@@ -159,12 +159,14 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
     SideCtx c;
     e = acquire_side(d, &c);
     if (e != cudaSuccess) return e;
-    // With fewer rest-of-round tiles than two per SM, REST(K) would fill the
-    // SMs the moment it is ready and phase 1 of round K+1, on the critical
-    // path, would wait for one of its CTAs to finish; REST(K) then waits for
-    // NEXT(K) instead (which follows phase 2 of round K on the side stream),
-    // so phase 1 is dispatched first.
-    const bool tight = (double)(nb - 2) * (nb - 2) * m.batch < 2.0 * m.sms;
+    // With fewer rest-of-round tiles than SMs, REST(K) would take the SMs
+    // the moment it is ready and phase 1 of round K+1, on the critical path,
+    // would wait for its CTAs to finish; REST(K) then waits for NEXT(K)
+    // instead (which follows phase 2 of round K on the side stream), so
+    // phase 1 is dispatched first.  With more, REST(K) is long enough that
+    // starting it early pays more (measured).
+    const double rest_tiles = m.sym ? 0.5 * (nb - 2) * (nb - 1) : (double)(nb - 2) * (nb - 2);
+    const bool tight = rest_tiles * m.batch < m.sms;
     // main_done[1] stands for "REST(-1)": everything enqueued on s so far.
     e = cudaEventRecord(c.main_done[1], s);
     bool forked = false;   // side work enqueued that s has not yet waited for

@@ -34,7 +34,11 @@ def as_dtype(Uq, Lq, dtype):
 
 
 SIZES_PERK = [1, 2, 3, 4, 5, 7, 31, 33, 64, 255, 256]
-SIZES_BLOCKED = [1, 2, 3, 5, 31, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 383, 385, 513]
+# the last 64-wide tile ends on every kind of 16-row stripe boundary: inside
+# the first stripe (1, 2, 3, 5), on one (16, 48, 96 = 64 + 32), inside a later
+# one (31, 63, 300 = 256 + 44)
+SIZES_BLOCKED = [1, 2, 3, 5, 16, 31, 48, 63, 64, 65, 96, 127, 128, 129, 255, 256, 257, 300, 383,
+                 385, 513]
 # blocked-mode schedules: automatic, forced tile sizes, with and without look-ahead
 SCHEDULES = {
     "auto": 0,
