@@ -87,8 +87,9 @@ def phase_cells(n, fb, sym=False):
 def next_cells(n, fb):
     """Cell updates of the look-ahead launches of one blocked smoothing: the
     tiles of block row and column K+1 (outside row and column K) in block
-    rounds K < nb - 1.  They run on the library's side stream; the rest of
-    phase 3 runs on the caller's stream."""
+    rounds K < nb - 1.  They run on the library's side streams (for small
+    matrices tile (K+1, K+1)'s share inside phase 1 of round K+1); the rest
+    of phase 3 runs on the caller's stream."""
     nb = (n + fb - 1) // fb
     sizes = [min(fb, n - K * fb) for K in range(nb)]
     cells = 0

@@ -497,6 +497,15 @@ constexpr int CL = FB_SMALL / SB;   // CTAs per cluster: one per 16-row stripe
 constexpr int CNT = CL * AT;        // threads per CTA: one group per sub-block column
 constexpr int CS = SB + 2;          // row stride of the row-major 16 x 16 buffers (pairs aligned)
 static_assert(CNT == SB * SB, "one thread per cell of a 16 x 16 block");
+constexpr int PTS = FB_SMALL + 2;   // row stride of the staged column panel stripe
+
+// Dynamic shared memory of a launch that first applies the previous block
+// round's update (pre): the row panel tile k-interleaved and this stripe's
+// rows of the column panel tile, U and L.
+template <bool HAS_L>
+constexpr size_t p1c_pre_bytes() {
+    return (HAS_L ? 2 : 1) * (size_t)(FB_SMALL * FB_SMALL + SB * PTS) * 4;
+}
 
 template <class T>
 struct P1CSmem {
@@ -563,16 +572,16 @@ __device__ __forceinline__ void p1c_push_k(T* dU, T* dL, int i, int j, const T (
 
 // Product step for the thread's cells (i, j0 .. j0+3): X[i,j] against
 // A[i,k] (row i of a row-major array: aU, aL at row i) and B[k,j]
-// (k-interleaved, BW columns; the thread's columns at jb), middle atoms in
-// pairs as in phase 3.
-template <class T, bool HAS_L, int BW>
+// (k-interleaved, BW columns; the thread's columns at jb) over KN middle
+// atoms, in pairs as in phase 3.
+template <class T, bool HAS_L, int BW, int KN = SB>
 __device__ __forceinline__ void p1c_product(T (&u)[4], T (&l)[4], const T* aU, const T* aL,
                                             const T* bU, const T* bL, int jb) {
     using LD = PairLoad<T>;
     using P = typename LD::P;
     constexpr bool NEG = std::is_same<T, int>::value;
-#pragma unroll
-    for (int kk = 0; kk < SB; kk += 2) {
+#pragma unroll 8
+    for (int kk = 0; kk < KN; kk += 2) {
         P a = LD::ld2(aU + kk);
         P al = a;
         if (HAS_L) al = LD::ld2(aL + kk);
@@ -654,10 +663,12 @@ __device__ __forceinline__ void p1c_get_rows(const T (*buf)[SB * CS], int i, int
 
 template <class T, bool HAS_L>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CNT)
-k_phase1c(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec) {
+k_phase1c(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K, bool vec,
+          bool pre) {
     using E = El<T>;
     constexpr int FB = FB_SMALL;
     __shared__ P1CSmem<T> sm;
+    extern __shared__ __align__(16) unsigned char p1c_dyn[];
 
     const int c = blockIdx.x;                 // cluster rank = stripe
     const int g = threadIdx.x / AT;           // column block held
@@ -694,6 +705,80 @@ k_phase1c(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride
             u[q] = in ? Ur[j0 + q] : E::upad();
             l[q] = HAS_L ? (in ? Lr[j0 + q] : E::lpad()) : T(0);
         }
+    }
+
+    // Block round K-1's update of this tile, which the look-ahead schedule
+    // leaves to this launch: X = X + C R over the middle atoms of block K-1
+    // (min-plus, the phase-3 rules), C = tile (K, K-1) (this stripe's rows),
+    // R = tile (K-1, K), both staged here, R k-interleaved.  Block K-1 is
+    // full, so only the columns of R and the rows of C beyond m get pads.
+    if (pre) {
+        T* RU = reinterpret_cast<T*>(p1c_dyn);
+        T* RL = RU + FB * FB;
+        T* CU = RU + (HAS_L ? 2 : 1) * FB * FB;
+        T* CL = CU + SB * PTS;
+        const int op = o - FB;
+        const size_t rg = off + (size_t)op * ld + o;             // tile (K-1, K)
+        const size_t cg = off + (size_t)(o + c * SB) * ld + op;  // tile (K, K-1), stripe c
+        using V4 = typename E::V4;
+        for (int e = threadIdx.x; e < FB * FB / 4; e += CNT) {
+            const int k = e / (FB / 4), j = (e % (FB / 4)) * 4;
+            T xu[4], xl[4];
+            if (vec && j + 4 <= m) {
+                const V4 v = *reinterpret_cast<const V4*>(U + rg + (size_t)k * ld + j);
+                xu[0] = v.x; xu[1] = v.y; xu[2] = v.z; xu[3] = v.w;
+                if (HAS_L) {
+                    const V4 w = *reinterpret_cast<const V4*>(L + rg + (size_t)k * ld + j);
+                    xl[0] = w.x; xl[1] = w.y; xl[2] = w.z; xl[3] = w.w;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const bool in = j + q < m;
+                    xu[q] = in ? U[rg + (size_t)k * ld + j + q] : E::upad();
+                    xl[q] = HAS_L ? (in ? L[rg + (size_t)k * ld + j + q] : E::lpad()) : T(0);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int d = (k >> 1) * (2 * FB) + 2 * (j + q) + (k & 1);
+                RU[d] = xu[q];
+                if (HAS_L) RL[d] = xl[q];
+            }
+        }
+        for (int e = threadIdx.x; e < SB * FB / 4; e += CNT) {
+            const int r = e / (FB / 4), k = (e % (FB / 4)) * 4;
+            T xu[4], xl[4];
+            if (c * SB + r < m) {
+                if (vec) {
+                    const V4 v = *reinterpret_cast<const V4*>(U + cg + (size_t)r * ld + k);
+                    xu[0] = v.x; xu[1] = v.y; xu[2] = v.z; xu[3] = v.w;
+                    if (HAS_L) {
+                        const V4 w = *reinterpret_cast<const V4*>(L + cg + (size_t)r * ld + k);
+                        xl[0] = w.x; xl[1] = w.y; xl[2] = w.z; xl[3] = w.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        xu[q] = U[cg + (size_t)r * ld + k + q];
+                        xl[q] = HAS_L ? L[cg + (size_t)r * ld + k + q] : T(0);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    xu[q] = E::upad();
+                    xl[q] = E::lpad();
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                CU[r * PTS + k + q] = xu[q];
+                if (HAS_L) CL[r * PTS + k + q] = xl[q];
+            }
+        }
+        __syncthreads();
+        p1c_product<T, HAS_L, FB, FB>(u, l, CU + i * PTS, CL + i * PTS, RU, RL, j0);
     }
     cluster_wait();
 
@@ -778,6 +863,8 @@ static cudaError_t setup1() {
     set(k_phase1<T, false, FB_LARGE>, P1Smem<T, false, FB_LARGE>::BYTES);
     set(k_phase1<T, true, FB_SMALL>, P1Smem<T, true, FB_SMALL>::BYTES);
     set(k_phase1<T, false, FB_SMALL>, P1Smem<T, false, FB_SMALL>::BYTES);
+    set(k_phase1c<T, true>, p1c_pre_bytes<true>());
+    set(k_phase1c<T, false>, p1c_pre_bytes<false>());
     return e;
 }
 
@@ -801,27 +888,30 @@ static cudaError_t phase1_t(const Mats& m, int K, cudaStream_t s) {
 }
 
 template <class T, bool HAS_L>
-static cudaError_t phase1c_t(const Mats& m, int K, cudaStream_t s) {
+static cudaError_t phase1c_t(const Mats& m, int K, bool pre, cudaStream_t s) {
     return for_batch_chunks(m, [&](int b0, int nbz) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
         before_launch(s, PH_ONE);
-        const cudaError_t e = launch_prio(k_phase1c<T, HAS_L>, dim3(CL, 1, nbz), dim3(CNT), 0, s,
-                                          U, L, m.n, m.ld, m.bstride, K, m.vec);
+        const size_t dyn = pre ? p1c_pre_bytes<HAS_L>() : 0;
+        const cudaError_t e = launch_prio(k_phase1c<T, HAS_L>, dim3(CL, 1, nbz), dim3(CNT), dyn,
+                                          s, U, L, m.n, m.ld, m.bstride, K, m.vec, pre);
         after_launch(s, PH_ONE);
         return e;
     });
 }
 
 template <class T, bool HAS_L>
-static cudaError_t phase1_fb(const Mats& m, int K, cudaStream_t s) {
-    if (m.fb == FB_SMALL) return phase1c_t<T, HAS_L>(m, K, s);
+static cudaError_t phase1_fb(const Mats& m, int K, bool pre, cudaStream_t s) {
+    if (m.fb == FB_SMALL) return phase1c_t<T, HAS_L>(m, K, pre && K > 0, s);
+    if (pre) return cudaErrorInvalidValue;   // 128-wide tiles: NEXT keeps the diagonal tile
     return phase1_t<T, HAS_L, FB_LARGE>(m, K, s);
 }
 
-cudaError_t launch_phase1(bool is_int, const Mats& m, int K, cudaStream_t s) {
-    if (is_int) return m.L ? phase1_fb<int, true>(m, K, s) : phase1_fb<int, false>(m, K, s);
-    return m.L ? phase1_fb<float, true>(m, K, s) : phase1_fb<float, false>(m, K, s);
+cudaError_t launch_phase1(bool is_int, const Mats& m, int K, bool pre, cudaStream_t s) {
+    if (is_int)
+        return m.L ? phase1_fb<int, true>(m, K, pre, s) : phase1_fb<int, false>(m, K, pre, s);
+    return m.L ? phase1_fb<float, true>(m, K, pre, s) : phase1_fb<float, false>(m, K, pre, s);
 }
 
 }  // namespace bs
