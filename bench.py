@@ -84,12 +84,30 @@ def phase_cells(n, fb, sym=False):
     return p1, p2, p3
 
 
+def diag_cells(n, fb):
+    """Cell updates of tile (K+1, K+1) in block rounds K < nb - 1: with the
+    merged look-ahead of small matrices phase 1 of round K+1 applies them,
+    and the caller's stream runs the rest of each round's phase 3."""
+    nb = (n + fb - 1) // fb
+    sizes = [min(fb, n - K * fb) for K in range(nb)]
+    return sum(sizes[K] * sizes[K + 1] ** 2 for K in range(nb - 1))
+
+
+def merged_lookahead(n, fb, batch, sms, sym=False):
+    """The library's rule for its merged look-ahead schedule (64-wide tiles,
+    fewer rest-of-round tiles than half the SMs)."""
+    nb = (n + fb - 1) // fb
+    if fb != 64 or nb < 3:
+        return False
+    rest = 0.5 * (nb - 2) * (nb - 1) if sym else float(nb - 2) ** 2
+    return rest * batch < 0.5 * sms
+
+
 def next_cells(n, fb):
     """Cell updates of the look-ahead launches of one blocked smoothing: the
     tiles of block row and column K+1 (outside row and column K) in block
-    rounds K < nb - 1.  They run on the library's side streams (for small
-    matrices tile (K+1, K+1)'s share inside phase 1 of round K+1); the rest
-    of phase 3 runs on the caller's stream."""
+    rounds K < nb - 1.  They run on the library's side stream; the rest of
+    phase 3 runs on the caller's stream."""
     nb = (n + fb - 1) // fb
     sizes = [min(fb, n - K * fb) for K in range(nb)]
     cells = 0
@@ -426,6 +444,8 @@ def main():
     fb = tile_size(n)
     p3_cells_step = phase_cells(n, fb)[2]
     main_cells_step = p3_cells_step - (next_cells(n, fb) if prof["phase3_next"]["launches"] else 0)
+    if merged_lookahead(n, fb, 1, sms):
+        main_cells_step -= diag_cells(n, fb)
     p3_ops_step = main_cells_step * OPS_PER_CELL
     p3_s_step = p3["ms"] * 1e-3 / args.steps
     p3_achieved = p3_ops_step / p3_s_step if p3["launches"] else None

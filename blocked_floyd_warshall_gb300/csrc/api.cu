@@ -16,10 +16,9 @@ constexpr int kMaxDevices = 64;
 // one exclusively while it enqueues, so concurrent callers never share events.
 struct SideCtx {
     cudaStream_t side = nullptr;
-    cudaStream_t next = nullptr;                     // NEXT(K) beside phase 1 (64-wide tiles)
     cudaEvent_t main_done[2] = {nullptr, nullptr};   // on the caller's stream, by round parity
     cudaEvent_t side_done = nullptr;                 // on the side stream
-    cudaEvent_t next_done = nullptr;                 // after NEXT(K)
+    cudaEvent_t next_done = nullptr;                 // on the side stream, after NEXT(K)
 };
 
 struct DeviceState {
@@ -95,14 +94,12 @@ cudaError_t acquire_side(DeviceState* d, SideCtx* out) {
     int lo = 0, hi = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, hi);
-    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.next, cudaStreamNonBlocking, hi);
     for (cudaEvent_t* ev : {&c.main_done[0], &c.main_done[1], &c.side_done, &c.next_done})
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {
         for (cudaEvent_t ev : {c.main_done[0], c.main_done[1], c.side_done, c.next_done})
             if (ev) cudaEventDestroy(ev);
         if (c.side) cudaStreamDestroy(c.side);
-        if (c.next) cudaStreamDestroy(c.next);
         return e;
     }
     *out = c;
@@ -145,13 +142,14 @@ int choose_tile(int n, int batch, int mode) {
 // and (K+1,K), which REST(K) does not read; it writes tiles outside
 // block-rows and -columns K and K+1.  NEXT(K)'s short wave thus overlaps
 // REST(K) instead of running alone (except with few rest tiles, see below).
-// With 64-wide tiles and few rest tiles a third stream takes NEXT(K)
-// without tile (K+1,K+1) (P3_NEXT_OFF), and phase 1 of round K+1 on the side
-// stream applies round K's update to that tile itself before closing it, so
-// NEXT(K) and phase 1 run side by side: phase 1 reads tiles (K+1,K) and (K,K+1), which NEXT(K)
-// only reads too, and writes tile (K+1,K+1), which NEXT(K) leaves alone;
-// both wait for REST(K-1), which writes tile (K+1,K+1) and the other tiles
-// of block-row and -column K+1, and phase 2 of round K+1 waits for both.
+// With 64-wide tiles and few rest tiles (see `merged` below) phase 3 of
+// round K runs whole but for tile (K+1,K+1) (P3_ALL_OFF) on `s`, and phase 1
+// of round K+1 on the side stream applies round K's update to that tile
+// itself before closing it, so the two run side by side: phase 1 reads tiles
+// (K+1,K) and (K,K+1), which phase 3 only reads too, and writes tile
+// (K+1,K+1), which phase 3 leaves alone; phase 1 waits for phase 3 of round
+// K-1 (which writes tile (K+1,K+1)), phase 2 of round K+1 for phase 3 of
+// round K, and phase 3 of round K+1 for phase 2 of round K+1.
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
                         DeviceState* d) {
     const int nb = (m.n + m.fb - 1) / m.fb;
@@ -187,17 +185,33 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
         if (r == cudaSuccess) r = cudaEventRecord(c.main_done[K & 1], s);
         return r;
     };
-    // 64-wide tiles, fewer rest tiles than half the SMs (the chain NEXT(K),
-    // phases 1 and 2 of round K+1 is then the critical path): NEXT(K) leaves
-    // tile (K+1,K+1) to phase 1 of round K+1, which applies round K's update
-    // to it first, and runs on a stream of its own beside that phase 1;
-    // phase 2 of round K+1 waits for both.  Measured: n = 256 0.141 -> 0.128
-    // ms, n = 512 0.273 -> 0.247 ms.  With more rest tiles the chain matters
-    // less and the extra product in phase 1 costs (n = 768: 0.41 against
-    // 0.43 ms; n = 2048: 2.20 against 2.27 ms).
-    const bool split = m.fb == bs::FB_SMALL && rest_tiles * m.batch < 0.5 * m.sms;
-    bool next_pending = false;   // NEXT(K) recorded on c.next, not yet waited for
-    for (int K = 0; K + 1 < nb && e == cudaSuccess; ++K) {
+    // 64-wide tiles, fewer rest tiles than half the SMs: the chain NEXT(K),
+    // phases 1 and 2 of round K+1 is then the critical path, so NEXT(K) and
+    // REST(K) become one launch without tile (K+1,K+1), beside phase 1 of
+    // round K+1, which applies round K's update to that tile first.
+    // Measured: n = 256 0.141 -> 0.128 ms, n = 512 0.273 -> 0.247 ms.  With
+    // more rest tiles the extra product in phase 1 costs more than the
+    // overlap gains (n = 768: 0.43 against 0.39-0.41 ms; n = 2048: 2.27
+    // against 2.20 ms).
+    const bool merged = m.fb == bs::FB_SMALL && rest_tiles * m.batch < 0.5 * m.sms;
+    for (int K = 0; merged && K + 1 < nb && e == cudaSuccess; ++K) {
+        // s: phase 3 of round K but tile (K+1,K+1), after phase 2 of round K
+        if (forked) e = cudaStreamWaitEvent(s, c.side_done, 0);
+        forked = false;
+        if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, bs::P3_ALL_OFF, s);
+        if (e == cudaSuccess) e = cudaEventRecord(c.main_done[K & 1], s);
+        // side: phase 1 of round K+1 after phase 3 of round K-1, phase 2 of
+        // round K+1 after phase 3 of round K
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c.side, c.main_done[(K + 1) & 1], 0);
+        if (e != cudaSuccess) break;
+        forked = true;
+        e = bs::launch_phase1(is_int, m, K + 1, true, c.side);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c.side, c.main_done[K & 1], 0);
+        if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K + 1, c.side);
+        cudaError_t r = cudaEventRecord(c.side_done, c.side);
+        if (e == cudaSuccess) e = r;
+    }
+    for (int K = 0; !merged && K + 1 < nb && e == cudaSuccess; ++K) {
         if (!tight) {
             // REST(K) after phase 2 of round K
             e = rest(K, forked ? c.side_done : nullptr);
@@ -208,34 +222,17 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
         e = cudaStreamWaitEvent(c.side, c.main_done[(K + 1) & 1], 0);
         if (e != cudaSuccess) break;
         forked = true;
-        if (split) {
-            // c.next: after REST(K-1) and phase 2 of round K (on the side
-            // stream from round 1 on; on s, before main_done[1], for round 0)
-            e = cudaStreamWaitEvent(c.next, c.main_done[(K + 1) & 1], 0);
-            if (e == cudaSuccess && K > 0) e = cudaStreamWaitEvent(c.next, c.side_done, 0);
-            if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT_OFF, c.next);
-            if (e == cudaSuccess) e = cudaEventRecord(c.next_done, c.next);
-            if (e == cudaSuccess) next_pending = true;
-            if (e == cudaSuccess) e = bs::launch_phase1(is_int, m, K + 1, true, c.side);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(c.side, c.next_done, 0);
-            if (e == cudaSuccess) next_pending = false;
-        } else {
-            e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT, c.side);
-            if (e == cudaSuccess && tight) e = cudaEventRecord(c.next_done, c.side);
-            if (e == cudaSuccess) e = bs::launch_phase1(is_int, m, K + 1, false, c.side);
-        }
+        e = bs::launch_phase3(is_int, m, K, bs::P3_NEXT, c.side);
+        if (e == cudaSuccess && tight) e = cudaEventRecord(c.next_done, c.side);
+        if (e == cudaSuccess) e = bs::launch_phase1(is_int, m, K + 1, false, c.side);
         if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, K + 1, c.side);
         cudaError_t r = cudaEventRecord(c.side_done, c.side);
         if (e == cudaSuccess) e = r;
         if (e == cudaSuccess && tight) e = rest(K, c.next_done);
     }
-    // always join the side streams back, on success or failure
+    // always join the side stream back, on success or failure
     if (forked) {
         cudaError_t j = cudaStreamWaitEvent(s, c.side_done, 0);
-        if (e == cudaSuccess) e = j;
-    }
-    if (next_pending) {
-        cudaError_t j = cudaStreamWaitEvent(s, c.next_done, 0);
         if (e == cudaSuccess) e = j;
     }
     if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, nb - 1, bs::P3_ALL, s);

@@ -45,12 +45,12 @@ cudaError_t blocked_setup(bool is_int);   // once per device: shared-memory limi
 cudaError_t phase3_setup(bool is_int);
 // pre: first apply block round K-1's update to tile (K,K) (its product with
 // the panels of round K-1), which the look-ahead schedule then leaves out of
-// NEXT(K-1); 64-wide tiles only.
+// phase 3 of round K-1; 64-wide tiles only.
 cudaError_t launch_phase1(bool is_int, const Mats& m, int K, bool pre, cudaStream_t s);
 cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
 // Phase 3 of block round K over the tiles `part` selects (P3_* below).
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s);
-enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2, P3_PANELS = 3, P3_NEXT_OFF = 4 };
+enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2, P3_PANELS = 3, P3_ALL_OFF = 4 };
 
 // Feasibility count and precondition checks.  `count` and `flags` are device
 // words the caller has zeroed on `s`.

@@ -124,14 +124,14 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
 //   P3_ALL    : every tile outside block-row K and block-column K;
 //   P3_NEXT   : those in block-row K+1 or block-column K+1 (the tiles the next
 //               block round's phases 1 and 2 read and write);
-//   P3_NEXT_OFF: P3_NEXT without tile (K+1,K+1), whose update phase 1 of
-//               round K+1 takes over;
 //   P3_REST   : the others;
+//   P3_ALL_OFF: P3_ALL without tile (K+1,K+1), whose update phase 1 of round
+//               K+1 takes over;
 //   P3_PANELS : phase 2, the row panel (K,J) then the column panel (I,K).
 // With symmetric inputs only tiles with I <= J are computed (each off-diagonal
-// one is also stored transposed): (nb-1)nb/2, nb-1, nb-2 and (nb-2)(nb-1)/2
-// tiles; phase 2 computes the row panel and stores it transposed as the
-// column panel.
+// one is also stored transposed): (nb-1)nb/2, nb-1, (nb-2)(nb-1)/2 and
+// (nb-1)nb/2 - 1 tiles; phase 2 computes the row panel and stores it
+// transposed as the column panel.
 
 // t -> (a, b), a <= b, enumerating the upper triangle column by column.
 __device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
@@ -156,7 +156,8 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
         return;
     }
     if (!sym) {
-        if (part == P3_ALL) {
+        if (part == P3_ALL || part == P3_ALL_OFF) {
+            if (part == P3_ALL_OFF) t += t >= K * nb;   // skip (K+1,K+1): ti = tj = K
             const int ti = t / (nb - 1), tj = t % (nb - 1);
             I = ti + (ti >= K);
             J = tj + (tj >= K);
@@ -169,15 +170,6 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
                 I = u + 2 * (u >= K);
                 J = K + 1;
             }
-        } else if (part == P3_NEXT_OFF) {
-            if (t < nb - 2) {
-                I = K + 1;
-                J = t + 2 * (t >= K);
-            } else {
-                const int u = t - (nb - 2);
-                I = u + 2 * (u >= K);
-                J = K + 1;
-            }
         } else {
             const int ti = t / (nb - 2), tj = t % (nb - 2);
             I = ti + 2 * (ti >= K);
@@ -186,7 +178,8 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
         return;
     }
     int a, b;
-    if (part == P3_ALL) {
+    if (part == P3_ALL || part == P3_ALL_OFF) {
+        if (part == P3_ALL_OFF) t += t >= K * (K + 1) / 2 + K;   // skip (K+1,K+1): a = b = K
         p3_tri(t, a, b);
         I = a + (a >= K);
         J = b + (b >= K);
@@ -196,14 +189,6 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
             J = K + 1 + t;
         } else {
             I = t - (nb - K - 1);
-            J = K + 1;
-        }
-    } else if (part == P3_NEXT_OFF) {
-        if (t < nb - K - 2) {
-            I = K + 1;
-            J = K + 2 + t;
-        } else {
-            I = t - (nb - K - 2);
             J = K + 1;
         }
     } else {
@@ -522,11 +507,11 @@ static int p3_tiles(bool sym, int part, int nb, int K) {
     if (sym)
         return part == P3_ALL ? (nb - 1) * nb / 2
                : part == P3_NEXT ? (K + 1 < nb ? nb - 1 : 0)
-               : part == P3_NEXT_OFF ? (K + 1 < nb ? nb - 2 : 0)
+               : part == P3_ALL_OFF ? (K + 1 < nb ? (nb - 1) * nb / 2 - 1 : 0)
                                      : (K + 1 < nb ? (nb - 2) * (nb - 1) / 2 : 0);
     return part == P3_ALL ? (nb - 1) * (nb - 1)
            : part == P3_NEXT ? (K + 1 < nb ? 2 * nb - 3 : 0)
-           : part == P3_NEXT_OFF ? (K + 1 < nb ? 2 * nb - 4 : 0)
+           : part == P3_ALL_OFF ? (K + 1 < nb ? (nb - 1) * (nb - 1) - 1 : 0)
                                  : (K + 1 < nb ? (nb - 2) * (nb - 2) : 0);
 }
 
@@ -538,9 +523,7 @@ static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {
     return for_batch_chunks(m, [&](int b0, int nbz) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
-        const Phase ph = part == P3_PANELS               ? PH_TWO
-                         : part == P3_NEXT || part == P3_NEXT_OFF ? PH_NEXT
-                                                                  : PH_THREE;
+        const Phase ph = part == P3_PANELS ? PH_TWO : part == P3_NEXT ? PH_NEXT : PH_THREE;
         before_launch(s, ph);
         const cudaError_t e = launch_prio(k_phase3<T, HAS_L, FB, WIDE>, dim3(tiles, 1, nbz),
                                           dim3(P3S<FB, WIDE>::NT), P3Smem<T, HAS_L, FB>::BYTES, s,
@@ -558,9 +541,7 @@ static cudaError_t strip_t(const Mats& m, int K, int part, cudaStream_t s) {
     return for_batch_chunks(m, [&](int b0, int nbz) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
-        const Phase ph = part == P3_PANELS               ? PH_TWO
-                         : part == P3_NEXT || part == P3_NEXT_OFF ? PH_NEXT
-                                                                  : PH_THREE;
+        const Phase ph = part == P3_PANELS ? PH_TWO : part == P3_NEXT ? PH_NEXT : PH_THREE;
         before_launch(s, ph);
         const cudaError_t e = launch_prio(k_strip<T, HAS_L, SPLIT>, dim3(tiles, SPLIT, nbz),
                                           dim3(SNT), StripSmem<T, HAS_L>::BYTES, s, U, L, m.n,

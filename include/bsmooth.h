@@ -38,15 +38,16 @@
  * the matrices.  Smoothing calls return before the GPU finishes.
  * bs_check_feasible synchronises `stream` before it returns.  In blocked mode
  * with three or more block rows (unless BS_NO_LOOKAHEAD) the tiles of block
- * row and column K+1 and phases 1 and 2 of block round K+1 run on internal
- * high-priority streams of the library (two of them for small matrices),
- * forked from and joined back into `stream` with events inside the call,
- * while the rest of round K's phase 3 runs on `stream`; all work still
- * completes in `stream` order.  The
+ * row and column K+1 and phases 1 and 2 of block round K+1 run on an internal
+ * high-priority stream of the library, forked from and joined back into
+ * `stream` with events inside the call, while the rest of round K's phase 3
+ * runs on `stream` (for small matrices all of it but tile (K+1,K+1), whose
+ * update phase 1 of round K+1 applies); all work still completes in
+ * `stream` order.  The
  * smoothing calls can be captured into a CUDA graph (stream capture on
  * `stream`) once the library has run one smoothing of the same kind on the
  * device, which sets up its per-device state; the look-ahead fork and join
- * are captured with it, and the internal streams' priority is kept on their
+ * are captured with it, and the internal stream's priority is kept on its
  * kernels as a launch attribute.  Replaying a captured call saves the
  * per-launch host overhead, which matters for small n (n = 256: about a
  * quarter of the call).

@@ -695,12 +695,19 @@ def test_empty_and_launch_counting():
     before = bsm.bs_launch_count()
     bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)),
                          flags=bsm.BS_TILE_64 | bsm.BS_FORCE_LOOKAHEAD)
-    # 5 block rounds: 5 x (phase 1, phase 2); phase 3 split in two for rounds 0..3
-    assert bsm.bs_launch_count() - before == 5 + 5 + 4 * 2 + 1
+    # 5 block rounds: 5 x (phase 1, phase 2); 9 rest tiles, fewer than half
+    # the SMs: phase 3 of rounds 0..3 is one launch without the next
+    # diagonal tile (phase 1 of the next round takes it), then the last round
+    assert bsm.bs_launch_count() - before == 5 + 5 + 4 + 1
     before = bsm.bs_launch_count()
     bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_TILE_64)
     # look-ahead is the default from three block rounds on: the same launches
-    assert bsm.bs_launch_count() - before == 5 + 5 + 4 * 2 + 1
+    assert bsm.bs_launch_count() - before == 5 + 5 + 4 + 1
+    Uq7, Lq7 = W.random_bounds(700, 1, p_bad=0.01)
+    before = bsm.bs_launch_count()
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq7)), dev(W.to_f32(Lq7)), flags=bsm.BS_TILE_64)
+    # 11 block rounds, 81 rest tiles: phase 3 split in two for rounds 0..9
+    assert bsm.bs_launch_count() - before == 11 + 11 + 10 * 2 + 1
     before = bsm.bs_launch_count()
     bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)),
                          flags=bsm.BS_TILE_64 | bsm.BS_NO_LOOKAHEAD)
@@ -717,3 +724,9 @@ def test_profile_records_every_launch():
     # block row and column (look-ahead stream)
     assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 3, 2]
     assert p["phase3"]["ms"] > 0 and p["phase3_next"]["ms"] > 0
+    # 64-wide tiles, few rest tiles: phase 3 of each round but the last is
+    # one launch on the caller's stream, beside phase 1 of the next round
+    bsm.bs_profile_begin()
+    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_TILE_64)
+    p = bsm.bs_profile_end()
+    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 5, 5, 5, 0]
