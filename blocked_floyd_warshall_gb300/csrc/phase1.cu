@@ -497,7 +497,7 @@ constexpr int CL = FB_SMALL / SB;   // CTAs per cluster: one per 16-row stripe
 constexpr int CNT = CL * AT;        // threads per CTA: one group per sub-block column
 constexpr int CS = SB + 2;          // row stride of the row-major 16 x 16 buffers (pairs aligned)
 static_assert(CNT == SB * SB, "one thread per cell of a 16 x 16 block");
-constexpr int PTS = FB_SMALL + 2;   // row stride of the staged column panel stripe
+constexpr int PTS = FB_SMALL + 4;   // row stride of the staged column panel stripe (16-byte rows)
 
 // Dynamic shared memory of a launch that first applies the previous block
 // round's update (pre): the row panel tile k-interleaved and this stripe's
@@ -720,63 +720,45 @@ k_phase1c(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride
         const int op = o - FB;
         const size_t rg = off + (size_t)op * ld + o;             // tile (K-1, K)
         const size_t cg = off + (size_t)(o + c * SB) * ld + op;  // tile (K, K-1), stripe c
-        using V4 = typename E::V4;
-        for (int e = threadIdx.x; e < FB * FB / 4; e += CNT) {
-            const int k = e / (FB / 4), j = (e % (FB / 4)) * 4;
-            T xu[4], xl[4];
-            if (vec && j + 4 <= m) {
-                const V4 v = *reinterpret_cast<const V4*>(U + rg + (size_t)k * ld + j);
-                xu[0] = v.x; xu[1] = v.y; xu[2] = v.z; xu[3] = v.w;
-                if (HAS_L) {
-                    const V4 w = *reinterpret_cast<const V4*>(L + rg + (size_t)k * ld + j);
-                    xl[0] = w.x; xl[1] = w.y; xl[2] = w.z; xl[3] = w.w;
-                }
+        // every copy in flight at once: R element by element into its
+        // k-interleaved place, C in 16-byte pieces where rows allow
+        for (int e = threadIdx.x; e < FB * FB; e += CNT) {
+            const int k = e / FB, j = e % FB;
+            const int d = (k >> 1) * (2 * FB) + 2 * j + (k & 1);
+            if (j < m) {
+                cp_async4(RU + d, U + rg + (size_t)k * ld + j);
+                if (HAS_L) cp_async4(RL + d, L + rg + (size_t)k * ld + j);
             } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const bool in = j + q < m;
-                    xu[q] = in ? U[rg + (size_t)k * ld + j + q] : E::upad();
-                    xl[q] = HAS_L ? (in ? L[rg + (size_t)k * ld + j + q] : E::lpad()) : T(0);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int d = (k >> 1) * (2 * FB) + 2 * (j + q) + (k & 1);
-                RU[d] = xu[q];
-                if (HAS_L) RL[d] = xl[q];
+                RU[d] = E::upad();
+                if (HAS_L) RL[d] = E::lpad();
             }
         }
         for (int e = threadIdx.x; e < SB * FB / 4; e += CNT) {
             const int r = e / (FB / 4), k = (e % (FB / 4)) * 4;
-            T xu[4], xl[4];
+            T* cu = CU + r * PTS + k;
+            T* cl = CL + r * PTS + k;
             if (c * SB + r < m) {
+                const size_t g = cg + (size_t)r * ld + k;
                 if (vec) {
-                    const V4 v = *reinterpret_cast<const V4*>(U + cg + (size_t)r * ld + k);
-                    xu[0] = v.x; xu[1] = v.y; xu[2] = v.z; xu[3] = v.w;
-                    if (HAS_L) {
-                        const V4 w = *reinterpret_cast<const V4*>(L + cg + (size_t)r * ld + k);
-                        xl[0] = w.x; xl[1] = w.y; xl[2] = w.z; xl[3] = w.w;
-                    }
+                    cp_async16(cu, U + g);
+                    if (HAS_L) cp_async16(cl, L + g);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        xu[q] = U[cg + (size_t)r * ld + k + q];
-                        xl[q] = HAS_L ? L[cg + (size_t)r * ld + k + q] : T(0);
+                        cp_async4(cu + q, U + g + q);
+                        if (HAS_L) cp_async4(cl + q, L + g + q);
                     }
                 }
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    xu[q] = E::upad();
-                    xl[q] = E::lpad();
+                    cu[q] = E::upad();
+                    if (HAS_L) cl[q] = E::lpad();
                 }
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                CU[r * PTS + k + q] = xu[q];
-                if (HAS_L) CL[r * PTS + k + q] = xl[q];
-            }
         }
+        cp_async_commit();
+        cp_async_wait<0>();
         __syncthreads();
         p1c_product<T, HAS_L, FB, FB>(u, l, CU + i * PTS, CL + i * PTS, RU, RL, j0);
     }

@@ -56,11 +56,6 @@ struct P3Smem {
     static constexpr size_t BYTES = 2 * STAGE * sizeof(T);
 };
 
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-
 // Stage k-chunk `c` of both panels into shared memory stage `stage`.
 template <class T, bool HAS_L, int FB, int NT>
 __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_t ld, int oi,
