@@ -318,9 +318,10 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only run this many smoothing calls of the workload (no timing, "
                          "no JSON line): a short target for ncu captures")
-    ap.add_argument("--mode", choices=["blocked", "perk"], default="blocked",
+    ap.add_argument("--mode", choices=["blocked", "perk", "upper"], default="blocked",
                     help="perk: the per-round reference mode (HBM-bound), for its roofline "
-                         "and captures")
+                         "and captures; upper: bs_smooth_upper (U alone), with "
+                         "--profile-calls only (the sweep times it)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU-oracle sample length for cpu_baseline")
     ap.add_argument("--ref-rounds", type=int, default=48,
@@ -336,6 +337,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.mode == "upper" and args.profile_calls <= 0:
+        ap.error("--mode upper is a capture target: use it with --profile-calls")
 
     ws, rank, local = dist_setup()
     if args.impl == "reference":
@@ -370,7 +373,10 @@ def main():
         for _ in range(args.profile_calls):
             wU.copy_(dU0)
             wL.copy_(dL0)
-            bsm.bs_smooth_bounds(wU, wL, flags=flags)
+            if args.mode == "upper":
+                bsm.bs_smooth_upper(wU)
+            else:
+                bsm.bs_smooth_bounds(wU, wL, flags=flags)
         torch.cuda.synchronize()
         print("profile calls done: %d x %s, n=%d" % (args.profile_calls, args.mode, n))
         return 0

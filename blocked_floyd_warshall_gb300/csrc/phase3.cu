@@ -194,7 +194,7 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
 }
 
 template <class T, bool HAS_L, int FB, bool WIDE>
-__global__ void __launch_bounds__(P3S<FB, WIDE>::NT)
+__global__ void __launch_bounds__(P3S<FB, WIDE>::NT, (!HAS_L && FB == FB_LARGE) ? 2 : 0)
 k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K,
          int part, bool vec, bool sym) {
     using S = P3S<FB, WIDE>;
@@ -235,8 +235,7 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
         const T* BU = AU + SM::A_ELEMS;
         const T* AL = BU + SM::B_ELEMS;
         const T* BL = AL + SM::A_ELEMS;
-#pragma unroll 1
-        for (int kk = 0; kk < BK; kk += 2) {
+        auto step = [&](int kk) {
             P a[S::TM], al[S::TM], b[S::TN], bl[S::TN];
 #pragma unroll
             for (int r = 0; r < S::TM; ++r) {
@@ -271,6 +270,17 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
                     for (int q = 0; q < S::TN; ++q)
                         PairOps<T>::lower(l[r][q], a[r], al[r], b[q], bl[q]);
             }
+        };
+        if constexpr (HAS_L || FB == FB_SMALL) {
+#pragma unroll 1
+            for (int kk = 0; kk < BK; kk += 2) step(kk);
+        } else {
+            // Upper bounds alone on 128-wide tiles: the whole chunk unrolled
+            // (addresses become immediates; 128 registers, two CTAs per SM),
+            // 5 % faster at n = 16384.  With L the registers do not allow
+            // it, and the 64-wide forms measured slower unrolled.
+#pragma unroll
+            for (int kk = 0; kk < BK; kk += 2) step(kk);
         }
         __syncthreads();
     }
