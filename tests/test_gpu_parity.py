@@ -609,13 +609,15 @@ def test_symmetric_flag_checks():
                          flags=bsm.BS_SYMMETRIC | bsm.BS_VALIDATE)
 
 
-@pytest.mark.parametrize("sched", ["t64", "t128", "sym", "perk"])
-def test_cuda_graph_capture_and_replay(sched):
+@pytest.mark.parametrize("sched,n", [("t64", 300), ("t128", 300), ("sym", 300), ("perk", 300),
+                                     ("auto", 1000)])
+def test_cuda_graph_capture_and_replay(sched, n):
     """A smoothing captured into a CUDA graph (look-ahead fork and join
-    included) replays to the same result, twice, on fresh inputs."""
+    included) replays to the same result, twice, on fresh inputs.  n = 1000
+    has more rest tiles than SMs: captured, it takes the order in which the
+    rest of each round waits for the next block row and column."""
     t = torch()
     flags = bsm.BS_PERK if sched == "perk" else SCHEDULES[sched]
-    n = 300
     Uq, Lq = W.random_bounds(n, 9300, p_bad=0.02)
     U0, L0 = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
     Uo, Lo = oracle.smooth(W.to_f32(Uq), W.to_f32(Lq))
