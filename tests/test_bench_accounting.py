@@ -1,0 +1,73 @@
+"""Host-side accounting of bench.py (no GPU): the cell-update counts its
+roofline divides by, and its copies of the library's schedule rules."""
+import itertools
+
+import pytest
+
+import bench
+
+
+def brute_phase_cells(n, fb):
+    """Count (i, j, k) by phase straight from the blocked schedule's
+    definition: round K owns the middle atoms of block K; a cell in block row
+    and column K is phase 1, one in exactly one of them phase 2, the rest
+    phase 3."""
+    p = [0, 0, 0]
+    for k in range(n):
+        K = k // fb
+        for i, j in itertools.product(range(n), repeat=2):
+            inr, inc = i // fb == K, j // fb == K
+            p[0 if inr and inc else 1 if inr or inc else 2] += 1
+    return tuple(p)
+
+
+@pytest.mark.parametrize("n,fb", [(1, 64), (5, 4), (9, 4), (12, 4), (13, 8)])
+def test_phase_cells_match_the_definition(n, fb):
+    assert bench.phase_cells(n, fb) == brute_phase_cells(n, fb)
+    assert sum(bench.phase_cells(n, fb)) == n ** 3
+
+
+@pytest.mark.parametrize("n,fb", [(9, 4), (12, 4), (13, 8), (300, 64)])
+def test_next_and_diagonal_cells(n, fb):
+    """NEXT(K) covers the tiles of block row and column K+1 outside row and
+    column K; the diagonal tile (K+1, K+1) is one of them."""
+    nb = (n + fb - 1) // fb
+    sizes = [min(fb, n - K * fb) for K in range(nb)]
+    nxt = diag = 0
+    for K in range(nb - 1):
+        mk = sizes[K]
+        for I in range(nb):
+            for J in range(nb):
+                if I == K or J == K:
+                    continue
+                if I == K + 1 or J == K + 1:
+                    nxt += sizes[I] * sizes[J] * mk
+                if I == J == K + 1:
+                    diag += sizes[I] * sizes[J] * mk
+    assert bench.next_cells(n, fb) == nxt
+    assert bench.diag_cells(n, fb) == diag
+    assert diag <= nxt <= bench.phase_cells(n, fb)[2]
+
+
+def test_merged_lookahead_rule():
+    """The library's merged look-ahead: 64-wide tiles and fewer rest tiles
+    than half the SMs -- general n <= 640, symmetric n <= 832 on 152 SMs."""
+    sms = 152
+    assert bench.merged_lookahead(640, 64, 1, sms)
+    assert not bench.merged_lookahead(641, 64, 1, sms)
+    assert bench.merged_lookahead(832, 64, 1, sms, sym=True)
+    assert not bench.merged_lookahead(833, 64, 1, sms, sym=True)
+    assert not bench.merged_lookahead(128, 64, 1, sms)          # two block rounds: no look-ahead
+    assert not bench.merged_lookahead(256, 128, 1, sms)         # 128-wide tiles
+    assert bench.merged_lookahead(300, 64, 4, sms)              # 9 rest tiles x 4 molecules
+    assert not bench.merged_lookahead(257, 64, 12, sms)         # 9 x 12 = 108
+
+
+def test_tile_rule_matches_documented_thresholds():
+    """64-wide tiles unless a 128-wide phase 3 holds >= 3000 tiles over the
+    batch (768 for int32)."""
+    assert bench.tile_size(4096) == 64
+    assert bench.tile_size(16384) == 128
+    assert bench.tile_size(7040) == 64 and bench.tile_size(7041) == 128
+    assert bench.tile_size(4096, flags=1) == 128              # int32: 31^2 = 961 >= 768
+    assert bench.tile_size(512, batch=256) == 64               # 9 x 256 = 2304
