@@ -428,6 +428,29 @@ def test_batched_small_molecules(n, B, dtype, sched):
         assert same_bits(Ug[b], Uo) and same_bits(Lg[b], Lo)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_small_schedules_random_sizes(seed):
+    """Random sizes and batches across the small-matrix schedules (the
+    merged look-ahead below half an SM's worth of rest tiles, the tight one
+    up to an SM's worth, then the loose one), random dtype and symmetry,
+    every molecule against the oracle."""
+    rng = np.random.default_rng(7100 + seed)
+    n = int(rng.integers(130, 1000))
+    B = int(rng.integers(1, 4))
+    dtype = "f32" if rng.integers(2) else "i32"
+    flags = bsm.BS_SYMMETRIC if rng.integers(2) else 0
+    mols = [W.random_bounds(n, 7200 + 10 * seed + b, p_known=0.25, p_bad=0.01) for b in range(B)]
+    Uq = np.stack([m[0] for m in mols])
+    Lq = np.stack([m[1] for m in mols])
+    U0, L0 = (W.to_f32(Uq), W.to_f32(Lq)) if dtype == "f32" else (Uq, Lq)
+    U, L = dev(U0), dev(L0)
+    bsm.bs_smooth_bounds_batched(U, L, flags=flags)
+    Ug, Lg = host(U), host(L)
+    for b in range(B):
+        Uo, Lo = oracle.smooth(U0[b], L0[b])
+        assert same_bits(Ug[b], Uo) and same_bits(Lg[b], Lo), (n, B, dtype, flags, b)
+
+
 def test_batched_per_round_and_strided():
     """Per-round mode and a batch stride larger than one molecule."""
     B, n, ld = 5, 70, 72
