@@ -469,10 +469,10 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
 // 16 x 16 block each, group g the block in sub-block column g, thread t of a
 // group row t/4 and columns 4(t%4) .. +3 of it (the layout of step (a)
 // above).  Sub-block s (middle atoms 16s .. 16s+15):
-//   CTA s closes block (s,s) (group s, step (a)) and
-//   stores the closed block, and its row sub-panel as it stood before the
-//   sub-block, R0, into the shared memory of every CTA of the cluster
-//   (distributed shared memory); one cluster barrier;
+//   CTA s closes block (s,s) (group s, step (a)) and stores the closed
+//   block, and its row sub-panel as it stood before the sub-block, R0, into
+//   the shared memory of every CTA of the cluster (distributed shared
+//   memory); one cluster barrier;
 //   every other CTA takes the product of its cells in sub-block column s
 //   with the closed block (its column sub-panel C, as in phase 2), then the
 //   product of C with R0 for the rest of its stripe;
@@ -492,6 +492,8 @@ k_phase1(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
 // visible.  A first barrier at entry makes sure every CTA of the cluster is
 // running before any remote store; no CTA touches another's shared memory
 // after barrier 3, so none has to wait for the others before it exits.
+// With `pre` (the merged look-ahead of small matrices) each CTA first applies
+// the previous block round's product to its own stripe, before the closures.
 
 constexpr int CL = FB_SMALL / SB;   // CTAs per cluster: one per 16-row stripe
 constexpr int CNT = CL * AT;        // threads per CTA: one group per sub-block column
