@@ -36,8 +36,9 @@
 namespace bs {
 
 // Phase 1 computes the closure of tile (K,K) by the same blocked scheme one
-// level down, on the tile held in shared memory: for each SB-wide sub-block s
-// of its middle atoms,
+// level down.  On one CTA (k_phase1, 128-wide tiles; 64-wide tiles take the
+// cluster form further below), on the tile held in shared memory: for each
+// SB-wide sub-block s of its middle atoms,
 //   (a) two warps close sub-block (s,s), k serially, exchanging row and
 //       column k through shared memory with a two-warp barrier per middle
 //       atom; for s > 0 this runs during (c) of s-1, on the two warps (c)
@@ -54,10 +55,10 @@ namespace bs {
 constexpr int SB = 16;          // sub-block width
 constexpr int HALVES = SB / 8;     // (b): 8-cell units per sub-panel line
 
-// (c) micro-tile: 4 x 4 cells on 64-wide tiles (256 threads), 8 x 4 on 128-wide
-// tiles (512 threads).  In both, warp w covers tile rows 8w .. 8w+7 and thread
-// tx columns 4tx .. 4tx+3, so a sub-block row is whole warps and a sub-block
-// column whole quads.
+// (c) micro-tile: 8 x 4 cells on 128-wide tiles (512 threads; the shape
+// gives 4 x 4 and 256 threads for a 64-wide tile).  Warp w covers tile rows
+// 8w .. 8w+7 and thread tx columns 4tx .. 4tx+3, so a sub-block row is whole
+// warps and a sub-block column whole quads.
 template <int FB> using P1S = Shape<FB, (FB == FB_SMALL ? 4 : 8), 4>;
 
 template <class T, bool HAS_L, int FB>
@@ -845,8 +846,6 @@ static cudaError_t setup1() {
     };
     set(k_phase1<T, true, FB_LARGE>, P1Smem<T, true, FB_LARGE>::BYTES);
     set(k_phase1<T, false, FB_LARGE>, P1Smem<T, false, FB_LARGE>::BYTES);
-    set(k_phase1<T, true, FB_SMALL>, P1Smem<T, true, FB_SMALL>::BYTES);
-    set(k_phase1<T, false, FB_SMALL>, P1Smem<T, false, FB_SMALL>::BYTES);
     set(k_phase1c<T, true>, p1c_pre_bytes<true>());
     set(k_phase1c<T, false>, p1c_pre_bytes<false>());
     return e;
