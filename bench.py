@@ -53,15 +53,15 @@ def make_workload(name):
     return globule_bounds(wl["box"], wl["seed"], wl["p_long"])
 
 
-def tile_size(n, flags=0, batch=1):
+def tile_size(n, flags=0, batch=1, upper=False):
     """Tile size the library picks (mirrors its rule; forced by the tile bits;
-    flags bit 0 set: int32)."""
+    flags bit 0 set: int32; upper: bs_smooth_upper, U alone)."""
     if flags & (1 << 5):
         return 64
     if flags & (1 << 6):
         return 128
     nb = (n + 127) // 128
-    return 128 if (nb - 1) ** 2 * batch >= (768 if flags & 1 else 3000) else 64
+    return 128 if (nb - 1) ** 2 * batch >= (768 if flags & 1 or upper else 3000) else 64
 
 
 def phase_cells(n, fb, sym=False):
