@@ -98,6 +98,21 @@ def test_symmetric_upper_only(n, algo):
     assert ok and same_bits(Ug, Uo)
 
 
+@pytest.mark.parametrize("n", [997, 1001, 1003])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+@pytest.mark.parametrize("sched", ["auto", "sym", "t128"])
+def test_blocked_tails_near_1000(n, dtype, sched):
+    """Sizes around the n = 1000 chain with ragged last tiles (37, 41, 43 rows
+    of 64; 101, 105, 107 of 128), a padded leading dimension n + 5 with
+    canaries, every cell against the oracle."""
+    Uq, Lq = W.random_bounds(n, 6100 + n, p_known=0.05, p_bad=0.005)
+    U0, L0 = as_dtype(Uq, Lq, dtype)
+    Uo, Lo = oracle.smooth(U0, L0)
+    Ug, Lg, ok = gpu_bounds(U0, L0, SCHEDULES[sched], ld=n + 5)
+    assert ok
+    assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
+
+
 @pytest.mark.parametrize("n", [129, 300])
 @pytest.mark.parametrize("sched", ["t64", "t128"])
 def test_blocked_asymmetric(n, sched):
