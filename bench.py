@@ -84,6 +84,14 @@ def phase_cells(n, fb, sym=False):
     return p1, p2, p3
 
 
+def perk_bytes(n):
+    """DRAM bytes the per-round mode must move per smoothing: U and L read
+    and written once per pass over the matrix, a pass taking two rounds
+    (and a lone last round when n is odd)."""
+    passes = (n + 1) // 2
+    return 16.0 * float(n) ** 2 * passes
+
+
 def diag_cells(n, fb):
     """Cell updates of tile (K+1, K+1) in block rounds K < nb - 1: with the
     merged look-ahead of small matrices phase 1 of round K+1 applies them,
@@ -501,15 +509,17 @@ def main():
                               "event time of the call (launch, counter reset, 8-byte readback)"},
     }
     if args.mode == "perk":
-        # per-round mode: every round reads and writes all of U and L, 16 bytes
-        # per cell update, HBM-bound; its kernels are timed as the "round" phase
-        r_gbs = 16.0 * float(n) ** 3 / (total_ms / args.steps * 1e-3) / 1e9
+        # per-round mode, two rounds per pass: every pass reads and writes all
+        # of U and L, 8 bytes per cell update, HBM-bound; its kernels are timed
+        # as the "round" phase
+        r_gbs = perk_bytes(n) / (total_ms / args.steps * 1e-3) / 1e9
         line["roofline"] = {
-            "kernel": "k_round + k_cross (per-round mode)", "bound": "hbm",
+            "kernel": "k_round2 + k_cross2 (per-round mode)", "bound": "hbm",
             "achieved": r_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": r_gbs / peaks["hbm_gbs"], "traffic": None,
-            "achieved_basis": "16 bytes (read + write of U and L) x n^3 cell updates / step "
-                              "time (the step is these launches only)",
+            "achieved_basis": "16 bytes (read + write of U and L) x n^2 cells per pass of two "
+                              "rounds (a lone last round for n odd) / step time (the step is "
+                              "these launches only)",
             "peak_basis": "STREAM-style copy (%s)" % peaks["source"],
             "launches_per_step": launches / args.steps,
         }
@@ -637,7 +647,7 @@ def sweep(args):
                 # U alone: an add and a min per cell update
                 line["fp32_alu_frac_upper"] = rate * 2 / alu
             if algo == "perk":
-                gbs = rate * 16 / 1e9
+                gbs = perk_bytes(n) * batch / (ms * 1e-3) / 1e9
                 line["hbm_gbs_algorithmic"] = gbs
                 line["hbm_frac"] = gbs / peaks["hbm_gbs"]
             print(json.dumps(line), flush=True)

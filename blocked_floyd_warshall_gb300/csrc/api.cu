@@ -323,10 +323,17 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
     }
     cudaError_t e = cudaSuccess;
     if (perk) {
-        // each round's launch also applies the row/column k update of the round
-        // before it (perk.cu); the last round's has its own launch
-        for (int k = 0; k < n && e == cudaSuccess; ++k) e = bs::launch_round(is_int, m, k, literal, s);
-        if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, n - 1, s);
+        // two rounds per pass (perk.cu), each pass followed by its rows and
+        // columns; with n odd the last round alone, which also applies the
+        // row/column update of the round before it (already in place: no
+        // change) and is followed by its own
+        int k = 0;
+        for (; k + 1 < n && e == cudaSuccess; k += 2)
+            e = bs::launch_round2(is_int, m, k, literal, s);
+        if (e == cudaSuccess && k < n) {
+            e = bs::launch_round(is_int, m, k, literal, s);
+            if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
+        }
     } else {
         e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0, d);
     }

@@ -39,6 +39,8 @@ void note_launch();
 // Per-round (reference) mode, round k.
 cudaError_t launch_round(bool is_int, const Mats& m, int k, bool literal, cudaStream_t s);
 cudaError_t launch_cross(bool is_int, const Mats& m, int k, cudaStream_t s);
+// Rounds k and k+1 in one pass, then their rows and columns (two launches).
+cudaError_t launch_round2(bool is_int, const Mats& m, int k, bool literal, cudaStream_t s);
 
 // Blocked mode, block round K.
 cudaError_t blocked_setup(bool is_int);   // once per device: shared-memory limits
