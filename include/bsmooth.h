@@ -87,7 +87,9 @@ enum {
     BS_INT32_Q10 = 1,         /* element type: int32, 1/1024 Angstrom */
     BS_DTYPE_MASK = 3,
     BS_BLOCKED = 0,           /* three-phase blocked Floyd-Warshall (default) */
-    BS_PERK = 1 << 2,         /* one round per middle atom k, round-synchronous */
+    BS_PERK = 1 << 2,         /* round by round over the middle atoms k,
+                                 round-synchronous (two rounds per pass over
+                                 the matrix, each exactly as alone) */
     BS_RULE_CLOSURE = 0,      /* default lower-bound rule (see above) */
     BS_RULE_LITERAL = 1 << 3, /* printed rule; BS_PERK only, else BS_ERR_ARG */
     BS_VALIDATE = 1 << 4,     /* check the preconditions first (synchronises) */
