@@ -1,0 +1,156 @@
+"""CPU checks of the identities the GPU schedules rest on (no GPU, no CUDA
+code): plain Python on small integer and on-grid fp32 matrices, compared
+with the oracle.
+
+1. Two rounds per pass (per-round mode).  Round k+1's operands -- row k+1,
+   column k+1 and cell (k+1,k+1) after round k -- formed by each cell from
+   values before round k, then both rounds on the cell, give exactly the two
+   oracle rounds; rows and columns k, k+1 themselves follow the same
+   expressions with the four corner cells as they were before the pass.
+2. The pre-update row sub-panel (phase 1 on a cluster).  With D the closure
+   of a diagonal block, C = C0 + C0 D its column sub-panel and R = R0 + D R0
+   its row sub-panel (min-plus sums and products of the doubled bound
+   graph), the update of the rest, C R, equals C R0.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from workloads import molecules as W
+
+
+# ---------------------------------------------------------------- one round
+
+def one_round(u, l, uik, lik, ukj, lkj, lkk, closure, T):
+    """Round k on cell (i,j) (GPU Gems 2 ch. 43, section 2's rules, upper
+    first; the lower column raised by the closure rule or taken as printed)."""
+    lc = max(lik, T(lkk - uik)) if closure else lik
+    return min(u, T(uik + ukj)), max(l, max(T(lkj - uik), T(lc - ukj)))
+
+
+def two_rounds(u, l, row_i, col_j, corners, closure, T):
+    """Rounds k and k+1 on cell (i,j) from values before round k.
+    row_i: U, L at (i,k), (i,k+1); col_j: U, L at (k,j), (k+1,j);
+    corners: U, L at (k,k), (k,k+1), (k+1,k), (k+1,k+1)."""
+    (uik, lik, uik1, lik1), (ukj, lkj, uk1j, lk1j) = row_i, col_j
+    (_, lkk), (ukk1, lkk1), (uk1k, lk1k), (uk1k1, lk1k1) = corners
+    u, l = one_round(u, l, uik, lik, ukj, lkj, lkk, closure, T)
+    uik1, lik1 = one_round(uik1, lik1, uik, lik, ukk1, lkk1, lkk, closure, T)
+    uk1j, lk1j = one_round(uk1j, lk1j, uk1k, lk1k, ukj, lkj, lkk, closure, T)
+    _, l11 = one_round(uk1k1, lk1k1, uk1k, lk1k, ukk1, lkk1, lkk, closure, T)
+    return one_round(u, l, uik1, lik1, uk1j, lk1j, l11, closure, T)
+
+
+def smooth_two_per_pass(U, L, closure, step=None):
+    """Every pair of rounds as one pass, every value from before the pass
+    (`step`: the two-round cell update, two_rounds unless a test plants a
+    mistake)."""
+    step = step or two_rounds
+    U, L = U.copy(), L.copy()
+    T = U.dtype.type
+    n = U.shape[0]
+    k = 0
+    while k + 1 < n:
+        k1 = k + 1
+        U0, L0 = U.copy(), L.copy()
+        corners = [(U0[a, b], L0[a, b]) for a, b in ((k, k), (k, k1), (k1, k), (k1, k1))]
+        for i in range(n):
+            for j in range(n):
+                row_i = (U0[i, k], L0[i, k], U0[i, k1], L0[i, k1])
+                col_j = (U0[k, j], L0[k, j], U0[k1, j], L0[k1, j])
+                U[i, j], L[i, j] = step(U0[i, j], L0[i, j], row_i, col_j, corners, closure, T)
+        k += 2
+    if k < n:
+        U0, L0 = U.copy(), L.copy()
+        for i in range(n):
+            for j in range(n):
+                U[i, j], L[i, j] = one_round(U0[i, j], L0[i, j], U0[i, k], L0[i, k], U0[k, j],
+                                             L0[k, j], L0[k, k], closure, T)
+    return U, L
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 6, 9, 14])
+@pytest.mark.parametrize("dtype", ["i32", "f32"])
+@pytest.mark.parametrize("closure", [True, False])
+def test_two_rounds_per_pass_equal_two_rounds(n, dtype, closure):
+    Uq, Lq = W.random_bounds(n, 4400 + n, p_known=0.3, p_bad=0.05)
+    U0, L0 = (W.to_f32(Uq), W.to_f32(Lq)) if dtype == "f32" else (Uq, Lq)
+    Uo, Lo = oracle.smooth(U0, L0, rule=oracle.RULE_CLOSURE if closure else oracle.RULE_LITERAL)
+    Ug, Lg = smooth_two_per_pass(U0, L0, closure)
+    assert np.array_equal(Ug.view(np.int32), Uo.view(np.int32))
+    assert np.array_equal(Lg.view(np.int32), Lo.view(np.int32))
+
+
+def test_two_rounds_per_pass_catches_a_wrong_operand():
+    """Planted mistake: round k+1 taking row k+1 from before round k."""
+    n = 9
+    Uq, Lq = W.random_bounds(n, 4499, p_known=0.5, p_bad=0.05)
+    Uo, Lo = oracle.smooth(Uq, Lq)
+
+    def wrong(u, l, row_i, col_j, corners, closure, T):
+        (uik, lik, uik1, lik1), (ukj, lkj, uk1j, lk1j) = row_i, col_j
+        (_, lkk), (ukk1, lkk1), (uk1k, lk1k), (uk1k1, lk1k1) = corners
+        u, l = one_round(u, l, uik, lik, ukj, lkj, lkk, closure, T)
+        uik1, lik1 = one_round(uik1, lik1, uik, lik, ukk1, lkk1, lkk, closure, T)
+        _, l11 = one_round(uk1k1, lk1k1, uk1k, lk1k, ukk1, lkk1, lkk, closure, T)
+        return one_round(u, l, uik1, lik1, uk1j, lk1j, l11, closure, T)
+
+    Ug, Lg = smooth_two_per_pass(Uq, Lq, True, step=wrong)
+    assert not (np.array_equal(Ug, Uo) and np.array_equal(Lg, Lo))
+
+
+# ---------------------------------------------------------------- doubled-graph products
+
+def product(A, B):
+    """A (x) B in the doubled bound graph: the phase-3 rules with A the column
+    operand and B the row operand; pairs (U, L) of integer arrays."""
+    AU, AL = A
+    BU, BL = B
+    U = (AU[:, :, None] + BU[None, :, :]).min(axis=1)
+    L = np.maximum((BL[None, :, :] - AU[:, :, None]).max(axis=1),
+                   (AL[:, :, None] - BU[None, :, :]).max(axis=1))
+    return U, L
+
+
+def plus(X, Y):
+    return np.minimum(X[0], Y[0]), np.maximum(X[1], Y[1])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_pre_update_row_panel_gives_the_same_product(seed):
+    rng = np.random.default_rng(4500 + seed)
+    s, r, c = 6, 9, 7          # block width, column sub-panel rows, row sub-panel columns
+    Uq, Lq = W.random_bounds(s, 4600 + seed, p_known=0.4, p_bad=0.05)
+    D = tuple(a.astype(np.int64) for a in oracle.smooth(Uq, Lq))          # closed block
+    big = 1 << 28
+    C0 = (rng.integers(0, big, (r, s)), rng.integers(0, big // 4, (r, s)))
+    R0 = (rng.integers(0, big, (s, c)), rng.integers(0, big // 4, (s, c)))
+    C = plus(C0, product(C0, D))
+    R = plus(R0, product(D, R0))
+    X = (rng.integers(0, big, (r, c)), rng.integers(0, big // 4, (r, c)))
+    full = plus(X, product(C, R))
+    short = plus(X, product(C, R0))
+    assert np.array_equal(full[0], short[0]) and np.array_equal(full[1], short[1])
+
+
+def test_pre_update_identity_needs_the_closure():
+    """With an unclosed block in place of D the two products differ for some
+    input: the identity is not vacuous."""
+    differs = False
+    for seed in range(20):
+        rng = np.random.default_rng(4700 + seed)
+        s, r, c = 6, 9, 7
+        Uq, Lq = W.random_bounds(s, 4800 + seed, p_known=0.4, p_bad=0.05)
+        D = (Uq.astype(np.int64), Lq.astype(np.int64))                        # not closed
+        big = 1 << 28
+        C0 = (rng.integers(0, big, (r, s)), rng.integers(0, big // 4, (r, s)))
+        R0 = (rng.integers(0, big, (s, c)), rng.integers(0, big // 4, (s, c)))
+        C = plus(C0, product(C0, D))
+        R = plus(R0, product(D, R0))
+        X = (rng.integers(0, big, (r, c)), rng.integers(0, big // 4, (r, c)))
+        full = plus(X, product(C, R))
+        short = plus(X, product(C, R0))
+        if not (np.array_equal(full[0], short[0]) and np.array_equal(full[1], short[1])):
+            differs = True
+            break
+    assert differs
