@@ -73,3 +73,11 @@ def test_tile_rule_matches_documented_thresholds():
     assert bench.tile_size(512, batch=256) == 64               # 9 x 256 = 2304
     assert bench.tile_size(4096, upper=True) == 128            # U alone: 961 >= 768
     assert bench.tile_size(3000, upper=True) == 64             # 23^2 = 529
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4096, 4097])
+def test_per_round_bytes(n):
+    """Per-round mode: one read and one write of U and L per pass, a pass
+    taking two rounds and a lone last round for n odd."""
+    passes = n // 2 + n % 2
+    assert bench.perk_bytes(n) == 16 * n * n * passes
