@@ -46,7 +46,7 @@ BS_TILE_64 = 1 << 5
 BS_TILE_128 = 1 << 6
 BS_NO_LOOKAHEAD = 1 << 7
 BS_SYMMETRIC = 1 << 8
-BS_FORCE_LOOKAHEAD = 1 << 9
+BS_PERK_PAIRED = 1 << 10
 
 PHASES = ("round", "phase1", "phase2", "phase3", "phase3_next")
 

@@ -259,10 +259,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
                      long long bstride, int batch, int mode, bs::Mats* m) {
     const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE | BS_TILE_64 |
-                      BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC | BS_FORCE_LOOKAHEAD;
+                      BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC | BS_PERK_PAIRED;
     if (mode & ~known) return BS_ERR_ARG;
     if ((mode & BS_TILE_64) && (mode & BS_TILE_128)) return BS_ERR_ARG;
-    if ((mode & BS_NO_LOOKAHEAD) && (mode & BS_FORCE_LOOKAHEAD)) return BS_ERR_ARG;
+    if ((mode & BS_PERK_PAIRED) && !(mode & BS_PERK)) return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
     if (n < 0 || batch < 0) return BS_ERR_ARG;
     if (n > 0 && ld < n) return BS_ERR_ARG;
@@ -323,14 +323,14 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
     }
     cudaError_t e = cudaSuccess;
     if (perk) {
-        // two rounds per pass (perk.cu), each pass followed by its rows and
-        // columns; with n odd the last round alone, which also applies the
-        // row/column update of the round before it (already in place: no
-        // change) and is followed by its own
+        // plain: every round alone, then its row and column (perk.cu);
+        // paired: two rounds per pass, each pass followed by its rows and
+        // columns, and with n odd the last round in the plain form
         int k = 0;
-        for (; k + 1 < n && e == cudaSuccess; k += 2)
-            e = bs::launch_round2(is_int, m, k, literal, s);
-        if (e == cudaSuccess && k < n) {
+        if (mode & BS_PERK_PAIRED)
+            for (; k + 1 < n && e == cudaSuccess; k += 2)
+                e = bs::launch_round2(is_int, m, k, literal, s);
+        for (; k < n && e == cudaSuccess; ++k) {
             e = bs::launch_round(is_int, m, k, literal, s);
             if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
         }

@@ -1,28 +1,22 @@
 // Per-round mode (GPU Gems 2 ch. 43, section 3, "Floyd-Warshall rounds";
 // section 5 computes each round from a copy of the matrix taken at its
-// start).  The call takes the rounds two at a time (k_round2 + k_cross2
-// below: one pass over the matrix per two rounds); with n odd the last round
-// runs alone (k_round + k_cross).
+// start).  Two forms:
+//   BS_PERK              one round per pass: k_round, then k_cross, for every
+//                        round k -- the plain round-synchronous reference;
+//   BS_PERK | PAIRED     two rounds per pass (k_round2 + k_cross2 below), with
+//                        n odd the last round in the plain form.
 //
 // Round k reads only row k and column k.  Round-synchronous semantics without
 // a second matrix: k_round updates every cell OUTSIDE row k and column k, so
 // nothing it reads changes during the launch (the 16-byte store that covers
-// column k writes that lane back unchanged).  Row k and column k then take
-// round k's update, whose new values depend only on themselves, L[k,k] and U
-// (all unchanged by round k: U[i,k] + U[k,k] = U[i,k] because U[k,k] = 0):
+// column k writes that lane back unchanged).  k_cross then gives row k and
+// column k round k's update, whose new values depend only on themselves,
+// L[k,k] and U (all unchanged by round k: U[i,k] + U[k,k] = U[i,k] because
+// U[k,k] = 0 and U >= 0):
 //   cell (i,k): L[i,k] <- max(L[i,k], L[k,k] - U[i,k])
 //   cell (k,j): L[k,j] <- max(L[k,j], L[k,k] - U[k,j])
 // Both rules give these same row/column updates.  The upper bound of row and
-// column k never changes in round k, so the upper-only mode needs none.
-//
-// That row/column update of round k is applied by the next launch, k_round
-// of round k+1, as it loads those cells (the cell's own U, still the value
-// round k left, and L[k,k], which round k+1 does not change); where round k+1
-// reads one of them as an operand -- cell (k+1,k) of its row, cell (k,k+1) of
-// its column -- it applies the update to the value it reads and one thread
-// stores it.  Only the last round's needs its own launch (k_cross).  A
-// second application changes nothing (max is idempotent), so concurrent
-// readers of a cell being stored see an equivalent value.
+// column k never changes in round k, so the upper-only mode needs no k_cross.
 //
 // HBM-bound: each cell is read and written once per pass (U and L: 16 bytes
 // per fp32 cell update for k_round, 8 for k_round2).
@@ -43,11 +37,7 @@ k_round(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
     const int j = jq * 4;
     if (j >= n) return;
     const T* Uk = U + (size_t)k * ld;
-    T* Lk = HAS_L ? L + (size_t)k * ld : nullptr;
-    // the row/column update of round kp = k-1, still to apply (see above)
-    const int kp = k - 1;
-    const bool cross = HAS_L && kp >= 0;
-    const T lpp = cross ? L[(size_t)kp * ld + kp] : T(0);
+    const T* Lk = HAS_L ? L + (size_t)k * ld : nullptr;
 
     // row k: the same four values serve every row i
     T ukj[4], lkj[4];
@@ -66,15 +56,6 @@ k_round(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
             if (HAS_L) lkj[q] = j + q < n ? Lk[j + q] : E::lpad();
         }
     }
-    if (cross) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (j + q != kp) continue;
-            // cell (k, kp): column kp's pending update
-            lkj[q] = E::mx(lkj[q], E::sub(lpp, ukj[q]));
-            if (blockIdx.y == 0) Lk[kp] = lkj[q];
-        }
-    }
     const T lkk = HAS_L ? Lk[k] : T(0);
 
     for (int i = blockIdx.y; i < n; i += gridDim.y) {
@@ -85,13 +66,6 @@ k_round(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
         T lc = T(0);
         if (HAS_L) {
             lc = Li[k];
-            if (cross && i == kp) {
-                // cell (kp, k): row kp's pending update; stored before the
-                // loads below, so the thread whose quad holds column k writes
-                // the new value back with its quad
-                lc = E::mx(lc, E::sub(lpp, uik));
-                if (j <= k && k < j + 4) Li[k] = lc;
-            }
             if (!LITERAL) lc = E::mx(lc, E::sub(lkk, uik));
         }
         T u[4], l[4];
@@ -111,10 +85,7 @@ k_round(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            if (j + q == k) continue;   // column k: next launch
-            // row kp / column kp: round kp's pending update, from the U that
-            // round kp left, before this round changes it
-            if (cross && (i == kp || j + q == kp)) l[q] = E::mx(l[q], E::sub(lpp, u[q]));
+            if (j + q == k) continue;   // column k: k_cross
             u[q] = E::mn(u[q], E::add(uik, ukj[q]));
             if (HAS_L) l[q] = E::mx(l[q], E::mx(E::sub(lkj[q], uik), E::sub(lc, ukj[q])));
         }

@@ -88,8 +88,8 @@ enum {
     BS_DTYPE_MASK = 3,
     BS_BLOCKED = 0,           /* three-phase blocked Floyd-Warshall (default) */
     BS_PERK = 1 << 2,         /* round by round over the middle atoms k,
-                                 round-synchronous (two rounds per pass over
-                                 the matrix, each exactly as alone) */
+                                 round-synchronous: one pass over the matrix
+                                 per round (the plain reference mode) */
     BS_RULE_CLOSURE = 0,      /* default lower-bound rule (see above) */
     BS_RULE_LITERAL = 1 << 3, /* printed rule; BS_PERK only, else BS_ERR_ARG */
     BS_VALIDATE = 1 << 4,     /* check the preconditions first (synchronises) */
@@ -101,11 +101,10 @@ enum {
     BS_TILE_128 = 1 << 6,     /* force 128 x 128 tiles; both tile bits: BS_ERR_ARG */
     BS_NO_LOOKAHEAD = 1 << 7, /* run the three phases of each block round in
                                  sequence on `stream` only (see below) */
-    BS_FORCE_LOOKAHEAD = 1 << 9, /* use the look-ahead schedule; it is the
-                                    default whenever the matrix has three or more
-                                    block rows, so this bit changes nothing and is
-                                    kept for callers that set it; with
-                                    BS_NO_LOOKAHEAD: BS_ERR_ARG */
+    /* 1 << 9 is not used (any unknown bit: BS_ERR_ARG) */
+    BS_PERK_PAIRED = 1 << 10, /* with BS_PERK: two rounds per pass over the
+                                 matrix (half the memory traffic), each round
+                                 exactly as alone; without BS_PERK: BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the
                                  diagonal are computed, each mirrored into its
@@ -163,8 +162,10 @@ const char *bs_strerror(bs_status status);
  * accepted.  Synchronises `stream`.
  *
  * The first call on each device looks up the device address of the array
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture on the device.  Every call clears the counters it
+ * (cudaGetSymbolAddress, with that device current) and keeps it for the life
+ * of the process; make that first call before any stream capture on the
+ * device.  cudaDeviceReset unloads the array with the device's context, so do
+ * not call this entry point on a device after resetting it.  Every call clears the counters it
  * uses, but all calls share one array: calls whose GPU work can overlap
  * (different streams or host threads) race and must be serialised by the
  * caller. */

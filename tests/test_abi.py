@@ -87,7 +87,8 @@ def no_gpu():
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_RULE_LITERAL), bsm.BS_ERR_ARG),     # literal needs per-round
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_TILE_64 | bsm.BS_TILE_128), bsm.BS_ERR_ARG),
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_PERK | bsm.BS_SYMMETRIC), bsm.BS_ERR_ARG),
-    ((FAKE, FAKE2, 8, 8, None, bsm.BS_NO_LOOKAHEAD | bsm.BS_FORCE_LOOKAHEAD), bsm.BS_ERR_ARG),
+    ((FAKE, FAKE2, 8, 8, None, 1 << 9), bsm.BS_ERR_ARG),                  # retired bit
+    ((FAKE, FAKE2, 8, 8, None, bsm.BS_PERK_PAIRED), bsm.BS_ERR_ARG),      # paired needs per-round
     ((None, FAKE2, 8, 8, None, 0), bsm.BS_ERR_ARG),                       # null U
     ((FAKE, None, 8, 8, None, 0), bsm.BS_ERR_ARG),                        # null L
     ((FAKE, FAKE, 8, 8, None, 0), bsm.BS_ERR_ARG),                        # U aliases L

@@ -42,21 +42,28 @@ SIZES_BLOCKED = [1, 2, 3, 5, 16, 31, 48, 63, 64, 65, 96, 127, 128, 129, 255, 256
 # blocked-mode schedules: automatic, forced tile sizes, with and without look-ahead
 SCHEDULES = {
     "auto": 0,
-    "t64": bsm.BS_TILE_64 | bsm.BS_FORCE_LOOKAHEAD,
-    "t128": bsm.BS_TILE_128 | bsm.BS_FORCE_LOOKAHEAD,
+    "t64": bsm.BS_TILE_64,
+    "t128": bsm.BS_TILE_128,
     "t64_serial": bsm.BS_TILE_64 | bsm.BS_NO_LOOKAHEAD,
     "t128_serial": bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD,
     "sym": bsm.BS_SYMMETRIC,
 }
+# every algorithm: the blocked schedules and both per-round forms
+ALGOS = dict(SCHEDULES, perk=bsm.BS_PERK, perk2=bsm.BS_PERK | bsm.BS_PERK_PAIRED)
 
 
 @pytest.mark.parametrize("n", SIZES_PERK)
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
 @pytest.mark.parametrize("rule", ["closure", "literal"])
-def test_per_round_matches_oracle(n, dtype, rule):
+@pytest.mark.parametrize("form", ["plain", "paired"])
+def test_per_round_matches_oracle(n, dtype, rule, form):
+    """Both per-round forms: one round per pass (the plain reference mode) and
+    two rounds per pass."""
     Uq, Lq = W.random_bounds(n, 1000 + n, p_known=0.3, p_bad=0.03)
     U0, L0 = as_dtype(Uq, Lq, dtype)
     flags = bsm.BS_PERK | (bsm.BS_RULE_LITERAL if rule == "literal" else 0)
+    if form == "paired":
+        flags |= bsm.BS_PERK_PAIRED
     r = oracle.RULE_LITERAL if rule == "literal" else oracle.RULE_CLOSURE
     Uo, Lo = oracle.smooth(U0, L0, rule=r)
     Ug, Lg, ok = gpu_bounds(U0, L0, flags)
@@ -124,13 +131,13 @@ def test_blocked_asymmetric(n, sched):
 
 @pytest.mark.parametrize("n,ld,offset", [(130, 140, 0), (130, 133, 0), (257, 260, 1),
                                          (97, 101, 3), (200, 200, 1)])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
 def test_leading_dimension_and_misalignment(n, ld, offset, algo):
     """ld > n keeps the padding untouched; ld % 4 != 0 or a base not 16-byte
     aligned takes the scalar-IO instantiation with identical results."""
     Uq, Lq = W.random_bounds(n, 4000 + n, p_bad=0.02)
     U0, L0 = W.to_f32(Uq), W.to_f32(Lq)
-    flags = bsm.BS_PERK if algo == "perk" else SCHEDULES[algo]
+    flags = ALGOS[algo]
     Uo, Lo = oracle.smooth(U0, L0)
     Ug, Lg, ok = gpu_bounds(U0, L0, flags, ld=ld, offset=offset)
     assert ok
@@ -139,12 +146,12 @@ def test_leading_dimension_and_misalignment(n, ld, offset, algo):
 
 @pytest.mark.parametrize("n", [1, 5, 128, 129, 300])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
 def test_upper_only(n, dtype, algo):
     Uq, _ = W.random_bounds(n, 5000 + n, p_known=0.25)
     U0 = W.to_f32(Uq) if dtype == "f32" else Uq
     Uo = oracle.smooth_upper(U0)
-    Ug, ok = gpu_upper(U0, bsm.BS_PERK if algo == "perk" else SCHEDULES[algo], ld=n + 3)
+    Ug, ok = gpu_upper(U0, ALGOS[algo], ld=n + 3)
     assert ok and same_bits(Ug, Uo)
 
 
@@ -232,7 +239,7 @@ def gamma(m):
 
 @pytest.mark.parametrize("n,p_bad,seed", [(300, 0.0, 1), (300, 0.02, 2), (700, 0.01, 3),
                                           (517, 0.005, 4)])
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "sym", "perk"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "sym", "perk", "perk2"])
 def test_fp32_off_grid_per_cell_bound(n, p_bad, seed, sched):
     """Off the 1/1024 grid, every fp32 cell against the fp64 oracle, with a
     bound from the cell's own path (oracle provenance: edges h and summed
@@ -245,7 +252,7 @@ def test_fp32_off_grid_per_cell_bound(n, p_bad, seed, sched):
     covers the oracle's own fp64 rounding."""
     U0, L0 = off_grid(n, 8000 + seed, p_bad)
     U64, L64, HU, HL, ML = oracle.smooth_track(U0.astype(np.float64), L0.astype(np.float64))
-    flags = bsm.BS_PERK if sched == "perk" else SCHEDULES[sched]
+    flags = ALGOS[sched]
     Ug, Lg, ok = gpu_bounds(U0, L0, flags)
     assert ok
     Ug, Lg = Ug.astype(np.float64), Lg.astype(np.float64)
@@ -295,10 +302,10 @@ def edge_cases():
 
 
 @pytest.mark.parametrize("case", sorted(edge_cases()))
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
 def test_edge_cases(case, algo):
     Uq, Lq = edge_cases()[case]
-    flags = bsm.BS_PERK if algo == "perk" else SCHEDULES[algo]
+    flags = ALGOS[algo]
     for U0, L0 in ((Uq, Lq), (W.to_f32(Uq), W.to_f32(Lq))):
         if case == "int32_ceiling" and U0.dtype == np.float32:
             continue                      # above 2^24 units the fp32 grid is not exact
@@ -309,7 +316,7 @@ def test_edge_cases(case, algo):
         np.testing.assert_array_equal(Uo, Uq.astype(Uo.dtype) / (1 if Uo.dtype == np.int32 else 1024))
 
 
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
 def test_infinite_upper_bounds(algo):
     """fp32 U may be +inf for unknown pairs; inf + x = inf never wins."""
     Uq, Lq = W.random_bounds(200, 9500, p_known=0.1, p_bad=0.01)
@@ -325,7 +332,7 @@ def test_infinite_upper_bounds(algo):
     U0 = np.where(Uq == W.sentinel_q(200), np.float32(np.inf), U0).astype(np.float32)
     Uo, Lo = oracle.smooth(U0, L0)
     assert np.isinf(Uo).any()
-    Ug, Lg, ok = gpu_bounds(U0, L0, bsm.BS_PERK if algo == "perk" else SCHEDULES[algo])
+    Ug, Lg, ok = gpu_bounds(U0, L0, ALGOS[algo])
     assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
 
 
@@ -396,7 +403,7 @@ def test_globule_4096_fp32_blocked_and_per_round(globule4096):
     m, Uo, Lo = globule4096
     U0, L0 = W.to_f32(m["U"]), W.to_f32(m["L"])
     expect_flags = oracle.count_infeasible(Uo, Lo)
-    for flags in (0, bsm.BS_PERK):
+    for flags in (0, bsm.BS_PERK, bsm.BS_PERK | bsm.BS_PERK_PAIRED):
         Ug, Lg, ok = gpu_bounds(U0, L0, flags)
         assert ok
         # fp32 on the grid equals int32 / 1024 exactly
@@ -477,7 +484,7 @@ def test_batched_per_round_and_strided():
     for b, (uq, lq) in enumerate(Us):
         Ubuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(uq))
         Lbuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(lq))
-    for flags in (bsm.BS_PERK, 0, bsm.BS_TILE_128):
+    for flags in (bsm.BS_PERK, bsm.BS_PERK | bsm.BS_PERK_PAIRED, 0, bsm.BS_TILE_128):
         U, L = Ubuf.clone(), Lbuf.clone()
         bsm.bs_smooth_bounds_batched(U, L, n, ld, stride, B, None, bsm.BS_FP32 | flags)
         Uh, Lh = host(U), host(L)
@@ -605,6 +612,40 @@ def test_globule_16384_sampled_rows(globule16384, sched):
     assert np.all(Lg <= d + 1e-6) and np.all(d <= Ug + 1e-6)
 
 
+@pytest.mark.parametrize("sched", ["auto", "sym"])
+def test_globule_16384_every_cell_against_oracle(globule16384, sched):
+    """n = 16384, fp32, blocked, as timed by the benchmark, against the
+    oracle's own full result: every cell of U and L bit for bit, through the
+    SHA-256 digests of the oracle's output that tests/golden/
+    make_oracle_digest.py stored (whole matrices and blocks of 128 rows).  The
+    input's digests are checked first, so a generator that drew a different
+    molecule on this host is reported as such."""
+    import json
+    import os
+    from golden.make_oracle_digest import digest
+    m = globule16384[0]
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "globule16384_oracle.json")
+    with open(path) as f:
+        ref = json.load(f)
+    U0, L0 = W.to_f32(m["U"]), W.to_f32(m["L"])
+    assert ref["n"] == m["n"]
+    assert digest(U0)["sha256"] == ref["input"]["U"]["sha256"], "generator drew another input"
+    assert digest(L0)["sha256"] == ref["input"]["L"]["sha256"], "generator drew another input"
+    t = torch()
+    U, L = dev(U0), dev(L0)
+    del U0, L0
+    bsm.bs_smooth_bounds(U, L, flags=SCHEDULES[sched])
+    t.cuda.synchronize()
+    for name, mat in (("U", U), ("L", L)):
+        got = digest(host(mat))
+        bad = [b for b, (x, y) in enumerate(zip(got["blocks"], ref["output"][name]["blocks"]))
+               if x != y]
+        assert not bad, "%s differs from the oracle in row blocks %s" % (name, bad[:16])
+        assert got["sha256"] == ref["output"][name]["sha256"]
+    assert bsm.bs_check_feasible(U, L) == ref["flags"]
+
+
 # ------------------------------------------------------------------ checks and errors
 
 
@@ -655,7 +696,7 @@ def test_cuda_graph_capture_and_replay(sched, n):
     has more rest tiles than SMs: captured, it takes the order in which the
     rest of each round waits for the next block row and column."""
     t = torch()
-    flags = bsm.BS_PERK if sched == "perk" else SCHEDULES[sched]
+    flags = ALGOS[sched]
     Uq, Lq = W.random_bounds(n, 9300, p_bad=0.02)
     U0, L0 = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
     Uo, Lo = oracle.smooth(W.to_f32(Uq), W.to_f32(Lq))
@@ -733,16 +774,21 @@ def test_empty_and_launch_counting():
                          flags=bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD)
     assert bsm.bs_launch_count() - before == 3 * 3        # three phases x three block rounds
     before = bsm.bs_launch_count()
-    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)),
-                         flags=bsm.BS_TILE_64 | bsm.BS_FORCE_LOOKAHEAD)
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_TILE_64)
     # 5 block rounds: 5 x (phase 1, phase 2); 9 rest tiles, fewer than half
     # the SMs: phase 3 of rounds 0..3 is one launch without the next
     # diagonal tile (phase 1 of the next round takes it), then the last round
     assert bsm.bs_launch_count() - before == 5 + 5 + 4 + 1
     before = bsm.bs_launch_count()
-    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_TILE_64)
-    # look-ahead is the default from three block rounds on: the same launches
-    assert bsm.bs_launch_count() - before == 5 + 5 + 4 + 1
+    Ul, Ll = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
+    bsm.bs_smooth_bounds(Ul, Ll, flags=bsm.BS_PERK)
+    # the plain per-round mode: a pass and a row/column launch per round
+    assert bsm.bs_launch_count() - before == 2 * 300
+    before = bsm.bs_launch_count()
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)),
+                         flags=bsm.BS_PERK | bsm.BS_PERK_PAIRED)
+    # two rounds per pass: 150 passes, each with its row/column launch
+    assert bsm.bs_launch_count() - before == 2 * 150
     Uq7, Lq7 = W.random_bounds(700, 1, p_bad=0.01)
     before = bsm.bs_launch_count()
     bsm.bs_smooth_bounds(dev(W.to_f32(Uq7)), dev(W.to_f32(Lq7)), flags=bsm.BS_TILE_64)
@@ -758,7 +804,7 @@ def test_profile_records_every_launch():
     Uq, Lq = W.random_bounds(300, 2, p_bad=0.01)
     U, L = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
     bsm.bs_profile_begin()
-    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_TILE_128 | bsm.BS_FORCE_LOOKAHEAD)
+    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_TILE_128)
     p = bsm.bs_profile_end()
     # rounds 0, 1: phase 3 split into the rest (caller's stream) and the next
     # block row and column (look-ahead stream)
