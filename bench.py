@@ -27,6 +27,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# mode bits of the per-round forms: one round per pass, two rounds per pass
+PERK_FLAGS = {"perk": 1 << 2, "perk2": (1 << 2) | (1 << 10)}
 METRIC = "bound-smoothing cell-updates/s (n³/time) and % of GB300 FP32 ALU peak"
 UNIT = "cell-updates/s"
 OPS_PER_CELL = 6
@@ -84,12 +86,32 @@ def phase_cells(n, fb, sym=False):
     return p1, p2, p3
 
 
-def perk_bytes(n):
+def perk_bytes(n, paired=True):
     """DRAM bytes the per-round mode must move per smoothing: U and L read
-    and written once per pass over the matrix, a pass taking two rounds
-    (and a lone last round when n is odd)."""
-    passes = (n + 1) // 2
+    and written once per pass over the matrix; a pass takes one round (plain
+    form) or two (paired form, with a lone last round when n is odd)."""
+    passes = (n + 1) // 2 if paired else n
     return 16.0 * float(n) ** 2 * passes
+
+
+def phase3_algorithmic_bytes(cells, fb):
+    """DRAM bytes phase 3 must move for `cells` cell updates on fb-wide
+    tiles: each output tile of U and L (8 fb^2 bytes, fp32) read and written
+    once per block round, which applies fb middle atoms to its fb^2 cells --
+    16 / fb bytes per cell update."""
+    return 16.0 / fb * float(cells)
+
+
+def mix_ceiling_cells_per_clk(probe_instr_per_clk=None):
+    """Cell updates per clock per SM the phase-3 instruction mix allows: a
+    cell update is 3 adds (FP32 pipe) and 3 comparisons (ALU pipe), issued as
+    paired add.f32x2 and three-input min/max, two operations per instruction.
+    With both pipes fed every cycle (the probe interleaving the two forms
+    measures the issue rate) that is rate x 2 / 6; without a probe, the
+    128 + 128 lanes of the two pipes give 128 / 3."""
+    if probe_instr_per_clk:
+        return probe_instr_per_clk * 2.0 / 6.0
+    return 128.0 / 3.0
 
 
 def diag_cells(n, fb):
@@ -136,12 +158,16 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, sm_max_mhz=2070.0, source="fallback")
 
 
+KERNEL_SOURCES = ("phase3.cu", "pairops.cuh", "bs_tile.cuh", "bs_types.cuh")
+
+
 def kernel_hash():
-    """Hash of the phase-3 kernel's sources (the blocked kernels and their
-    device helpers): ties a committed ncu traffic figure to the code."""
+    """Hash of the phase-3 kernel's code (its source file, the device helpers
+    and the types it includes; not the host-side declarations of the other
+    kernels): ties a committed ncu traffic figure to the code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blocked_floyd_warshall_gb300", "csrc")
-    for f in ("phase3.cu", "pairops.cuh", "bs_tile.cuh", "bs_internal.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -282,6 +308,69 @@ def oracle_rate(U0, L0, seconds, max_rounds=None):
     return rounds * float(n) * n / el, rounds, oracle.threads(), el
 
 
+def oracle_plan(args):
+    """The CPU oracle as a reported baseline across the benchmark molecules:
+    one thread and all host cores on configs 0-3 (each a bounded sample: whole
+    smoothings, or its first rounds, or its first molecules, until about
+    --cpu-seconds of work), and with --oracle-full one full all-core run of
+    the n = 16384 globule, whose result is checked against the stored digest
+    of the oracle (tests/golden/globule16384_oracle.json).  One JSON line each."""
+    import oracle
+    from workloads import make_config, to_f32
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    all_threads = oracle.threads()
+    cases = [(0, "f32"), (1, "f32"), (2, "f32"), (2, "i32"), (3, "f32")]
+    for cfg, dt in cases:
+        m = make_config(cfg)
+        U0, L0 = (to_f32(m["U"]), to_f32(m["L"])) if dt == "f32" else (m["U"], m["L"])
+        n, batch = m["n"], m.get("batch", 1)
+        for threads in (1, all_threads):
+            oracle.set_threads(threads)
+            done, t0 = 0.0, time.perf_counter()
+            if batch > 1:
+                mols = 0
+                while mols < batch and time.perf_counter() - t0 < args.cpu_seconds:
+                    oracle.smooth(U0[mols], L0[mols])
+                    mols += 1
+                done = mols * float(n) ** 3
+                sample = "%d of %d molecules, whole smoothings" % (mols, batch)
+            else:
+                U, L = U0.copy(), L0.copy()
+                k = 0
+                while k < n and time.perf_counter() - t0 < args.cpu_seconds:
+                    k1 = min(n, k + 8)
+                    oracle.smooth(U, L, k_begin=k, k_end=k1, inplace=True)
+                    k = k1
+                done = k * float(n) ** 2
+                sample = ("whole smoothing" if k == n
+                          else "rounds 0..%d of %d" % (k - 1, n))
+            el = time.perf_counter() - t0
+            print(json.dumps({"oracle": "config %d" % cfg, "dtype": dt, "n": n, "batch": batch,
+                              "threads": threads, "host_cores": cores, "seconds": el,
+                              "cell_updates_per_s": done / el, "sample": sample}), flush=True)
+    oracle.set_threads(all_threads)
+    if args.oracle_full:
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from golden.make_oracle_digest import OUT, digest
+        m = make_config(4)
+        U, L = to_f32(m["U"]), to_f32(m["L"])
+        n = m["n"]
+        t0 = time.perf_counter()
+        oracle.smooth(U, L, inplace=True)
+        el = time.perf_counter() - t0
+        with open(OUT) as f:
+            ref = json.load(f)
+        same = (digest(U)["sha256"] == ref["output"]["U"]["sha256"]
+                and digest(L)["sha256"] == ref["output"]["L"]["sha256"])
+        print(json.dumps({"oracle": "config 4, full", "dtype": "f32", "n": n, "batch": 1,
+                          "threads": all_threads, "host_cores": cores, "seconds": el,
+                          "cell_updates_per_s": float(n) ** 3 / el,
+                          "sample": "whole smoothing",
+                          "matches_stored_digest": same}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ main
 
 
@@ -326,8 +415,9 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only run this many smoothing calls of the workload (no timing, "
                          "no JSON line): a short target for ncu captures")
-    ap.add_argument("--mode", choices=["blocked", "perk", "upper"], default="blocked",
-                    help="perk: the per-round reference mode (HBM-bound), for its roofline "
+    ap.add_argument("--mode", choices=["blocked", "perk", "perk2", "upper"], default="blocked",
+                    help="perk: the per-round reference mode, one round per pass (HBM-bound); "
+                         "perk2: its two-rounds-per-pass form; both for their HBM roofline "
                          "and captures; upper: bs_smooth_upper (U alone), with "
                          "--profile-calls only (the sweep times it)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -342,6 +432,12 @@ def main():
                     help="skip the extra timing of the symmetric half-work mode")
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark molecule (one JSON line each) instead")
+    ap.add_argument("--oracle-plan", action="store_true",
+                    help="time the CPU oracle on configs 0-3, one thread and all cores "
+                         "(one JSON line each), instead")
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="with --oracle-plan: also run the full n=16384 oracle once on all "
+                         "cores and check it against the stored digest (minutes)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -349,6 +445,8 @@ def main():
         ap.error("--mode upper is a capture target: use it with --profile-calls")
 
     ws, rank, local = dist_setup()
+    if args.oracle_plan:
+        return oracle_plan(args) if rank == 0 else 0
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     if args.sweep:
@@ -376,7 +474,7 @@ def main():
     copies = [(dU0.clone(), dL0.clone()) for _ in range(ncopies)]
     wU, wL = dU0.clone(), dL0.clone()
 
-    flags = bsm.BS_PERK if args.mode == "perk" else 0
+    flags = PERK_FLAGS.get(args.mode, 0)
     if args.profile_calls > 0:
         for _ in range(args.profile_calls):
             wU.copy_(dU0)
@@ -405,9 +503,9 @@ def main():
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = bsm.bs_launch_count()
-    # the per-round mode makes 2n launches per call: per-launch profile events
-    # would add their own cost to its time, so it is timed without them
-    profile = args.mode != "perk"
+    # the per-round mode makes up to 2n launches per call: per-launch profile
+    # events would add their own cost to its time, so it is timed without them
+    profile = args.mode not in PERK_FLAGS
     with ClockSampler(gpu_smi_id(torch)) as clk:
         if profile:
             bsm.bs_profile_begin()
@@ -433,8 +531,14 @@ def main():
     value = units / (total_ms * 1e-3)
 
     # parity of the timed output: the stored result is the fixed point, so one
-    # more smoothing must leave it unchanged and the flags must be zero
+    # more smoothing must leave every bit unchanged, and the flags must be zero
     U, L = copies[0]
+    U2, L2 = U.clone(), L.clone()
+    bsm.bs_smooth_bounds(U2, L2, flags=flags)
+    torch.cuda.synchronize()
+    fixed_point = bool(torch.equal(U2, U) and torch.equal(L2, L))
+    del U2, L2
+    assert fixed_point, "timed output is not the smoothing fixed point"
     if wl.get("consistent", True):
         assert bsm.bs_check_feasible(U, L) == 0
     # the feasibility pass (HBM-bound: reads 8 n^2 bytes), timed on its own
@@ -464,7 +568,12 @@ def main():
     p3_s_step = p3["ms"] * 1e-3 / args.steps
     p3_achieved = p3_ops_step / p3_s_step if p3["launches"] else None
     traffic = committed_traffic(main_cells_step)
+    algo_bytes = phase3_algorithmic_bytes(main_cells_step, fb)
     clocks = clk.summary()
+    probes = {} if args.no_probe else {
+        name: round(bsm.bs_probe_alu(name), 2) for name in bsm.PROBES}
+    mix_cells = mix_ceiling_cells_per_clk(probes.get("fadd2+fmnmx3"))
+    mix_peak_cells = sms * mix_cells * fmax
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -487,6 +596,17 @@ def main():
             "traffic": traffic,
             "traffic_basis": "DRAM bytes of the same launches in one smoothing step (ncu bytes "
                              "per cell update, profiles/phase3_traffic.json, x their cell updates)",
+            "algorithmic_bytes": algo_bytes,
+            "traffic_over_algorithmic": (traffic / algo_bytes) if traffic else None,
+            "algorithmic_bytes_basis": "16 / tile width bytes per cell update: each output tile "
+                                       "of U and L read and written once per block round",
+            "frac_of_instruction_mix_ceiling": (p3_achieved / OPS_PER_CELL / mix_peak_cells)
+                                               if p3_achieved else None,
+            "instruction_mix_ceiling_cells_per_clk_per_sm": mix_cells,
+            "instruction_mix_ceiling_basis": "3 adds (FP32 pipe) + 3 comparisons (ALU pipe) per "
+                                             "cell update, two per add.f32x2 / three-input "
+                                             "min-max; issue rate of the two interleaved, "
+                                             "measured by the ALU probe in this run",
             "ops_per_step": p3_ops_step,
             "cells_share_of_phase3": main_cells_step / p3_cells_step,
             "ms_per_step": p3_s_step * 1e3,
@@ -508,33 +628,37 @@ def main():
                      "basis": "bs_check_feasible on the smoothed matrices: 8 n^2 bytes read / "
                               "event time of the call (launch, counter reset, 8-byte readback)"},
     }
-    if args.mode == "perk":
-        # per-round mode, two rounds per pass: every pass reads and writes all
-        # of U and L, 8 bytes per cell update, HBM-bound; its kernels are timed
-        # as the "round" phase
-        r_gbs = perk_bytes(n) / (total_ms / args.steps * 1e-3) / 1e9
+    if args.mode in PERK_FLAGS:
+        # per-round mode: every pass reads and writes all of U and L (16 bytes
+        # per cell update with one round per pass, 8 with two), HBM-bound; the
+        # step is these launches only
+        paired = args.mode == "perk2"
+        r_gbs = perk_bytes(n, paired) / (total_ms / args.steps * 1e-3) / 1e9
         line["roofline"] = {
-            "kernel": "k_round2 + k_cross2 (per-round mode)", "bound": "hbm",
+            "kernel": ("k_round2 + k_cross2 (per-round mode, two rounds per pass)" if paired
+                       else "k_round + k_cross (per-round mode, one round per pass)"),
+            "bound": "hbm",
             "achieved": r_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": r_gbs / peaks["hbm_gbs"], "traffic": None,
-            "achieved_basis": "16 bytes (read + write of U and L) x n^2 cells per pass of two "
-                              "rounds (a lone last round for n odd) / step time (the step is "
-                              "these launches only)",
+            "achieved_basis": "16 bytes (read + write of U and L) x n^2 cells per pass (%s) / "
+                              "step time (the step is these launches only)"
+                              % ("two rounds per pass, a lone last round for n odd" if paired
+                                 else "one round per pass"),
             "peak_basis": "STREAM-style copy (%s)" % peaks["source"],
             "launches_per_step": launches / args.steps,
         }
 
     if not args.no_symmetric:
         line["symmetric"] = symmetric_leg(torch, bsm, dU0, dL0, copies, args, value / ws)
-    if not args.no_probe:
-        line["alu_probe_instr_per_clk_per_sm"] = {
-            name: round(bsm.bs_probe_alu(name), 2) for name in bsm.PROBES}
+    if probes:
+        line["alu_probe_instr_per_clk_per_sm"] = probes
     if not args.no_e2e:
         line["e2e"] = e2e_leg(torch, bsm, U0, L0, args, ws)
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:
         rate, rounds, thr, el = oracle_rate(U0, L0, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "host_cores": len(os.sched_getaffinity(0)),
             "sample": "rounds 0..%d of the n=%d workload (%d x n^2 cell updates, %.1f s)"
                       % (rounds - 1, n, rounds, el)}
     if rank == 0:
@@ -544,9 +668,9 @@ def main():
     return 0
 
 
-SCHEDULE_FLAGS = {"auto": 0, "t64": (1 << 5) | (1 << 9), "t128": (1 << 6) | (1 << 9),
+SCHEDULE_FLAGS = {"auto": 0, "t64": 1 << 5, "t128": 1 << 6,
                   "t64_serial": (1 << 5) | (1 << 7), "t128_serial": (1 << 6) | (1 << 7),
-                  "perk": 1 << 2, "sym": 1 << 8,
+                  "perk": 1 << 2, "perk2": (1 << 2) | (1 << 10), "sym": 1 << 8,
                   "graph": 0,   # "graph": the auto schedule captured once, replayed
                   "upper": 0}   # "upper": bs_smooth_upper, U alone
 ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial", "sym")
@@ -556,7 +680,7 @@ SWEEP = (
     (1, "f32", ALL_SCHEDULES + ("graph",), "chain n=1000"),
     (("random", 2048), "f32", ALL_SCHEDULES + ("graph",), "random bounds n=2048"),
     (("random", 3000), "f32", ("auto", "t64", "t128", "t128_serial"), "random bounds n=3000"),
-    (2, "f32", ALL_SCHEDULES + ("perk", "upper"), "globule n=4096"),
+    (2, "f32", ALL_SCHEDULES + ("perk", "perk2", "upper"), "globule n=4096"),
     (2, "i32", ("auto",), "globule n=4096"),
     (3, "f32", ALL_SCHEDULES, "256 chains n=512, batched"),
     (4, "f32", ("auto", "t128_serial", "sym", "upper"), "globule n=16384"),
@@ -646,8 +770,8 @@ def sweep(args):
             if algo == "upper":
                 # U alone: an add and a min per cell update
                 line["fp32_alu_frac_upper"] = rate * 2 / alu
-            if algo == "perk":
-                gbs = perk_bytes(n) * batch / (ms * 1e-3) / 1e9
+            if algo in PERK_FLAGS:
+                gbs = perk_bytes(n, algo == "perk2") * batch / (ms * 1e-3) / 1e9
                 line["hbm_gbs_algorithmic"] = gbs
                 line["hbm_frac"] = gbs / peaks["hbm_gbs"]
             print(json.dumps(line), flush=True)

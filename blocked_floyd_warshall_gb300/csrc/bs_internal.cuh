@@ -1,33 +1,9 @@
 // Internal declarations shared by the CUDA translation units of libbsmooth.
 #pragma once
 
-#include <cuda_runtime.h>
-#include <stdint.h>
+#include "bs_types.cuh"
 
 namespace bs {
-
-// Floyd-Warshall block (tile) sizes of the three-phase schedule: 128 for large
-// matrices, 64 for small ones (an eighth of the serial phase-1 work per block
-// round, and four times the tiles to spread over the SMs).
-constexpr int FB_LARGE = 128;
-constexpr int FB_SMALL = 64;
-
-// One batch of matrices as the kernels see it.
-struct Mats {
-    void* U;
-    void* L;              // nullptr: upper bounds only
-    int n;
-    int ld;
-    long long bstride;    // elements between molecules
-    int batch;
-    bool vec;             // 16-byte vector IO allowed (ld % 4 == 0, bases 16B-aligned)
-    int fb;               // blocked mode: tile size FB_LARGE or FB_SMALL
-    bool sym;             // blocked mode: inputs symmetric, compute half and mirror
-    int sms;              // multiprocessors of the device
-};
-
-// profile categories (the index of bs_profile's arrays)
-enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3, PH_NEXT = 4 };
 
 // Launch bookkeeping (api.cu): counts launches and, when profiling, records an
 // event pair around each launch on `s`.
@@ -50,9 +26,8 @@ cudaError_t phase3_setup(bool is_int);
 // phase 3 of round K-1; 64-wide tiles only.
 cudaError_t launch_phase1(bool is_int, const Mats& m, int K, bool pre, cudaStream_t s);
 cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
-// Phase 3 of block round K over the tiles `part` selects (P3_* below).
+// Phase 3 of block round K over the tiles `part` selects (P3_* in bs_types.cuh).
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s);
-enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2, P3_PANELS = 3, P3_ALL_OFF = 4 };
 
 // Feasibility count and precondition checks.  `count` and `flags` are device
 // words the caller has zeroed on `s`.

@@ -1,6 +1,8 @@
 """Host-side accounting of bench.py (no GPU): the cell-update counts its
 roofline divides by, and its copies of the library's schedule rules."""
 import itertools
+import json
+import os
 
 import pytest
 
@@ -77,7 +79,39 @@ def test_tile_rule_matches_documented_thresholds():
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4096, 4097])
 def test_per_round_bytes(n):
-    """Per-round mode: one read and one write of U and L per pass, a pass
-    taking two rounds and a lone last round for n odd."""
+    """Per-round mode: one read and one write of U and L per pass; the plain
+    form takes one round per pass, the paired form two (and a lone last round
+    for n odd)."""
     passes = n // 2 + n % 2
-    assert bench.perk_bytes(n) == 16 * n * n * passes
+    assert bench.perk_bytes(n, paired=True) == 16 * n * n * passes
+    assert bench.perk_bytes(n, paired=False) == 16 * n * n * n
+
+
+def test_phase3_algorithmic_bytes():
+    """One read and one write of every output tile of U and L per block round:
+    a 128-wide tile holds 128^2 cells x 8 bytes (fp32 U and L) and takes
+    128^3 cell updates per block round, 2 x 8 x 128^2 bytes -- 1/8 byte each."""
+    cells_one_tile_round = 128 ** 3
+    assert bench.phase3_algorithmic_bytes(cells_one_tile_round, 128) == 2 * 8 * 128 ** 2
+    assert bench.phase3_algorithmic_bytes(64 ** 3, 64) == 2 * 8 * 64 ** 2
+
+
+def test_instruction_mix_ceiling():
+    """3 adds + 3 comparisons per cell update, two operations per paired
+    instruction: at 128 paired instructions per clock per SM, 128 / 3 cells."""
+    assert bench.mix_ceiling_cells_per_clk(128.0) == pytest.approx(128.0 / 3)
+    assert bench.mix_ceiling_cells_per_clk(None) == pytest.approx(128.0 / 3)
+    assert bench.mix_ceiling_cells_per_clk(125.0) == pytest.approx(125.0 / 3)
+
+
+def test_committed_phase3_capture_is_current():
+    """The committed ncu DRAM figure of phase 3 was taken on the current
+    kernel code; after any change to that code the capture must be re-taken
+    (bench.py reports no traffic while the hashes differ)."""
+    with open(os.path.join(bench.ROOT, "profiles", "phase3_traffic.json")) as f:
+        d = json.load(f)
+    assert d["kernel_hash"] == bench.kernel_hash(), (
+        "profiles/phase3_traffic.json is stale: re-take the phase-3 DRAM capture")
+    per_cell = d["dram_bytes_per_cell_k"]
+    assert per_cell == pytest.approx(
+        (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["cells_per_launch"])
