@@ -117,8 +117,12 @@ def backbite(path: np.ndarray, box: tuple[int, int, int], moves: int,
 
 
 def lattice_globule(box: tuple[int, int, int], rng: np.random.Generator,
-                    moves_per_atom: int = 4) -> tuple[np.ndarray, np.ndarray]:
-    """Compact self-avoiding chain filling the box; returns (sites, coords in A)."""
+                    moves_per_atom: int = 20) -> tuple[np.ndarray, np.ndarray]:
+    """Compact self-avoiding chain filling the box; returns (sites, coords in A).
+
+    20 backbite moves per atom: each accepted move reverses a stretch of the
+    path, so after a few multiples of n moves the serpentine's long-range order
+    (contacts only between neighbouring rows of the boustrophedon) is gone."""
     sites = serpentine(box)
     sites = backbite(sites, box, moves_per_atom * len(sites), rng)
     return sites, sites.astype(np.float64) * BOND
