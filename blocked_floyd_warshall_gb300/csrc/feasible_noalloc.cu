@@ -57,7 +57,10 @@ k_feasible_each(const T* __restrict__ U, const T* __restrict__ L, int n, int ld,
 }
 
 // Device address of the static array on the current device.  Looked up once
-// per device, with that device current, on the first call.
+// per device, with that device current, on the first call, and kept for the
+// life of the process.  cudaDeviceReset destroys the device's context and
+// with it the module holding the array, so the kept address is stale after
+// one: this entry point must not be used on a device after a reset of it.
 cudaError_t noalloc_counts(unsigned long long** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -114,6 +117,9 @@ extern "C" bs_status bs_check_feasible_noalloc(const void* U, const void* L, int
         e = (mode & BS_DTYPE_MASK) == BS_INT32_Q10
                 ? bs::launch_each<int>(U, L, n, ld, stride, batch, counts, stream)
                 : bs::launch_each<float>(U, L, n, ld, stride, batch, counts, stream);
+    // The device counters are unsigned 64-bit; they are copied bit for bit
+    // into the caller's long long array, as bs_check_feasible returns its
+    // count.  A count is at most n^2 < 2^62, so it reads the same either way.
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(out_counts, counts, sizeof(unsigned long long) * (size_t)batch,
                             cudaMemcpyDeviceToHost, stream);
