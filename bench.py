@@ -671,18 +671,19 @@ def main():
 SCHEDULE_FLAGS = {"auto": 0, "t64": 1 << 5, "t128": 1 << 6,
                   "t64_serial": (1 << 5) | (1 << 7), "t128_serial": (1 << 6) | (1 << 7),
                   "perk": 1 << 2, "perk2": (1 << 2) | (1 << 10), "sym": 1 << 8,
+                  "one": 1 << 11, "one_sym": (1 << 11) | (1 << 8),   # one launch per call
                   "graph": 0,   # "graph": the auto schedule captured once, replayed
                   "upper": 0}   # "upper": bs_smooth_upper, U alone
 ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial", "sym")
 SWEEP = (
     # (config, dtype, schedules, description); config None: random bounds of size n
-    (0, "f32", ALL_SCHEDULES + ("graph",), "chain n=256"),
-    (1, "f32", ALL_SCHEDULES + ("graph",), "chain n=1000"),
-    (("random", 2048), "f32", ALL_SCHEDULES + ("graph",), "random bounds n=2048"),
+    (0, "f32", ALL_SCHEDULES + ("graph", "one"), "chain n=256"),
+    (1, "f32", ALL_SCHEDULES + ("graph", "one"), "chain n=1000"),
+    (("random", 2048), "f32", ALL_SCHEDULES + ("graph", "one"), "random bounds n=2048"),
     (("random", 3000), "f32", ("auto", "t64", "t128", "t128_serial"), "random bounds n=3000"),
     (2, "f32", ALL_SCHEDULES + ("perk", "perk2", "upper"), "globule n=4096"),
     (2, "i32", ("auto",), "globule n=4096"),
-    (3, "f32", ALL_SCHEDULES, "256 chains n=512, batched"),
+    (3, "f32", ALL_SCHEDULES + ("one", "one_sym"), "256 chains n=512, batched"),
     (4, "f32", ("auto", "t128_serial", "sym", "upper"), "globule n=16384"),
 )
 
@@ -763,8 +764,9 @@ def sweep(args):
             line = {"sweep": desc, "config": cfg, "dtype": dt, "mode": algo, "n": n, "batch": batch,
                     "ms_median": ms, "ms_best": min(times), "cell_updates_per_s": rate,
                     "fp32_alu_frac": rate * OPS_PER_CELL / alu}
-            if algo == "sym":
-                executed = batch * float(sum(phase_cells(n, tile_size(n, flags, batch), sym=True)))
+            if algo in ("sym", "one_sym"):
+                fb = 64 if algo == "one_sym" else tile_size(n, flags, batch)
+                executed = batch * float(sum(phase_cells(n, fb, sym=True)))
                 line["executed_cell_updates"] = executed
                 line["fp32_alu_frac_executed"] = executed / (ms * 1e-3) * OPS_PER_CELL / alu
             if algo == "upper":

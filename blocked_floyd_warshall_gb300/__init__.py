@@ -47,8 +47,9 @@ BS_TILE_128 = 1 << 6
 BS_NO_LOOKAHEAD = 1 << 7
 BS_SYMMETRIC = 1 << 8
 BS_PERK_PAIRED = 1 << 10
+BS_ONE_LAUNCH = 1 << 11
 
-PHASES = ("round", "phase1", "phase2", "phase3", "phase3_next")
+PHASES = ("round", "phase1", "phase2", "phase3", "phase3_next", "one_launch")
 
 PROBES = {"fadd": 0, "fmnmx": 1, "fmnmx3": 2, "fadd2": 3, "fadd2+fmnmx3": 4,
           "iadd": 5, "imnmx": 6, "viaddmin": 7, "vimnmx3": 8}
@@ -61,7 +62,7 @@ class BSError(RuntimeError):
 
 
 class _Profile(ctypes.Structure):
-    _fields_ = [("ms", ctypes.c_double * 5), ("launches", ctypes.c_longlong * 5),
+    _fields_ = [("ms", ctypes.c_double * 6), ("launches", ctypes.c_longlong * 6),
                 ("overflow", ctypes.c_int)]
 
 
@@ -106,6 +107,8 @@ def library() -> ctypes.CDLL:
         lib.bs_strerror.restype = ctypes.c_char_p
         lib.bs_launch_count.argtypes = []
         lib.bs_launch_count.restype = ll
+        lib.bs_one_launch_cluster.argtypes = []
+        lib.bs_one_launch_cluster.restype = i
         _lib = lib
         return lib
 
@@ -247,6 +250,12 @@ def bs_strerror(status: int) -> str:
 
 def bs_launch_count() -> int:
     return int(library().bs_launch_count())
+
+
+def bs_one_launch_cluster() -> int:
+    """CTAs per cluster of BS_ONE_LAUNCH on the current device (0 before the
+    first smoothing call on it)."""
+    return int(library().bs_one_launch_cluster())
 
 
 def bs_profile_begin() -> None:

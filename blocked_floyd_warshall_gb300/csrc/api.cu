@@ -56,6 +56,8 @@ cudaError_t device_state(DeviceState** out) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = bs::blocked_setup(false);
         if (e == cudaSuccess) e = bs::blocked_setup(true);
+        if (e == cudaSuccess) e = bs::fused_setup(false);
+        if (e == cudaSuccess) e = bs::fused_setup(true);
         if (e != cudaSuccess) return e;
         d.ready = true;
     }
@@ -259,10 +261,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
                      long long bstride, int batch, int mode, bs::Mats* m) {
     const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE | BS_TILE_64 |
-                      BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC | BS_PERK_PAIRED;
+                      BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC | BS_PERK_PAIRED |
+                      BS_ONE_LAUNCH;
     if (mode & ~known) return BS_ERR_ARG;
     if ((mode & BS_TILE_64) && (mode & BS_TILE_128)) return BS_ERR_ARG;
     if ((mode & BS_PERK_PAIRED) && !(mode & BS_PERK)) return BS_ERR_ARG;
+    if ((mode & BS_ONE_LAUNCH) && (mode & (BS_PERK | BS_TILE_128 | BS_NO_LOOKAHEAD)))
+        return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
     if (n < 0 || batch < 0) return BS_ERR_ARG;
     if (n > 0 && ld < n) return BS_ERR_ARG;
@@ -281,7 +286,7 @@ bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
     m->batch = batch;
     m->vec = (ld % 4 == 0) && aligned(U, 16) && (!bounds || aligned(L, 16)) &&
              (batch <= 1 || bstride % 4 == 0);
-    m->fb = choose_tile(n, batch, mode, bounds);
+    m->fb = (mode & BS_ONE_LAUNCH) ? bs::FB_SMALL : choose_tile(n, batch, mode, bounds);
     m->sym = (mode & BS_SYMMETRIC) != 0;
     m->sms = 1;
     return BS_OK;
@@ -334,6 +339,8 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
             e = bs::launch_round(is_int, m, k, literal, s);
             if (e == cudaSuccess && bounds) e = bs::launch_cross(is_int, m, k, s);
         }
+    } else if (mode & BS_ONE_LAUNCH) {
+        e = bs::launch_fused(is_int, m, s);
     } else {
         e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0, d);
     }
@@ -435,6 +442,8 @@ const char* bs_strerror(bs_status status) {
 }
 
 long long bs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int bs_one_launch_cluster(void) { return bs::fused_cluster_size(); }
 
 bs_status bs_profile_begin(void) {
     std::lock_guard<std::mutex> lk(g_prof_mu);

@@ -29,6 +29,12 @@ cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
 // Phase 3 of block round K over the tiles `part` selects (P3_* in bs_types.cuh).
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s);
 
+// The whole blocked smoothing in one launch, one cluster per molecule
+// (fused.cu); fused_setup once per device and dtype.
+cudaError_t fused_setup(bool is_int);
+cudaError_t launch_fused(bool is_int, const Mats& m, cudaStream_t s);
+int fused_cluster_size();   // CTAs per cluster on the current device (0: not set up)
+
 // Feasibility count and precondition checks.  `count` and `flags` are device
 // words the caller has zeroed on `s`.
 cudaError_t launch_feasible(bool is_int, const Mats& m, unsigned char* mask,

@@ -29,7 +29,7 @@ struct Mats {
 };
 
 // profile categories (the index of bs_profile's arrays)
-enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3, PH_NEXT = 4 };
+enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3, PH_NEXT = 4, PH_FUSED = 5 };
 
 // Which tiles a phase-3 launch covers (see p3_tile in phase3.cu).
 enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2, P3_PANELS = 3, P3_ALL_OFF = 4 };

@@ -2,294 +2,23 @@
 // bulk tile updates, one kernel.  (The schedule as a whole, and why the panels
 // are the same product as the bulk tiles, is described at the top of
 // phase1.cu.)
-#include "pairops.cuh"
+#include "p3_tile.cuh"
 
 namespace bs {
-
-// Micro-tile shape: no barrier per step, so many cells per thread (few
-// shared-memory loads per cell update).  128-wide tiles: 8 x 8 cells, 256
-// threads, one CTA per SM.  64-wide tiles: 8 x 4 cells, 128 threads: half the
-// registers of 8 x 8, so four CTAs per SM hold twice the warps (measured
-// against 8 x 8 with 64 threads: n = 3000 16 % faster, n = 4096 on 64-wide
-// tiles 11 %).  When a launch has too few tiles to fill the GPU, each CTA is
-// latency-bound; the wide form of the 64-wide tile then spreads it over 256
-// threads (4 x 4 cells each).
-template <int FB, bool WIDE>
-using P3S = Shape<FB, (WIDE ? 4 : 8), (WIDE || FB == FB_SMALL ? 4 : 8)>;
-
-// ---------------------------------------------------------------- phase 3
-//
-// The kernel updates tile (I,J) from the column operand (I,K) and the row
-// operand (K,J): in phase 3 the finished panels; in phase 2 the finished
-// diagonal tile (K,K) and the panel tile itself, read before the CTA writes it
-// (no other CTA touches it).  Both are streamed through shared memory in chunks of BK
-// middle atoms (two stages, cp.async).  The inner loop takes the middle atoms
-// two at a time: a thread holds, per row r, the pair (U[i,k], U[i,k+1]) in one
-// 64-bit register (the column panel is stored [i][k], so the pair is one
-// 8-byte load), and per column c the pair (U[k,j], U[k+1,j]) (the row panel is
-// stored k-interleaved, [k/2][j][k%2]).  For fp32 one add.rn.f32x2 then forms
-// both candidate sums of a cell and one three-input min.f32 folds them into
-// the accumulator; the lower bound takes two sub.rn.f32x2 and two three-input
-// max.f32.  3 instructions per cell update instead of 6.  min and max are
-// exact, so the grouping of k changes no result; every sum is the same
-// round-to-nearest fp32 add.  int32 uses the add-then-min/max forms
-// (__viaddmin_s32 / __viaddmax_s32).
-
-// Middle atoms staged per pipeline stage: 32 on 128-wide tiles (half the
-// barriers of 16; measured 5 % faster), 16 on 64-wide tiles (keeps four CTAs
-// per SM within shared memory).  The column panel's row stride BK + 4 keeps its
-// rows 16-byte aligned.
-template <int FB> struct P3K {
-    static constexpr int BK = FB == FB_LARGE ? 32 : 16;
-    static constexpr int AST = BK + 4;
-};
-
-template <class T, bool HAS_L, int FB>
-struct P3Smem {
-    static constexpr int BK = P3K<FB>::BK;
-    static constexpr int AST = P3K<FB>::AST;
-    // one stage: column panel A[i][k] (FB x AST) and row panel B[k/2][j][k%2]
-    static constexpr int A_ELEMS = FB * AST;
-    static constexpr int B_ELEMS = BK * FB;
-    static constexpr int MATS = HAS_L ? 2 : 1;
-    static constexpr int STAGE = MATS * (A_ELEMS + B_ELEMS);   // layout AU | BU | AL | BL
-    static constexpr size_t BYTES = 2 * STAGE * sizeof(T);
-};
-
-// Stage k-chunk `c` of both panels into shared memory stage `stage`.
-template <class T, bool HAS_L, int FB, int NT>
-__device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_t ld, int oi,
-                                         int oj, int ok, int mi, int mj, int mk, int c,
-                                         bool vec) {
-    using E = El<T>;
-    using SM = P3Smem<T, HAS_L, FB>;
-    constexpr int BK = P3K<FB>::BK, AST = P3K<FB>::AST;
-    T* AU = stage;
-    T* BU = stage + SM::A_ELEMS;
-    T* AL = HAS_L ? BU + SM::B_ELEMS : nullptr;
-    T* BL = HAS_L ? AL + SM::A_ELEMS : nullptr;
-    const int kc = c * BK;
-    // column panel: FB rows x BK middle atoms, [i][k]
-    if (vec) {
-        for (int p = threadIdx.x; p < FB * (BK / 4); p += NT) {
-            const int i = p / (BK / 4);
-            const int kq = (p % (BK / 4)) * 4;
-            const size_t g = (size_t)(oi + i) * ld + ok + kc + kq;
-            if (i < mi && kc + kq + 4 <= mk) {
-                cp_async16(AU + i * AST + kq, U + g);
-                if (HAS_L) cp_async16(AL + i * AST + kq, L + g);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const bool in = i < mi && kc + kq + q < mk;
-                    AU[i * AST + kq + q] = in ? U[g + q] : E::upad();
-                    if (HAS_L) AL[i * AST + kq + q] = in ? L[g + q] : E::lpad();
-                }
-            }
-        }
-    } else {
-        for (int p = threadIdx.x; p < FB * BK; p += NT) {
-            const int i = p / BK, k = p % BK;
-            const size_t g = (size_t)(oi + i) * ld + ok + kc + k;
-            if (i < mi && kc + k < mk) {
-                cp_async4(AU + i * AST + k, U + g);
-                if (HAS_L) cp_async4(AL + i * AST + k, L + g);
-            } else {
-                AU[i * AST + k] = E::upad();
-                if (HAS_L) AL[i * AST + k] = E::lpad();
-            }
-        }
-    }
-    // row panel: BK middle atoms x FB columns, k-interleaved
-    for (int p = threadIdx.x; p < BK * FB; p += NT) {
-        const int k = p / FB, j = p % FB;
-        const int d = (k >> 1) * (2 * FB) + j * 2 + (k & 1);
-        const size_t g = (size_t)(ok + kc + k) * ld + oj + j;
-        if (kc + k < mk && j < mj) {
-            cp_async4(BU + d, U + g);
-            if (HAS_L) cp_async4(BL + d, L + g);
-        } else {
-            BU[d] = E::upad();
-            if (HAS_L) BL[d] = E::lpad();
-        }
-    }
-}
-
-// Which tiles a launch covers (block round K, nb tile rows):
-//   P3_ALL    : every tile outside block-row K and block-column K;
-//   P3_NEXT   : those in block-row K+1 or block-column K+1 (the tiles the next
-//               block round's phases 1 and 2 read and write);
-//   P3_REST   : the others;
-//   P3_ALL_OFF: P3_ALL without tile (K+1,K+1), whose update phase 1 of round
-//               K+1 takes over;
-//   P3_PANELS : phase 2, the row panel (K,J) then the column panel (I,K).
-// With symmetric inputs only tiles with I <= J are computed (each off-diagonal
-// one is also stored transposed): (nb-1)nb/2, nb-1, (nb-2)(nb-1)/2 and
-// (nb-1)nb/2 - 1 tiles; phase 2 computes the row panel and stores it
-// transposed as the column panel.
-
-// t -> (a, b), a <= b, enumerating the upper triangle column by column.
-__device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
-    int c = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
-    while (c * (c + 1) / 2 > t) --c;
-    while ((c + 1) * (c + 2) / 2 <= t) ++c;
-    b = c;
-    a = t - c * (c + 1) / 2;
-}
-
-__device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K, int& I,
-                                        int& J) {
-    if (part == P3_PANELS) {
-        if (t < nb - 1) {
-            I = K;
-            J = t + (t >= K);
-        } else {
-            const int u = t - (nb - 1);
-            I = u + (u >= K);
-            J = K;
-        }
-        return;
-    }
-    if (!sym) {
-        if (part == P3_ALL || part == P3_ALL_OFF) {
-            if (part == P3_ALL_OFF) t += t >= K * nb;   // skip (K+1,K+1): ti = tj = K
-            const int ti = t / (nb - 1), tj = t % (nb - 1);
-            I = ti + (ti >= K);
-            J = tj + (tj >= K);
-        } else if (part == P3_NEXT) {
-            if (t < nb - 1) {
-                I = K + 1;
-                J = t + (t >= K);
-            } else {
-                const int u = t - (nb - 1);
-                I = u + 2 * (u >= K);
-                J = K + 1;
-            }
-        } else {
-            const int ti = t / (nb - 2), tj = t % (nb - 2);
-            I = ti + 2 * (ti >= K);
-            J = tj + 2 * (tj >= K);
-        }
-        return;
-    }
-    int a, b;
-    if (part == P3_ALL || part == P3_ALL_OFF) {
-        if (part == P3_ALL_OFF) t += t >= K * (K + 1) / 2 + K;   // skip (K+1,K+1): a = b = K
-        p3_tri(t, a, b);
-        I = a + (a >= K);
-        J = b + (b >= K);
-    } else if (part == P3_NEXT) {
-        if (t < nb - K - 1) {
-            I = K + 1;
-            J = K + 1 + t;
-        } else {
-            I = t - (nb - K - 1);
-            J = K + 1;
-        }
-    } else {
-        p3_tri(t, a, b);
-        I = a + 2 * (a >= K);
-        J = b + 2 * (b >= K);
-    }
-}
 
 template <class T, bool HAS_L, int FB, bool WIDE>
 __global__ void __launch_bounds__(P3S<FB, WIDE>::NT, (!HAS_L && FB == FB_LARGE) ? 2 : 0)
 k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K,
          int part, bool vec, bool sym) {
-    using S = P3S<FB, WIDE>;
-    using E = El<T>;
-    using SM = P3Smem<T, HAS_L, FB>;
-    using LD = PairLoad<T>;
-    constexpr int BK = P3K<FB>::BK, AST = P3K<FB>::AST;
-    using P = typename LD::P;
-    constexpr bool NEG = std::is_same<T, int>::value;   // int lower bound adds negated values
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    T* sm = reinterpret_cast<T*>(smem_raw);
-
     const size_t off = (size_t)blockIdx.z * (size_t)bstride;
     U += off;
     if (HAS_L) L += off;
     const int nb = (n + FB - 1) / FB;
     int I, J;
     p3_tile(part, sym, blockIdx.x, nb, K, I, J);
-    const int oi = I * FB, oj = J * FB, ok = K * FB;
-    const int mi = min(FB, n - oi), mj = min(FB, n - oj), mk = min(FB, n - ok);
-
-    T u[S::TM][S::TN], l[S::TM][S::TN];
-    load_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
-    if (HAS_L) load_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
-
-    const int nchunks = (mk + BK - 1) / BK;
-    p3_stage<T, HAS_L, FB, S::NT>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
-    cp_async_commit();
-    const int r0 = S::row0(), cq = S::cq();
-    for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks)
-            p3_stage<T, HAS_L, FB, S::NT>(sm + ((c + 1) & 1) * SM::STAGE, U, L, ld, oi, oj, ok,
-                                          mi, mj, mk, c + 1, vec);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const T* AU = sm + (c & 1) * SM::STAGE;
-        const T* BU = AU + SM::A_ELEMS;
-        const T* AL = BU + SM::B_ELEMS;
-        const T* BL = AL + SM::A_ELEMS;
-        auto step = [&](int kk) {
-            P a[S::TM], al[S::TM], b[S::TN], bl[S::TN];
-#pragma unroll
-            for (int r = 0; r < S::TM; ++r) {
-                a[r] = LD::ld2(AU + (r0 + r) * AST + kk);
-                if (HAS_L) al[r] = LD::ld2(AL + (r0 + r) * AST + kk);
-            }
-            const int bo = (kk >> 1) * (2 * FB);
-#pragma unroll
-            for (int h = 0; h < S::QUADS; ++h) {
-                const int jb = bo + (h * S::QSTRIDE + cq) * 2;
-                LD::ld4(BU + jb, b[h * 4 + 0], b[h * 4 + 1]);
-                LD::ld4(BU + jb + 4, b[h * 4 + 2], b[h * 4 + 3]);
-                if (HAS_L) {
-                    LD::ld4(BL + jb, bl[h * 4 + 0], bl[h * 4 + 1]);
-                    LD::ld4(BL + jb + 4, bl[h * 4 + 2], bl[h * 4 + 3]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < S::TM; ++r)
-#pragma unroll
-                for (int q = 0; q < S::TN; ++q) PairOps<T>::upper(u[r][q], a[r], b[q]);
-            if (HAS_L) {
-                if (NEG) {
-#pragma unroll
-                    for (int r = 0; r < S::TM; ++r) a[r] = LD::neg(a[r]);
-#pragma unroll
-                    for (int q = 0; q < S::TN; ++q) b[q] = LD::neg(b[q]);
-                }
-#pragma unroll
-                for (int r = 0; r < S::TM; ++r)
-#pragma unroll
-                    for (int q = 0; q < S::TN; ++q)
-                        PairOps<T>::lower(l[r][q], a[r], al[r], b[q], bl[q]);
-            }
-        };
-        if constexpr (HAS_L || FB == FB_SMALL) {
-#pragma unroll 1
-            for (int kk = 0; kk < BK; kk += 2) step(kk);
-        } else {
-            // Upper bounds alone on 128-wide tiles: the whole chunk unrolled
-            // (addresses become immediates; 128 registers, two CTAs per SM),
-            // 5 % faster at n = 16384.  With L the registers do not allow
-            // it, and the 64-wide forms measured slower unrolled.
-#pragma unroll
-            for (int kk = 0; kk < BK; kk += 2) step(kk);
-        }
-        __syncthreads();
-    }
-    store_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
-    if (HAS_L) store_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
-    if (sym && I != J) {
-        store_tile_t<S>(u, U + (size_t)oj * ld + oi, ld, mi, mj, vec);
-        if (HAS_L) store_tile_t<S>(l, L + (size_t)oj * ld + oi, ld, mi, mj, vec);
-    }
+    p3_update_tile<T, HAS_L, FB, WIDE>(U, L, n, ld, I, J, K, vec, sym,
+                                       reinterpret_cast<T*>(smem_raw));
 }
 
 // ---------------------------------------------------------------- strips
@@ -504,21 +233,6 @@ static cudaError_t setup3() {
 }
 
 cudaError_t phase3_setup(bool is_int) { return is_int ? setup3<int>() : setup3<float>(); }
-
-// Tiles a phase-3 launch covers (see p3_tile).
-static int p3_tiles(bool sym, int part, int nb, int K) {
-    if (nb < 2) return 0;
-    if (part == P3_PANELS) return sym ? nb - 1 : 2 * (nb - 1);
-    if (sym)
-        return part == P3_ALL ? (nb - 1) * nb / 2
-               : part == P3_NEXT ? (K + 1 < nb ? nb - 1 : 0)
-               : part == P3_ALL_OFF ? (K + 1 < nb ? (nb - 1) * nb / 2 - 1 : 0)
-                                     : (K + 1 < nb ? (nb - 2) * (nb - 1) / 2 : 0);
-    return part == P3_ALL ? (nb - 1) * (nb - 1)
-           : part == P3_NEXT ? (K + 1 < nb ? 2 * nb - 3 : 0)
-           : part == P3_ALL_OFF ? (K + 1 < nb ? (nb - 1) * (nb - 1) - 1 : 0)
-                                 : (K + 1 < nb ? (nb - 2) * (nb - 2) : 0);
-}
 
 template <class T, bool HAS_L, int FB, bool WIDE>
 static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {

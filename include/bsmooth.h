@@ -105,6 +105,13 @@ enum {
     BS_PERK_PAIRED = 1 << 10, /* with BS_PERK: two rounds per pass over the
                                  matrix (half the memory traffic), each round
                                  exactly as alone; without BS_PERK: BS_ERR_ARG */
+    BS_ONE_LAUNCH = 1 << 11,  /* blocked mode in a single kernel launch: one
+                                 thread-block cluster (16 CTAs where the device
+                                 allows, else 8) per molecule, 64 x 64 tiles,
+                                 the phases of each block round separated by
+                                 cluster barriers only; same results.  Meant
+                                 for batches of small molecules.  With BS_PERK,
+                                 BS_TILE_128 or BS_NO_LOOKAHEAD: BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the
                                  diagonal are computed, each mirrored into its
@@ -180,6 +187,10 @@ bs_status bs_check_feasible_noalloc(const void *U, const void *L, int n, int ld,
 /* Number of kernels this library has launched since it was loaded. */
 long long bs_launch_count(void);
 
+/* CTAs per thread-block cluster of BS_ONE_LAUNCH on the current device (16 or
+ * 8), or 0 before the library's first smoothing call on it. */
+int bs_one_launch_cluster(void);
+
 /* Per-phase device time.  After bs_profile_begin(), every smoothing call
  * records a CUDA event pair around each of its kernel launches, on the stream
  * the kernel runs on (the caller's, or the library's look-ahead stream).
@@ -187,9 +198,9 @@ long long bs_launch_count(void);
  * launch counts per phase and stops recording.  Index: 0 per-round kernels,
  * 1 phase 1, 2 phase 2, 3 phase 3 on the caller's stream, 4 phase 3 of the
  * next block row and column on the look-ahead stream (these overlap index 3
- * in time).  At most 1<<16 launches are recorded per session; more set
- * *overflow to 1. */
-#define BS_PROFILE_PHASES 5
+ * in time), 5 the single kernel of BS_ONE_LAUNCH.  At most 1<<16 launches
+ * are recorded per session; more set *overflow to 1. */
+#define BS_PROFILE_PHASES 6
 typedef struct {
     double ms[BS_PROFILE_PHASES];
     long long launches[BS_PROFILE_PHASES];

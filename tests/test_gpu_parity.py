@@ -47,6 +47,8 @@ SCHEDULES = {
     "t64_serial": bsm.BS_TILE_64 | bsm.BS_NO_LOOKAHEAD,
     "t128_serial": bsm.BS_TILE_128 | bsm.BS_NO_LOOKAHEAD,
     "sym": bsm.BS_SYMMETRIC,
+    "one": bsm.BS_ONE_LAUNCH,
+    "one_sym": bsm.BS_ONE_LAUNCH | bsm.BS_SYMMETRIC,
 }
 # every algorithm: the blocked schedules and both per-round forms
 ALGOS = dict(SCHEDULES, perk=bsm.BS_PERK, perk2=bsm.BS_PERK | bsm.BS_PERK_PAIRED)
@@ -146,7 +148,7 @@ def test_leading_dimension_and_misalignment(n, ld, offset, algo):
 
 @pytest.mark.parametrize("n", [1, 5, 128, 129, 300])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
 def test_upper_only(n, dtype, algo):
     Uq, _ = W.random_bounds(n, 5000 + n, p_known=0.25)
     U0 = W.to_f32(Uq) if dtype == "f32" else Uq
@@ -412,7 +414,7 @@ def test_globule_4096_fp32_blocked_and_per_round(globule4096):
         assert bsm.bs_check_feasible(dev(Ug), dev(Lg)) == expect_flags
 
 
-@pytest.mark.parametrize("sched", ["auto", "t128", "sym"])
+@pytest.mark.parametrize("sched", ["auto", "t128", "sym", "one", "one_sym"])
 def test_batched_chains(sched):
     """Batch of 256 molecules n=512 in one call; every 32nd molecule against the
     oracle, all molecules against a per-molecule GPU call."""
@@ -433,7 +435,7 @@ def test_batched_chains(sched):
 
 @pytest.mark.parametrize("n,B", [(200, 3), (300, 4), (257, 12), (130, 40)])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "sym"])
+@pytest.mark.parametrize("sched", ["auto", "sym", "one"])
 def test_batched_small_molecules(n, B, dtype, sched):
     """Small batches of small molecules: the launches take the strip forms
     (four or two CTAs per tile) or the 256-thread form depending on the
@@ -789,6 +791,11 @@ def test_empty_and_launch_counting():
                          flags=bsm.BS_PERK | bsm.BS_PERK_PAIRED)
     # two rounds per pass: 150 passes, each with its row/column launch
     assert bsm.bs_launch_count() - before == 2 * 150
+    before = bsm.bs_launch_count()
+    bsm.bs_smooth_bounds(dev(W.to_f32(Uq)), dev(W.to_f32(Lq)), flags=bsm.BS_ONE_LAUNCH)
+    # the one-launch form: a single kernel for the whole smoothing
+    assert bsm.bs_launch_count() - before == 1
+    assert bsm.bs_one_launch_cluster() in (8, 16)
     Uq7, Lq7 = W.random_bounds(700, 1, p_bad=0.01)
     before = bsm.bs_launch_count()
     bsm.bs_smooth_bounds(dev(W.to_f32(Uq7)), dev(W.to_f32(Lq7)), flags=bsm.BS_TILE_64)
@@ -808,11 +815,17 @@ def test_profile_records_every_launch():
     p = bsm.bs_profile_end()
     # rounds 0, 1: phase 3 split into the rest (caller's stream) and the next
     # block row and column (look-ahead stream)
-    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 3, 2]
+    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 3, 2, 0]
     assert p["phase3"]["ms"] > 0 and p["phase3_next"]["ms"] > 0
     # 64-wide tiles, few rest tiles: phase 3 of each round but the last is
     # one launch on the caller's stream, beside phase 1 of the next round
     bsm.bs_profile_begin()
     bsm.bs_smooth_bounds(U, L, flags=bsm.BS_TILE_64)
     p = bsm.bs_profile_end()
-    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 5, 5, 5, 0]
+    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 5, 5, 5, 0, 0]
+    # the one-launch form: its single kernel, in its own category
+    bsm.bs_profile_begin()
+    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_ONE_LAUNCH)
+    p = bsm.bs_profile_end()
+    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 0, 0, 0, 0, 1]
+    assert p["one_launch"]["ms"] > 0
