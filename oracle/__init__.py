@@ -59,6 +59,8 @@ def _load():
         lib.oracle_smooth_track_f64.restype = c_int
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = c_int
+        lib.oracle_set_threads.argtypes = [c_int]
+        lib.oracle_set_threads.restype = None
         for name in ("oracle_count_infeasible_f32", "oracle_count_infeasible_i32"):
             f = getattr(lib, name)
             f.argtypes = [vp, vp, i64, i64]
@@ -70,6 +72,11 @@ def _load():
 def threads() -> int:
     """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
     return int(_load().oracle_threads())
+
+
+def set_threads(t: int) -> None:
+    """Use t OpenMP threads from now on (timing only; results are the same)."""
+    _load().oracle_set_threads(int(t))
 
 
 _FN = {np.dtype(np.float32): "oracle_smooth_f32",

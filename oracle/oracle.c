@@ -65,6 +65,15 @@ int oracle_threads(void) {
 #endif
 }
 
+/* Threads for the following calls (timing only: results never depend on it). */
+void oracle_set_threads(int t) {
+#ifdef _OPENMP
+    if (t > 0) omp_set_num_threads(t);
+#else
+    (void)t;
+#endif
+}
+
 /* One implementation per arithmetic type.  T is the stored type, W the type in
  * which a sum or a difference is formed (int64 for int32 storage, so the oracle
  * itself never overflows), and the result of a min or max is always one of the
