@@ -430,6 +430,8 @@ def main():
                     help="skip the ALU issue-rate probes")
     ap.add_argument("--no-symmetric", action="store_true",
                     help="skip the extra timing of the symmetric half-work mode")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the timing of the other benchmark molecules (configs 0-3)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark molecule (one JSON line each) instead")
     ap.add_argument("--oracle-plan", action="store_true",
@@ -654,6 +656,8 @@ def main():
         line["alu_probe_instr_per_clk_per_sm"] = probes
     if not args.no_e2e:
         line["e2e"] = e2e_leg(torch, bsm, U0, L0, args, ws)
+    if not args.no_configs and args.mode == "blocked":
+        line["other_configs"] = configs_leg(torch, bsm, alu_peak_ops, peaks["hbm_gbs"])
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:
         rate, rounds, thr, el = oracle_rate(U0, L0, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -807,6 +811,56 @@ def symmetric_leg(torch, bsm, dU0, dL0, copies, args, general_rate):
             "executed_cell_updates_per_s": executed / (ms * 1e-3),
             "note": "inputs are symmetric; only tiles with I <= J are computed and mirrored, "
                     "so about half of the n^3 cell updates are executed"}
+
+
+def configs_leg(torch, bsm, alu_peak_ops, hbm_gbs):
+    """The other benchmark molecules, timed in the same run: device time of
+    one call (median of 5, each on a fresh copy restored outside the timed
+    events), cell-updates/s and the fraction of the 6-op peak; config 2 also
+    in int32 and in the plain per-round mode (HBM-bound, GB/s of its 16 bytes
+    per cell update)."""
+    from workloads import make_config, to_f32
+    out = {}
+    cases = [("chain256", 0, "f32", 0), ("chain1000", 1, "f32", 0),
+             ("globule4096", 2, "f32", 0), ("globule4096_i32", 2, "i32", 0),
+             ("globule4096_perk", 2, "f32", PERK_FLAGS["perk"]),
+             ("batch256x512", 3, "f32", 0)]
+    cache = {}
+    for name, cfg, dt, flags in cases:
+        if cfg not in cache:
+            cache.clear()
+            cache[cfg] = make_config(cfg)
+        m = cache[cfg]
+        U0, L0 = (to_f32(m["U"]), to_f32(m["L"])) if dt == "f32" else (m["U"], m["L"])
+        dU0, dL0 = torch.from_numpy(U0).cuda(), torch.from_numpy(L0).cuda()
+        U, L = dU0.clone(), dL0.clone()
+        n, batch = m["n"], m.get("batch", 1)
+        times = []
+        for r in range(3 + 5):
+            U.copy_(dU0)
+            L.copy_(dL0)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            if batch > 1:
+                bsm.bs_smooth_bounds_batched(U, L, flags=flags)
+            else:
+                bsm.bs_smooth_bounds(U, L, flags=flags)
+            b.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        rate = batch * float(n) ** 3 / (ms * 1e-3)
+        rec = {"n": n, "batch": batch, "dtype": dt, "ms": ms, "cell_updates_per_s": rate}
+        if flags & PERK_FLAGS["perk"]:
+            gbs = perk_bytes(n, paired=False) * batch / (ms * 1e-3) / 1e9
+            rec.update(hbm_gbs_algorithmic=gbs, hbm_frac=gbs / hbm_gbs)
+        else:
+            rec["fp32_alu_frac"] = rate * OPS_PER_CELL / alu_peak_ops
+        out[name] = rec
+        del dU0, dL0, U, L
+    return out
 
 
 def e2e_leg(torch, bsm, U0, L0, args, ws):
