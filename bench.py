@@ -43,6 +43,8 @@ WORKLOADS = {
     # the small molecules of the benchmark set, for launch lists
     "chain256": dict(config=0, desc="random-walk chain n=256, fp32 U+L, blocked"),
     "chain1000": dict(config=1, desc="random-walk chain n=1000, fp32 U+L, blocked"),
+    # 256 molecules in one batched call: a capture target only (--profile-calls)
+    "batch256x512": dict(config=3, desc="256 random-walk chains n=512, fp32 U+L, batched"),
 }
 
 
@@ -415,11 +417,12 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only run this many smoothing calls of the workload (no timing, "
                          "no JSON line): a short target for ncu captures")
-    ap.add_argument("--mode", choices=["blocked", "perk", "perk2", "upper"], default="blocked",
+    ap.add_argument("--mode", choices=["blocked", "perk", "perk2", "upper", "one"],
+                    default="blocked",
                     help="perk: the per-round reference mode, one round per pass (HBM-bound); "
                          "perk2: its two-rounds-per-pass form; both for their HBM roofline "
-                         "and captures; upper: bs_smooth_upper (U alone), with "
-                         "--profile-calls only (the sweep times it)")
+                         "and captures; upper: bs_smooth_upper (U alone), and one: the "
+                         "one-launch form, with --profile-calls only (the sweep times them)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU-oracle sample length for cpu_baseline")
     ap.add_argument("--ref-rounds", type=int, default=48,
@@ -443,8 +446,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.mode == "upper" and args.profile_calls <= 0:
-        ap.error("--mode upper is a capture target: use it with --profile-calls")
+    if args.mode in ("upper", "one") and args.profile_calls <= 0:
+        ap.error("--mode %s is a capture target: use it with --profile-calls" % args.mode)
+    if args.workload == "batch256x512" and args.profile_calls <= 0:
+        ap.error("the batch workload is a capture target: use it with --profile-calls")
 
     ws, rank, local = dist_setup()
     if args.oracle_plan:
@@ -472,23 +477,25 @@ def main():
     dU0 = torch.from_numpy(U0).cuda()
     dL0 = torch.from_numpy(L0).cuda()
     stream = torch.cuda.current_stream()
-    ncopies = min(args.steps, 32)
-    copies = [(dU0.clone(), dL0.clone()) for _ in range(ncopies)]
     wU, wL = dU0.clone(), dL0.clone()
 
-    flags = PERK_FLAGS.get(args.mode, 0)
+    flags = PERK_FLAGS.get(args.mode, 0) | (bsm.BS_ONE_LAUNCH if args.mode == "one" else 0)
     if args.profile_calls > 0:
         for _ in range(args.profile_calls):
             wU.copy_(dU0)
             wL.copy_(dL0)
             if args.mode == "upper":
                 bsm.bs_smooth_upper(wU)
+            elif wU.dim() == 3:
+                bsm.bs_smooth_bounds_batched(wU, wL, flags=flags)
             else:
                 bsm.bs_smooth_bounds(wU, wL, flags=flags)
         torch.cuda.synchronize()
         print("profile calls done: %d x %s, n=%d" % (args.profile_calls, args.mode, n))
         return 0
 
+    ncopies = min(args.steps, 32)
+    copies = [(dU0.clone(), dL0.clone()) for _ in range(ncopies)]
     # warm-up on a scratch copy
     for _ in range(args.warmup):
         wU.copy_(dU0)

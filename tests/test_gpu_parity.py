@@ -87,7 +87,7 @@ def test_blocked_matches_oracle(n, dtype, sched):
 
 @pytest.mark.parametrize("n", [1, 2, 5, 63, 64, 65, 127, 129, 257, 300, 513])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "t64_serial", "t128_serial"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "t64_serial", "t128_serial", "one"])
 def test_symmetric_mode_matches_oracle(n, dtype, sched):
     """Half the tiles computed and mirrored: bit-identical to the oracle."""
     Uq, Lq = W.random_bounds(n, 2500 + n, p_known=0.2, p_bad=0.02)
@@ -99,7 +99,7 @@ def test_symmetric_mode_matches_oracle(n, dtype, sched):
 
 
 @pytest.mark.parametrize("n", [65, 300])
-@pytest.mark.parametrize("algo", ["t64", "t128"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "one"])
 def test_symmetric_upper_only(n, algo):
     Uq, _ = W.random_bounds(n, 5500 + n, p_known=0.25)
     Uo = oracle.smooth_upper(Uq)
@@ -109,7 +109,7 @@ def test_symmetric_upper_only(n, algo):
 
 @pytest.mark.parametrize("n", [997, 1001, 1003])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "sym", "t128"])
+@pytest.mark.parametrize("sched", ["auto", "sym", "t128", "one"])
 def test_blocked_tails_near_1000(n, dtype, sched):
     """Sizes around the n = 1000 chain with ragged last tiles (37, 41, 43 rows
     of 64; 101, 105, 107 of 128), a padded leading dimension n + 5 with
@@ -133,7 +133,7 @@ def test_blocked_asymmetric(n, sched):
 
 @pytest.mark.parametrize("n,ld,offset", [(130, 140, 0), (130, 133, 0), (257, 260, 1),
                                          (97, 101, 3), (200, 200, 1)])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
 def test_leading_dimension_and_misalignment(n, ld, offset, algo):
     """ld > n keeps the padding untouched; ld % 4 != 0 or a base not 16-byte
     aligned takes the scalar-IO instantiation with identical results."""
@@ -304,7 +304,7 @@ def edge_cases():
 
 
 @pytest.mark.parametrize("case", sorted(edge_cases()))
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
 def test_edge_cases(case, algo):
     Uq, Lq = edge_cases()[case]
     flags = ALGOS[algo]
@@ -318,7 +318,7 @@ def test_edge_cases(case, algo):
         np.testing.assert_array_equal(Uo, Uq.astype(Uo.dtype) / (1 if Uo.dtype == np.int32 else 1024))
 
 
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
 def test_infinite_upper_bounds(algo):
     """fp32 U may be +inf for unknown pairs; inf + x = inf never wins."""
     Uq, Lq = W.random_bounds(200, 9500, p_known=0.1, p_bad=0.01)
@@ -338,7 +338,8 @@ def test_infinite_upper_bounds(algo):
     assert ok and same_bits(Ug, Uo) and same_bits(Lg, Lo)
 
 
-def test_batch_beyond_grid_limit():
+@pytest.mark.parametrize("flags", [0, bsm.BS_ONE_LAUNCH])
+def test_batch_beyond_grid_limit(flags):
     """More molecules than a grid's z dimension holds (65535): launches are
     split in chunks; every molecule still matches a single-molecule call."""
     t = torch()
@@ -349,7 +350,7 @@ def test_batch_beyond_grid_limit():
     Uq = np.stack([base[p][0] for p in pick])
     Lq = np.stack([base[p][1] for p in pick])
     U, L = dev(W.to_f32(Uq)), dev(W.to_f32(Lq))
-    bsm.bs_smooth_bounds_batched(U, L)
+    bsm.bs_smooth_bounds_batched(U, L, flags=flags)
     Ug, Lg = host(U), host(L)
     ref = [oracle.smooth(W.to_f32(u), W.to_f32(l)) for u, l in base]
     for b in (0, 1, 65534, 65535, 65536, B - 1) + tuple(rng.integers(0, B, 50)):
@@ -363,10 +364,11 @@ def test_batch_beyond_grid_limit():
 
 
 @pytest.mark.parametrize("idx", [0, 1])
-@pytest.mark.parametrize("algo", ["blocked", "perk", "symmetric"])
+@pytest.mark.parametrize("algo", ["blocked", "perk", "symmetric", "one"])
 def test_chain_configs(idx, algo):
     m = W.make_config(idx)
-    flags = {"blocked": 0, "perk": bsm.BS_PERK, "symmetric": bsm.BS_SYMMETRIC}[algo]
+    flags = {"blocked": 0, "perk": bsm.BS_PERK, "symmetric": bsm.BS_SYMMETRIC,
+             "one": bsm.BS_ONE_LAUNCH}[algo]
     for U0, L0 in ((W.to_f32(m["U"]), W.to_f32(m["L"])), (m["U"], m["L"])):
         Uo, Lo = oracle.smooth(U0, L0)
         Ug, Lg, ok = gpu_bounds(U0, L0, flags)
@@ -486,7 +488,8 @@ def test_batched_per_round_and_strided():
     for b, (uq, lq) in enumerate(Us):
         Ubuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(uq))
         Lbuf[b * stride: b * stride + n * ld].view(n, ld)[:, :n] = dev(W.to_f32(lq))
-    for flags in (bsm.BS_PERK, bsm.BS_PERK | bsm.BS_PERK_PAIRED, 0, bsm.BS_TILE_128):
+    for flags in (bsm.BS_PERK, bsm.BS_PERK | bsm.BS_PERK_PAIRED, 0, bsm.BS_TILE_128,
+                  bsm.BS_ONE_LAUNCH):
         U, L = Ubuf.clone(), Lbuf.clone()
         bsm.bs_smooth_bounds_batched(U, L, n, ld, stride, B, None, bsm.BS_FP32 | flags)
         Uh, Lh = host(U), host(L)
@@ -691,7 +694,7 @@ def test_symmetric_flag_checks():
 
 
 @pytest.mark.parametrize("sched,n", [("t64", 300), ("t128", 300), ("sym", 300), ("perk", 300),
-                                     ("auto", 1000)])
+                                     ("auto", 1000), ("one", 300)])
 def test_cuda_graph_capture_and_replay(sched, n):
     """A smoothing captured into a CUDA graph (look-ahead fork and join
     included) replays to the same result, twice, on fresh inputs.  n = 1000
