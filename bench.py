@@ -160,7 +160,7 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, sm_max_mhz=2070.0, source="fallback")
 
 
-KERNEL_SOURCES = ("phase3.cu", "pairops.cuh", "bs_tile.cuh", "bs_types.cuh")
+KERNEL_SOURCES = ("phase3.cu", "p3_tile.cuh", "pairops.cuh", "bs_tile.cuh", "bs_types.cuh")
 
 
 def kernel_hash():

@@ -285,7 +285,69 @@ __device__ __forceinline__ void p3_update_tile(T* __restrict__ U, T* __restrict_
                         PairOps<T>::lower(l[r][q], a[r], al[r], b[q], bl[q]);
             }
         };
-        if constexpr (HAS_L || FB == FB_SMALL) {
+        // 128-wide tiles with L: the chunk's upper-bound updates first, then its
+        // lower-bound updates, each pass loading only the operands it uses.
+        // The upper pass needs half the registers of the fused step, so it is
+        // unrolled over the whole chunk (every shared-memory address an
+        // immediate), and the lower pass is unrolled four times (int32: two).
+        // Measured on the GB300 against the fused step: n = 16384 fp32
+        // 816.8 -> 778.5 ms, n = 4096 int32 14.09 -> 13.79 ms.  The operands
+        // a and b are loaded twice per chunk; shared memory is not the limit.
+        auto stepU = [&](int kk) {
+            P a[S::TM], b[S::TN];
+#pragma unroll
+            for (int r = 0; r < S::TM; ++r) a[r] = LD::ld2(AU + (r0 + r) * AST + kk);
+            const int bo = (kk >> 1) * (2 * FB);
+#pragma unroll
+            for (int h = 0; h < S::QUADS; ++h) {
+                const int jb = bo + (h * S::QSTRIDE + cq) * 2;
+                LD::ld4(BU + jb, b[h * 4 + 0], b[h * 4 + 1]);
+                LD::ld4(BU + jb + 4, b[h * 4 + 2], b[h * 4 + 3]);
+            }
+#pragma unroll
+            for (int r = 0; r < S::TM; ++r)
+#pragma unroll
+                for (int q = 0; q < S::TN; ++q) PairOps<T>::upper(u[r][q], a[r], b[q]);
+        };
+        auto stepL = [&](int kk) {
+            P a[S::TM], al[S::TM], b[S::TN], bl[S::TN];
+#pragma unroll
+            for (int r = 0; r < S::TM; ++r) {
+                a[r] = LD::ld2(AU + (r0 + r) * AST + kk);
+                al[r] = LD::ld2(AL + (r0 + r) * AST + kk);
+            }
+            const int bo = (kk >> 1) * (2 * FB);
+#pragma unroll
+            for (int h = 0; h < S::QUADS; ++h) {
+                const int jb = bo + (h * S::QSTRIDE + cq) * 2;
+                LD::ld4(BU + jb, b[h * 4 + 0], b[h * 4 + 1]);
+                LD::ld4(BU + jb + 4, b[h * 4 + 2], b[h * 4 + 3]);
+                LD::ld4(BL + jb, bl[h * 4 + 0], bl[h * 4 + 1]);
+                LD::ld4(BL + jb + 4, bl[h * 4 + 2], bl[h * 4 + 3]);
+            }
+            if (NEG) {
+#pragma unroll
+                for (int r = 0; r < S::TM; ++r) a[r] = LD::neg(a[r]);
+#pragma unroll
+                for (int q = 0; q < S::TN; ++q) b[q] = LD::neg(b[q]);
+            }
+#pragma unroll
+            for (int r = 0; r < S::TM; ++r)
+#pragma unroll
+                for (int q = 0; q < S::TN; ++q)
+                    PairOps<T>::lower(l[r][q], a[r], al[r], b[q], bl[q]);
+        };
+        if constexpr (HAS_L && FB == FB_LARGE) {
+#pragma unroll
+            for (int kk = 0; kk < BK; kk += 2) stepU(kk);
+            if constexpr (NEG) {
+#pragma unroll 2
+                for (int kk = 0; kk < BK; kk += 2) stepL(kk);
+            } else {
+#pragma unroll 4
+                for (int kk = 0; kk < BK; kk += 2) stepL(kk);
+            }
+        } else if constexpr (HAS_L || FB == FB_SMALL) {
 #pragma unroll 1
             for (int kk = 0; kk < BK; kk += 2) step(kk);
         } else {
