@@ -59,13 +59,15 @@ def make_workload(name):
 
 def tile_size(n, flags=0, batch=1, upper=False):
     """Tile size the library picks (mirrors its rule; forced by the tile bits;
-    flags bit 0 set: int32; upper: bs_smooth_upper, U alone)."""
+    flags bit 0 set: int32, bit 8 set: symmetric; upper: bs_smooth_upper,
+    U alone)."""
     if flags & (1 << 5):
         return 64
     if flags & (1 << 6):
         return 128
     nb = (n + 127) // 128
-    return 128 if (nb - 1) ** 2 * batch >= (768 if flags & 1 or upper else 3000) else 64
+    from_ = 768 if flags & 1 or upper else (3000 if flags & (1 << 8) else 900)
+    return 128 if (nb - 1) ** 2 * batch >= from_ else 64
 
 
 def phase_cells(n, fb, sym=False):
@@ -811,7 +813,7 @@ def symmetric_leg(torch, bsm, dU0, dL0, copies, args, general_rate):
         times.append(a.elapsed_time(b))
     ms = statistics.median(times)
     rate = float(n) ** 3 / (ms * 1e-3)
-    executed = float(sum(phase_cells(n, tile_size(n), sym=True)))
+    executed = float(sum(phase_cells(n, tile_size(n, flags=1 << 8), sym=True)))
     return {"ms_per_step": ms, "value": rate, "unit": UNIT + " (n^3 / time, same output)",
             "speedup_vs_general": rate / general_rate,
             "executed_cell_updates": executed,
