@@ -72,6 +72,35 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
     T* AL = HAS_L ? BU + SM::B_ELEMS : nullptr;
     T* BL = HAS_L ? AL + SM::A_ELEMS : nullptr;
     const int kc = c * BK;
+    if (vec && mi == FB && mj == FB && kc + BK <= mk) {
+        // Whole chunk inside the matrix: fixed per-thread bases, constant
+        // strides, no bounds tests.  Column panel: thread t copies 16-byte
+        // piece t % QP of rows t / QP + RSTEP i; row panel: column t % FB of
+        // middle atoms t / FB + KSTEP i (KSTEP even keeps its pair slot).
+        constexpr int QP = BK / 4, RSTEP = NT / QP, KSTEP = NT / FB;
+        static_assert(NT % QP == 0 && FB % RSTEP == 0, "column-panel passes");
+        static_assert(NT % FB == 0 && KSTEP % 2 == 0 && BK % KSTEP == 0, "row-panel passes");
+        const int r = threadIdx.x / QP, kq = (threadIdx.x % QP) * 4;
+        const T* gu = U + (size_t)(oi + r) * ld + ok + kc + kq;
+        const T* gl = HAS_L ? L + (size_t)(oi + r) * ld + ok + kc + kq : nullptr;
+        const size_t rstride = (size_t)RSTEP * ld;
+#pragma unroll
+        for (int i = 0; i < FB / RSTEP; ++i) {
+            cp_async16(AU + (r + i * RSTEP) * AST + kq, gu + i * rstride);
+            if (HAS_L) cp_async16(AL + (r + i * RSTEP) * AST + kq, gl + i * rstride);
+        }
+        const int j = threadIdx.x % FB, k0 = threadIdx.x / FB;
+        const int d0 = (k0 >> 1) * (2 * FB) + j * 2 + (k0 & 1);
+        const T* hu = U + (size_t)(ok + kc + k0) * ld + oj + j;
+        const T* hl = HAS_L ? L + (size_t)(ok + kc + k0) * ld + oj + j : nullptr;
+        const size_t kstride = (size_t)KSTEP * ld;
+#pragma unroll
+        for (int i = 0; i < BK / KSTEP; ++i) {
+            cp_async4(BU + d0 + i * KSTEP * FB, hu + i * kstride);
+            if (HAS_L) cp_async4(BL + d0 + i * KSTEP * FB, hl + i * kstride);
+        }
+        return;
+    }
     // column panel: FB rows x BK middle atoms, [i][k]
     if (vec) {
         for (int p = threadIdx.x; p < FB * (BK / 4); p += NT) {
