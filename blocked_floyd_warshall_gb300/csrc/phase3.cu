@@ -6,8 +6,11 @@
 
 namespace bs {
 
+// Occupancy floors: two CTAs per SM for the upper bound alone on 128-wide
+// tiles, four for the 8 x 4 form of 64-wide tiles (128 registers each).
 template <class T, bool HAS_L, int FB, bool WIDE>
-__global__ void __launch_bounds__(P3S<FB, WIDE>::NT, (!HAS_L && FB == FB_LARGE) ? 2 : 0)
+__global__ void __launch_bounds__(P3S<FB, WIDE>::NT,
+                                  (!HAS_L && FB == FB_LARGE) ? 2 : (FB == FB_SMALL && !WIDE ? 4 : 0))
 k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int K,
          int part, bool vec, bool sym) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
