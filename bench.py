@@ -59,13 +59,13 @@ def make_workload(name):
 
 def tile_size(n, flags=0, batch=1, upper=False):
     """Tile size the library picks (mirrors its rule; forced by the tile bits;
-    flags bit 0 set: int32; upper: bs_smooth_upper, U alone)."""
+    upper: bs_smooth_upper, U alone)."""
     if flags & (1 << 5):
         return 64
     if flags & (1 << 6):
         return 128
     nb = (n + 127) // 128
-    return 128 if (nb - 1) ** 2 * batch >= (768 if flags & 1 or upper else 3000) else 64
+    return 128 if (nb - 1) ** 2 * batch >= (768 if upper else 9000) else 64
 
 
 def phase_cells(n, fb, sym=False):

@@ -114,22 +114,22 @@ void release_side(DeviceState* d, const SideCtx& c) {
 }
 
 // Tile size for the blocked schedule: 64 x 64 unless a block round's phase 3
-// at 128 holds at least 3000 tiles over the batch (single matrices from
-// n = 7041 on), then 128 x 128.  Measured on the GB300 (ms, 64 against 128):
-// n = 3000 5.76 / 7.18, n = 4096 13.40 / 13.23, n = 5000 24.5 / 25.5,
-// n = 6000 40.3 / 41.2, n = 7000 64.0 / 63.9, 256 molecules of n = 512
-// 6.33 / 6.45, 64 of n = 1024 12.46 / 12.40, 128 of n = 768 10.52 / 10.60;
-// n = 16384 778 / 759.  The smaller tiles spread further over the SMs and
-// keep the serial phase 1 short; the larger halve the block rounds.
-// int32 takes 128 from 768 tiles (n = 3000: 6.10 / 7.10; n = 4096: 14.16 /
-// 13.67), and so does the upper bound alone, whose 128-wide form has its k
-// loop unrolled (n = 4096: 5.3 against 5.8 ms; n = 6000: 15.7 against 17.7
-// ms; n = 3000, 529 tiles: 3.3 against 2.6 ms).
+// at 128 holds at least 9000 tiles over the batch (single matrices from
+// n = 12161 on), then 128 x 128; fp32 and int32 alike.  Measured on the
+// GB300 (ms, 64 against 128): fp32 n = 4096 12.92 / 13.22, n = 6000 39.6 /
+// 41.1, n = 8192 97.1 / 98.6, n = 10000 178.8 / 185.7, n = 12288 324.7 /
+// 324.6, n = 16384 766.8 / 758.7; 64 molecules of n = 1024 12.24 / 12.40;
+// int32 n = 3000 5.91 / 6.46, n = 6000 41.8 / 42.8, n = 8192 102.6 / 102.6,
+// n = 16384 810.4 / 793.1.  The smaller tiles spread further over the SMs
+// and keep the serial phase 1 short; the larger halve the block rounds.
+// The upper bound alone takes 128 from 768 tiles: its 128-wide form has its
+// k loop unrolled (n = 4096: 5.3 against 5.8 ms; n = 6000: 15.7 against
+// 17.7 ms; n = 3000, 529 tiles: 3.3 against 2.6 ms).
 int choose_tile(int n, int batch, int mode, bool bounds) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
     if (mode & BS_TILE_128) return bs::FB_LARGE;
     const double nb = (double)((n + bs::FB_LARGE - 1) / bs::FB_LARGE);
-    const double from = (mode & BS_DTYPE_MASK) == BS_INT32_Q10 || !bounds ? 768.0 : 3000.0;
+    const double from = bounds ? 9000.0 : 768.0;
     return (nb - 1) * (nb - 1) * batch >= from ? bs::FB_LARGE : bs::FB_SMALL;
 }
 

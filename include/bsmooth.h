@@ -95,9 +95,9 @@ enum {
     BS_VALIDATE = 1 << 4,     /* check the preconditions first (synchronises) */
     /* Blocked-mode schedule knobs; every setting gives identical results. */
     BS_TILE_64 = 1 << 5,      /* force 64 x 64 tiles (default: 128 once a block
-                                 round's phase 3 holds at least 3000 tiles of
-                                 128 over the batch, 768 for int32 or for the
-                                 upper bound alone, else 64) */
+                                 round's phase 3 holds at least 9000 tiles of
+                                 128 over the batch, 768 for the upper bound
+                                 alone, else 64) */
     BS_TILE_128 = 1 << 6,     /* force 128 x 128 tiles; both tile bits: BS_ERR_ARG */
     BS_NO_LOOKAHEAD = 1 << 7, /* run the three phases of each block round in
                                  sequence on `stream` only (see below) */

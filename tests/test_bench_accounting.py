@@ -66,12 +66,13 @@ def test_merged_lookahead_rule():
 
 
 def test_tile_rule_matches_documented_thresholds():
-    """64-wide tiles unless a 128-wide phase 3 holds >= 3000 tiles over the
-    batch (768 for int32 or for the upper bound alone)."""
+    """64-wide tiles unless a 128-wide phase 3 holds >= 9000 tiles over the
+    batch, fp32 and int32 alike (768 for the upper bound alone)."""
     assert bench.tile_size(4096) == 64
+    assert bench.tile_size(10000) == 64
     assert bench.tile_size(16384) == 128
-    assert bench.tile_size(7040) == 64 and bench.tile_size(7041) == 128   # 54^2, 55^2 tiles
-    assert bench.tile_size(4096, flags=1) == 128              # int32: 31^2 = 961 >= 768
+    assert bench.tile_size(12160) == 64 and bench.tile_size(12161) == 128   # 94^2, 95^2 tiles
+    assert bench.tile_size(4096, flags=1) == 64 and bench.tile_size(16384, flags=1) == 128
     assert bench.tile_size(512, batch=256) == 64               # 9 x 256 = 2304
     assert bench.tile_size(4096, upper=True) == 128            # U alone: 961 >= 768
     assert bench.tile_size(3000, upper=True) == 64             # 23^2 = 529
