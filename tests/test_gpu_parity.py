@@ -723,7 +723,7 @@ def test_cuda_graph_capture_and_replay(sched, n):
         assert same_bits(host(U), Uo) and same_bits(host(L), Lo)
 
 
-@pytest.mark.parametrize("n", [700, 2000])
+@pytest.mark.parametrize("n", [700, 1000, 2000])
 def test_concurrent_calls_on_own_streams(n):
     """Three host threads smooth three molecules at once, each on its own
     stream (each call takes its own look-ahead stream and events); then work
