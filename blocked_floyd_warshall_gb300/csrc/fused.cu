@@ -4,8 +4,9 @@
 // atoms are sequential, only the pairs of one round run in parallel; here a
 // "round" is a block round of 64 middle atoms).
 //
-// Each CTA of a cluster of C (16 where the device allows clusters that large,
-// else 8) runs every block round K:
+// Each CTA of a cluster of C runs every block round K (C = 16 where the
+// device allows clusters that large, else 8, for a single molecule and small
+// batches; 4 or 8 for larger batches, see pick_cluster):
 //   phase 2: the panel tiles of round K, t = rank, rank + C, ...;
 //   cluster barrier;
 //   phase 3: rank 0 updates tile (K+1,K+1) and at once closes it (phase 1 of
@@ -104,43 +105,62 @@ k_fused(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
     }
 }
 
-int g_cluster[64];   // per device: CTAs per cluster (0: not set up)
+// Per device: the largest cluster size that can be placed (16 where the
+// device allows clusters that large, else 8) and how many clusters of it, and
+// of 4 CTAs, are resident at once (0: not set up).
+struct FzDevice {
+    int big = 0;
+    int active_big = 0;
+    int active4 = 0;
+};
+FzDevice g_fz[64];
 
 template <class T, bool HAS_L>
-cudaError_t setup_t(int* cluster) {
+int active_clusters(int c) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c, 1, 1);
+    cfg.blockDim = dim3(FZ_NT);
+    cfg.dynamicSmemBytes = fz_smem<T, HAS_L>();
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, k_fused<T, HAS_L>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return active;
+}
+
+template <class T, bool HAS_L>
+cudaError_t setup_t(FzDevice* d) {
     auto kernel = k_fused<T, HAS_L>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)fz_smem<T, HAS_L>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    if (*cluster) return cudaSuccess;
-    // the largest cluster the device can hold at least one of: 16, else 8
-    for (int c : {16, 8}) {
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = c;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(c, 1, 1);
-        cfg.blockDim = dim3(FZ_NT);
-        cfg.dynamicSmemBytes = fz_smem<T, HAS_L>();
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int active = 0;
-        e = cudaOccupancyMaxActiveClusters(&active, kernel, &cfg);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            continue;
-        }
-        if (active > 0) {
-            *cluster = c;
-            return cudaSuccess;
-        }
-    }
-    *cluster = 8;
+    if (e != cudaSuccess || d->big) return e;
+    const int a16 = active_clusters<T, HAS_L>(16);
+    d->big = a16 > 0 ? 16 : 8;
+    d->active_big = a16 > 0 ? a16 : active_clusters<T, HAS_L>(8);
+    d->active4 = active_clusters<T, HAS_L>(4);
     return cudaSuccess;
+}
+
+// CTAs per cluster for a launch of `batch` molecules.  While every molecule's
+// cluster of the largest size is resident at once, the largest (more CTAs
+// per molecule); then 4 while every molecule's cluster of 4 is (more
+// clusters fit: measured, 32 molecules of n = 256: 0.58 ms with 16, 0.28
+// with 8, 0.24 with 4); beyond, 8 (256 molecules of n = 512: 11.6 ms with 16,
+// 8.8 with 8, 8.9 with 4).
+int pick_cluster(const FzDevice& d, int batch) {
+    if (batch <= d.active_big) return d.big;
+    if (batch <= d.active4) return 4;
+    return 8;
 }
 
 template <class T, bool HAS_L>
@@ -180,7 +200,7 @@ cudaError_t fused_setup(bool is_int) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int* c = &g_cluster[dev];
+    FzDevice* c = &g_fz[dev];
     if (is_int) {
         e = setup_t<int, true>(c);
         if (e == cudaSuccess) e = setup_t<int, false>(c);
@@ -195,8 +215,8 @@ cudaError_t launch_fused(bool is_int, const Mats& m, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || g_cluster[dev] == 0) return cudaErrorInitializationError;
-    const int c = g_cluster[dev];
+    if (dev < 0 || dev >= 64 || g_fz[dev].big == 0) return cudaErrorInitializationError;
+    const int c = pick_cluster(g_fz[dev], m.batch);
     if (is_int) return m.L ? fused_t<int, true>(m, c, s) : fused_t<int, false>(m, c, s);
     return m.L ? fused_t<float, true>(m, c, s) : fused_t<float, false>(m, c, s);
 }
@@ -204,7 +224,7 @@ cudaError_t launch_fused(bool is_int, const Mats& m, cudaStream_t s) {
 int fused_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    return g_cluster[dev];
+    return g_fz[dev].big;
 }
 
 }  // namespace bs

@@ -106,11 +106,13 @@ enum {
                                  matrix (half the memory traffic), each round
                                  exactly as alone; without BS_PERK: BS_ERR_ARG */
     BS_ONE_LAUNCH = 1 << 11,  /* blocked mode in a single kernel launch: one
-                                 thread-block cluster (16 CTAs where the device
-                                 allows, else 8) per molecule, 64 x 64 tiles,
-                                 the phases of each block round separated by
-                                 cluster barriers only; same results.  Meant
-                                 for batches of small molecules.  With BS_PERK,
+                                 thread-block cluster per molecule (16 CTAs
+                                 where the device allows, else 8, while every
+                                 molecule's cluster fits at once; 4 or 8 for
+                                 larger batches), 64 x 64 tiles, the phases of
+                                 each block round separated by cluster
+                                 barriers only; same results.  Meant for
+                                 batches of small molecules.  With BS_PERK,
                                  BS_TILE_128 or BS_NO_LOOKAHEAD: BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the
@@ -187,8 +189,10 @@ bs_status bs_check_feasible_noalloc(const void *U, const void *L, int n, int ld,
 /* Number of kernels this library has launched since it was loaded. */
 long long bs_launch_count(void);
 
-/* CTAs per thread-block cluster of BS_ONE_LAUNCH on the current device (16 or
- * 8), or 0 before the library's first smoothing call on it. */
+/* CTAs per thread-block cluster of BS_ONE_LAUNCH for a single molecule on the
+ * current device (16 or 8), or 0 before the library's first smoothing call on
+ * it.  Batches larger than the number of such clusters resident at once use
+ * clusters of 4 or 8. */
 int bs_one_launch_cluster(void);
 
 /* Per-phase device time.  After bs_profile_begin(), every smoothing call
