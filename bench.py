@@ -825,13 +825,14 @@ def configs_leg(torch, bsm, alu_peak_ops, hbm_gbs):
     one call (median of 5, each on a fresh copy restored outside the timed
     events), cell-updates/s and the fraction of the 6-op peak; config 2 also
     in int32 and in the plain per-round mode (HBM-bound, GB/s of its 16 bytes
-    per cell update)."""
+    per cell update), and config 3 also in the one-launch form."""
     from workloads import make_config, to_f32
     out = {}
     cases = [("chain256", 0, "f32", 0), ("chain1000", 1, "f32", 0),
              ("globule4096", 2, "f32", 0), ("globule4096_i32", 2, "i32", 0),
              ("globule4096_perk", 2, "f32", PERK_FLAGS["perk"]),
-             ("batch256x512", 3, "f32", 0)]
+             ("batch256x512", 3, "f32", 0),
+             ("batch256x512_one_launch", 3, "f32", 1 << 11)]
     cache = {}
     for name, cfg, dt, flags in cases:
         if cfg not in cache:
