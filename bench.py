@@ -376,6 +376,14 @@ def oracle_plan(args):
 # ------------------------------------------------------------------ main
 
 
+def bench_config(wl, n, mode, ws):
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": wl["desc"], "n": n, "batch": 1, "mode": mode,
+            "parallelism": "replicas" if ws > 1 else "single",
+            "l2": "inputs larger than L2: each step smooths its own resident "
+                  "2 x %d MiB copy" % (n * n * 4 >> 20)}
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
@@ -397,7 +405,7 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl["desc"], "n": n, "batch": 1},
+        "config": bench_config(wl, n, "blocked", ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
                          "sample": "each step: rounds 0..%d of the n=%d workload "
                                    "(%d x n^2 cell updates)" % (per_step - 1, n, per_step)},
@@ -589,10 +597,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl["desc"], "n": n, "batch": 1, "mode": args.mode,
-                   "parallelism": "replicas" if ws > 1 else "single",
-                   "l2": "inputs larger than L2: each step smooths its own resident "
-                         "2 x %d MiB copy" % (n * n * 4 >> 20)},
+        "config": bench_config(wl, n, args.mode, ws),
         "fp32_alu_frac": value / ws * OPS_PER_CELL / alu_peak_ops,
         "fp32_alu_peak_basis": "%d SMs x %d lanes x %.0f MHz (%s max SM clock)" % (
             sms, FP32_LANES_PER_SM, peaks["sm_max_mhz"], peaks["source"]),
