@@ -425,12 +425,13 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only run this many smoothing calls of the workload (no timing, "
                          "no JSON line): a short target for ncu captures")
-    ap.add_argument("--mode", choices=["blocked", "perk", "perk2", "upper", "one"],
+    ap.add_argument("--mode", choices=["blocked", "perk", "perk2", "upper", "one", "sym"],
                     default="blocked",
                     help="perk: the per-round reference mode, one round per pass (HBM-bound); "
                          "perk2: its two-rounds-per-pass form; both for their HBM roofline "
-                         "and captures; upper: bs_smooth_upper (U alone), and one: the "
-                         "one-launch form, with --profile-calls only (the sweep times them)")
+                         "and captures; upper: bs_smooth_upper (U alone), one: the "
+                         "one-launch form, and sym: the symmetric half-work mode, with "
+                         "--profile-calls only (the sweep times them)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU-oracle sample length for cpu_baseline")
     ap.add_argument("--ref-rounds", type=int, default=48,
@@ -454,7 +455,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.mode in ("upper", "one") and args.profile_calls <= 0:
+    if args.mode in ("upper", "one", "sym") and args.profile_calls <= 0:
         ap.error("--mode %s is a capture target: use it with --profile-calls" % args.mode)
     if args.workload == "batch256x512" and args.profile_calls <= 0:
         ap.error("the batch workload is a capture target: use it with --profile-calls")
@@ -487,7 +488,8 @@ def main():
     stream = torch.cuda.current_stream()
     wU, wL = dU0.clone(), dL0.clone()
 
-    flags = PERK_FLAGS.get(args.mode, 0) | (bsm.BS_ONE_LAUNCH if args.mode == "one" else 0)
+    flags = PERK_FLAGS.get(args.mode, 0) | (bsm.BS_ONE_LAUNCH if args.mode == "one" else 0) \
+        | (bsm.BS_SYMMETRIC if args.mode == "sym" else 0)
     if args.profile_calls > 0:
         for _ in range(args.profile_calls):
             wU.copy_(dU0)
