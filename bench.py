@@ -432,6 +432,9 @@ def main():
                          "and captures; upper: bs_smooth_upper (U alone), one: the "
                          "one-launch form, and sym: the symmetric half-work mode, with "
                          "--profile-calls only (the sweep times them)")
+    ap.add_argument("--tile", choices=["auto", "64", "128"], default="auto",
+                    help="force the tile size of the blocked schedule (captures of one "
+                         "kernel form; the default line uses the library's own choice)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU-oracle sample length for cpu_baseline")
     ap.add_argument("--ref-rounds", type=int, default=48,
@@ -489,7 +492,8 @@ def main():
     wU, wL = dU0.clone(), dL0.clone()
 
     flags = PERK_FLAGS.get(args.mode, 0) | (bsm.BS_ONE_LAUNCH if args.mode == "one" else 0) \
-        | (bsm.BS_SYMMETRIC if args.mode == "sym" else 0)
+        | (bsm.BS_SYMMETRIC if args.mode == "sym" else 0) \
+        | {"auto": 0, "64": bsm.BS_TILE_64, "128": bsm.BS_TILE_128}[args.tile]
     if args.profile_calls > 0:
         for _ in range(args.profile_calls):
             wU.copy_(dU0)
@@ -578,7 +582,7 @@ def main():
     # phase 3 on the caller's stream (the rest of each block round, and the
     # last round whole): these launches never overlap one another
     p3 = prof["phase3"]
-    fb = tile_size(n)
+    fb = tile_size(n, flags)
     p3_cells_step = phase_cells(n, fb)[2]
     main_cells_step = p3_cells_step - (next_cells(n, fb) if prof["phase3_next"]["launches"] else 0)
     if merged_lookahead(n, fb, 1, sms):

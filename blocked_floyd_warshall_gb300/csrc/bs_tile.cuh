@@ -43,6 +43,7 @@ template <> struct El<int> {
 template <int FB_, int TM_, int TN_>
 struct Shape {
     static constexpr int FB = FB_;
+    static constexpr int COLS = FB_;                // columns of the block a CTA covers
     static constexpr int TM = TM_;
     static constexpr int TN = TN_;
     static constexpr int QUADS = TN / 4;
@@ -111,30 +112,54 @@ __device__ __forceinline__ void store_tile(const T (&x)[S::TM][S::TN], T* M, siz
     }
 }
 
-// Store the transpose of the thread's cells: cell (i, j) of an mr x mc tile
-// goes to MT[j*ld + i], MT being the origin of the mirrored tile.  For a fixed
-// column the thread's rows are consecutive elements (one 32-byte sector for
-// 8 rows).
-template <class S, class T>
-__device__ __forceinline__ void store_tile_t(const T (&x)[S::TM][S::TN], T* MT, size_t ld, int mr,
-                                             int mc, bool vec) {
+// Store the transpose of the thread's cells of U (and of L if HAS_L): cell
+// (i, j) of an mr x mc tile goes to MU[j*ld + i] (and ML[j*ld + i]), MU and
+// ML being the origins of the mirrored tiles.  The cells pass through shared
+// memory (`buf`: (1 + HAS_L) x S::FB x (S::FB + 4) elements, free when called;
+// every thread of the CTA calls it): each thread writes its cells
+// transposed, 4 rows of a column per 16-byte store, and then each warp copies
+// whole rows of the mirrored tiles out, so that the global stores are
+// coalesced (written from registers directly, every 16-byte store of a warp
+// went to a different row).  Both matrices are staged before the one
+// barrier, so no cell stays in a register across it.  Ends with a barrier,
+// so `buf` is free again.
+template <class S, bool HAS_L, class T>
+__device__ __forceinline__ void store_tile_t(const T (&u)[S::TM][S::TN], const T (&l)[S::TM][S::TN],
+                                             T* MU, T* ML, size_t ld, int mr, int mc, bool vec,
+                                             T* buf) {
     using V4 = typename El<T>::V4;
+    constexpr int FB = S::FB, TS = FB + 4;   // TS: 16-byte rows
+    constexpr int MAT = FB * TS;
+    static_assert(S::COLS == FB && S::TM % 4 == 0, "square tiles, whole 16-byte columns");
     const int r0 = S::row0();
 #pragma unroll
     for (int c = 0; c < S::TN; ++c) {
-        const int j = S::col(c);
-        if (j >= mc) continue;
-        T* row = MT + (size_t)j * ld + r0;
-        if (vec && r0 + S::TM <= mr) {
+        T* col = buf + S::col(c) * TS + r0;
 #pragma unroll
-            for (int r = 0; r < S::TM; r += 4)
-                *reinterpret_cast<V4*>(row + r) = V4{x[r][c], x[r + 1][c], x[r + 2][c], x[r + 3][c]};
-        } else {
-#pragma unroll
-            for (int r = 0; r < S::TM; ++r)
-                if (r0 + r < mr) row[r] = x[r][c];
+        for (int r = 0; r < S::TM; r += 4) {
+            *reinterpret_cast<V4*>(col + r) = V4{u[r][c], u[r + 1][c], u[r + 2][c], u[r + 3][c]};
+            if (HAS_L)
+                *reinterpret_cast<V4*>(col + MAT + r) =
+                    V4{l[r][c], l[r + 1][c], l[r + 2][c], l[r + 3][c]};
         }
     }
+    __syncthreads();
+    // the mirrored tiles: mc rows (the tile's columns) of mr cells each
+    for (int p = threadIdx.x; p < (HAS_L ? 2 : 1) * FB * (FB / 4); p += S::NT) {
+        const int m = p / (FB * (FB / 4)), pp = p % (FB * (FB / 4));
+        const int j = pp / (FB / 4), i = (pp % (FB / 4)) * 4;
+        if (j >= mc) continue;
+        const T* src = buf + m * MAT + j * TS + i;
+        T* dst = (m ? ML : MU) + (size_t)j * ld + i;
+        if (vec && i + 4 <= mr) {
+            *reinterpret_cast<V4*>(dst) = *reinterpret_cast<const V4*>(src);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (i + q < mr) dst[q] = src[q];
+        }
+    }
+    __syncthreads();
 }
 
 // One middle atom k applied to the thread's cells.  a/al: U[i,k] and the

@@ -394,8 +394,11 @@ __device__ __forceinline__ void p3_update_tile(T* __restrict__ U, T* __restrict_
     store_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
     if (HAS_L) store_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
     if (sym && I != J) {
-        store_tile_t<S>(u, U + (size_t)oj * ld + oi, ld, mi, mj, vec);
-        if (HAS_L) store_tile_t<S>(l, L + (size_t)oj * ld + oi, ld, mi, mj, vec);
+        // the k loop ended with a barrier: the stages are free
+        static_assert((HAS_L ? 2 : 1) * S::FB * (S::FB + 4) <= 2 * SM::STAGE,
+                      "the mirrored tiles fit the stages");
+        store_tile_t<S, HAS_L>(u, l, U + (size_t)oj * ld + oi,
+                               HAS_L ? L + (size_t)oj * ld + oi : nullptr, ld, mi, mj, vec, sm);
     }
 }
 
