@@ -153,7 +153,9 @@ int choose_tile(int n, int batch, int mode, bool bounds) {
 // (K+1,K) and (K,K+1), which phase 3 only reads too, and writes tile
 // (K+1,K+1), which phase 3 leaves alone; phase 1 waits for phase 3 of round
 // K-1 (which writes tile (K+1,K+1)), phase 2 of round K+1 for phase 3 of
-// round K, and phase 3 of round K+1 for phase 2 of round K+1.
+// round K, and phase 3 of round K+1 for phase 2 of round K+1.  With
+// symmetric inputs a last launch on `s` writes the lower triangle as the
+// transpose of the upper one.
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
                         DeviceState* d) {
     const int nb = (m.n + m.fb - 1) / m.fb;
@@ -166,6 +168,7 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
             if (e == cudaSuccess && K + 1 < nb) e = bs::launch_phase1(is_int, m, K + 1, false, s);
             if (e == cudaSuccess && K + 1 < nb) e = bs::launch_phase2(is_int, m, K + 1, s);
         }
+        if (e == cudaSuccess && m.sym) e = bs::launch_mirror(is_int, m, s);
         return e;
     }
     SideCtx c;
@@ -248,6 +251,7 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
         if (e == cudaSuccess) e = j;
     }
     if (e == cudaSuccess) e = bs::launch_phase3(is_int, m, nb - 1, bs::P3_ALL, s);
+    if (e == cudaSuccess && m.sym) e = bs::launch_mirror(is_int, m, s);
     release_side(d, c);
     return e;
 }

@@ -28,6 +28,9 @@ cudaError_t launch_phase1(bool is_int, const Mats& m, int K, bool pre, cudaStrea
 cudaError_t launch_phase2(bool is_int, const Mats& m, int K, cudaStream_t s);
 // Phase 3 of block round K over the tiles `part` selects (P3_* in bs_types.cuh).
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s);
+// Symmetric mode, after the last block round: the lower triangle written as
+// the transpose of the upper one.
+cudaError_t launch_mirror(bool is_int, const Mats& m, cudaStream_t s);
 
 // The whole blocked smoothing in one launch, one cluster per molecule
 // (fused.cu); fused_setup once per device and dtype.

@@ -12,6 +12,8 @@
 //   phase 3: rank 0 updates tile (K+1,K+1) and at once closes it (phase 1 of
 //            round K+1); ranks 1..C-1 share every other tile of round K;
 //   cluster barrier.
+// With symmetric inputs the CTAs then share the 64-wide blocks above the
+// diagonal, each written transposed over its mirror block.
 // Phase 1 of round K+1 needs only tile (K+1,K+1) after round K, and tiles
 // (K+1,K) and (K,K+1), which phase 2 of round K finished; phase 2 of round
 // K+1 waits for all of round K at the barrier.  Phase 1 of round 0 runs
@@ -42,6 +44,10 @@ constexpr size_t fz_smem() {
                ? P1Smem<T, HAS_L, FZ_FB>::BYTES
                : P3Smem<T, HAS_L, FZ_FB>::BYTES;
 }
+
+static_assert(2 * FZ_FB * (FZ_FB + 4) * 4 <= fz_smem<float, true>() &&
+                  FZ_FB * (FZ_FB + 4) * 4 <= fz_smem<float, false>(),
+              "the mirrored blocks fit the shared memory");
 
 __device__ __forceinline__ int fz_rank() {
     unsigned r;
@@ -84,24 +90,33 @@ k_fused(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
         fz_sync();
         if (K + 1 < nb) {
             if (rank == 0) {
-                p3_update_tile<T, HAS_L, FZ_FB, true>(U, L, n, ld, K + 1, K + 1, K, vec, sym, sm);
+                p3_update_tile<T, HAS_L, FZ_FB, true>(U, L, n, ld, K + 1, K + 1, K, vec, false, sm);
                 __syncthreads();   // the tile's stores, before the closure loads it
                 p1_close_tile<T, HAS_L, FZ_FB>(U, L, n, ld, K + 1, vec, smem_raw);
             } else {
                 const int nt = p3_tiles(sym, P3_ALL_OFF, nb, K);
                 for (int t = rank - 1; t < nt; t += C - 1) {
                     p3_tile(P3_ALL_OFF, sym, t, nb, K, I, J);
-                    p3_update_tile<T, HAS_L, FZ_FB, true>(U, L, n, ld, I, J, K, vec, sym, sm);
+                    p3_update_tile<T, HAS_L, FZ_FB, true>(U, L, n, ld, I, J, K, vec, false, sm);
                 }
             }
         } else {
             const int nt = p3_tiles(sym, P3_ALL, nb, K);
             for (int t = rank; t < nt; t += C) {
                 p3_tile(P3_ALL, sym, t, nb, K, I, J);
-                p3_update_tile<T, HAS_L, FZ_FB, true>(U, L, n, ld, I, J, K, vec, sym, sm);
+                p3_update_tile<T, HAS_L, FZ_FB, true>(U, L, n, ld, I, J, K, vec, false, sm);
             }
         }
         fz_sync();
+    }
+    if (sym) {
+        // every tile's last store came before the last barrier
+        const int np = (nb - 1) * nb / 2;
+        for (int t = rank; t < np; t += C) {
+            int a, c;
+            p3_tri(t, a, c);
+            p3_mirror_block<T, HAS_L>(U, L, n, ld, a, c + 1, vec, sm);
+        }
     }
 }
 

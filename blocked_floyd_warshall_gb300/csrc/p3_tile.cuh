@@ -155,10 +155,16 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
 //   P3_ALL_OFF: P3_ALL without tile (K+1,K+1), whose update phase 1 of round
 //               K+1 takes over;
 //   P3_PANELS : phase 2, the row panel (K,J) then the column panel (I,K).
-// With symmetric inputs only tiles with I <= J are computed (each off-diagonal
-// one is also stored transposed): (nb-1)nb/2, nb-1, (nb-2)(nb-1)/2 and
-// (nb-1)nb/2 - 1 tiles; phase 2 computes the row panel and stores it
-// transposed as the column panel.
+// With symmetric inputs only tiles with I <= J are computed: (nb-1)nb/2,
+// nb-1, (nb-2)(nb-1)/2 and (nb-1)nb/2 - 1 tiles.  Phase 2 computes, for each
+// block column j != K, the panel tile on the upper side -- (K,j) for j > K,
+// the column panel tile (j,K) for j < K -- and stores it also transposed, so
+// that both panels are whole for phase 3.  Phase-3 tiles are stored once:
+// no later step reads a tile below the diagonal but a panel, and the lower
+// triangle is written as the transpose of the upper one at the end
+// (p3_mirror_block).  With symmetric U and L the column panel tile (j,K) is
+// the transpose of the row panel tile (K,j), to the bit (the same sums, min
+// and max), so either side can be computed.
 
 // t -> (a, b), a <= b, enumerating the upper triangle column by column.
 __device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
@@ -173,8 +179,9 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
                                         int& J) {
     if (part == P3_PANELS) {
         if (t < nb - 1) {
-            I = K;
-            J = t + (t >= K);
+            const int j = t + (t >= K);
+            I = sym && j < K ? j : K;
+            J = sym && j < K ? K : j;
         } else {
             const int u = t - (nb - 1);
             I = u + (u >= K);
@@ -243,12 +250,12 @@ __host__ __device__ inline int p3_tiles(bool sym, int part, int nb, int K) {
 // Tile (I,J) of block round K: the product of the column operand (I,K) with
 // the row operand (K,J) applied to the tile, U and L fused (see above).  `sm`:
 // P3Smem<T, HAS_L, FB>::BYTES of shared memory.  Every thread of the CTA
-// (P3S<FB, WIDE>::NT) calls it; it ends with the tile stored (and, for
-// symmetric inputs off the diagonal, stored transposed too), after a block
-// barrier that ends every read of `sm`.
+// (P3S<FB, WIDE>::NT) calls it; it ends with the tile stored (and, with
+// `mirror` off the diagonal -- the panels of symmetric inputs -- stored
+// transposed too), after a block barrier that ends every read of `sm`.
 template <class T, bool HAS_L, int FB, bool WIDE>
 __device__ __forceinline__ void p3_update_tile(T* __restrict__ U, T* __restrict__ L, int n, int ld,
-                                               int I, int J, int K, bool vec, bool sym, T* sm) {
+                                               int I, int J, int K, bool vec, bool mirror, T* sm) {
     using S = P3S<FB, WIDE>;
     using E = El<T>;
     using SM = P3Smem<T, HAS_L, FB>;
@@ -393,13 +400,31 @@ __device__ __forceinline__ void p3_update_tile(T* __restrict__ U, T* __restrict_
     }
     store_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec);
     if (HAS_L) store_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec);
-    if (sym && I != J) {
+    if (mirror && I != J) {
         // the k loop ended with a barrier: the stages are free
         static_assert((HAS_L ? 2 : 1) * S::FB * (S::FB + 4) <= 2 * SM::STAGE,
                       "the mirrored tiles fit the stages");
         store_tile_t<S, HAS_L>(u, l, U + (size_t)oj * ld + oi,
                                HAS_L ? L + (size_t)oj * ld + oi : nullptr, ld, mi, mj, vec, sm);
     }
+}
+
+// Symmetric inputs, at the end of the smoothing: the 64-wide block (a,b),
+// a < b, written transposed over block (b,a), U and L.  Every thread of a CTA
+// of P3S<FB_SMALL, true>::NT threads calls it; `sm`: (1 + HAS_L) x 64 x 68
+// elements of shared memory, free again on return.
+template <class T, bool HAS_L>
+__device__ __forceinline__ void p3_mirror_block(T* __restrict__ U, T* __restrict__ L, int n, int ld,
+                                                int a, int b, bool vec, T* sm) {
+    using S = P3S<FB_SMALL, true>;
+    using E = El<T>;
+    const int oi = a * FB_SMALL, oj = b * FB_SMALL;
+    const int mi = min(FB_SMALL, n - oi), mj = min(FB_SMALL, n - oj);
+    T u[S::TM][S::TN], l[S::TM][S::TN];
+    load_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
+    if (HAS_L) load_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
+    store_tile_t<S, HAS_L>(u, HAS_L ? l : u, U + (size_t)oj * ld + oi,
+                           HAS_L ? L + (size_t)oj * ld + oi : nullptr, ld, mi, mj, vec, sm);
 }
 
 }  // namespace bs

@@ -20,7 +20,7 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     const int nb = (n + FB - 1) / FB;
     int I, J;
     p3_tile(part, sym, blockIdx.x, nb, K, I, J);
-    p3_update_tile<T, HAS_L, FB, WIDE>(U, L, n, ld, I, J, K, vec, sym,
+    p3_update_tile<T, HAS_L, FB, WIDE>(U, L, n, ld, I, J, K, vec, sym && part == P3_PANELS,
                                        reinterpret_cast<T*>(smem_raw));
 }
 
@@ -205,7 +205,7 @@ k_strip(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
             if (lc + q >= cj) continue;
             Us[(size_t)i * ld + lc + q] = u[r][q];
             if (HAS_L) Ls[(size_t)i * ld + lc + q] = l[r][q];
-            if (sym && I != J) {
+            if (sym && part == P3_PANELS && I != J) {
                 // the mirrored cell of tile (J, I)
                 const size_t t = (size_t)(oj + c0 + lc + q) * ld + oi + r0 + i;
                 U[t] = u[r][q];
@@ -213,6 +213,54 @@ k_strip(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, 
             }
         }
     }
+}
+
+// ---------------------------------------------------------------- mirror
+
+// Symmetric mode, after the last block round: each CTA writes one 64-wide
+// block (a,b), a < b, transposed over (b,a).  Blocks inside a diagonal tile
+// of the schedule (a and b in the same block of fb) were computed whole and
+// are left alone.
+using MS = P3S<FB_SMALL, true>;
+
+template <class T, bool HAS_L>
+constexpr size_t mirror_bytes() {
+    return (HAS_L ? 2 : 1) * (size_t)FB_SMALL * (FB_SMALL + 4) * sizeof(T);
+}
+
+template <class T, bool HAS_L>
+__global__ void __launch_bounds__(MS::NT)
+k_mirror(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride, int fb, bool vec) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    int a, c;
+    p3_tri(blockIdx.x, a, c);
+    const int b = c + 1, r = fb / FB_SMALL;
+    if (a / r == b / r) return;   // the whole CTA
+    const size_t off = (size_t)blockIdx.z * (size_t)bstride;
+    p3_mirror_block<T, HAS_L>(U + off, HAS_L ? L + off : nullptr, n, ld, a, b, vec,
+                              reinterpret_cast<T*>(smem_raw));
+}
+
+template <class T, bool HAS_L>
+static cudaError_t mirror_t(const Mats& m, cudaStream_t s) {
+    const int nb = (m.n + FB_SMALL - 1) / FB_SMALL;
+    const long long pairs = (long long)(nb - 1) * nb / 2;
+    if (pairs <= 0) return cudaSuccess;
+    return for_batch_chunks(m, [&](int b0, int nbz) {
+        T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
+        T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
+        before_launch(s, PH_THREE);
+        const cudaError_t e = launch_prio(k_mirror<T, HAS_L>, dim3((unsigned)pairs, 1, nbz),
+                                          dim3(MS::NT), mirror_bytes<T, HAS_L>(), s, U, L, m.n,
+                                          m.ld, m.bstride, m.fb, m.vec);
+        after_launch(s, PH_THREE);
+        return e;
+    });
+}
+
+cudaError_t launch_mirror(bool is_int, const Mats& m, cudaStream_t s) {
+    if (is_int) return m.L ? mirror_t<int, true>(m, s) : mirror_t<int, false>(m, s);
+    return m.L ? mirror_t<float, true>(m, s) : mirror_t<float, false>(m, s);
 }
 
 // ---------------------------------------------------------------- launchers

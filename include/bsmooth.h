@@ -116,8 +116,12 @@ enum {
                                  BS_TILE_128 or BS_NO_LOOKAHEAD: BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the
-                                 diagonal are computed, each mirrored into its
-                                 transpose -- about half the work, same output.
+                                 diagonal are computed (the panels of each block
+                                 round stored on both sides), and the lower
+                                 triangle is written as the transpose of the
+                                 upper one at the end -- about half the work,
+                                 same output on the 1/1024 grid (off it, within
+                                 the fp32 rounding of the general schedule).
                                  With BS_PERK: BS_ERR_ARG.  With BS_VALIDATE,
                                  asymmetric input returns BS_ERR_INPUT. */
 };

@@ -11,6 +11,14 @@ with the oracle.
    of a diagonal block, C = C0 + C0 D its column sub-panel and R = R0 + D R0
    its row sub-panel (min-plus sums and products of the doubled bound
    graph), the update of the rest, C R, equals C R0.
+3. The symmetric schedule.  With symmetric inputs, computing only the tiles
+   on and above the diagonal -- phase 2 takes, for each block column j, the
+   panel tile on the upper side ((K,j) for j > K as a row panel, (j,K) for
+   j < K as a column panel) and stores it also transposed; phase 3 stores
+   its tiles once -- and writing the lower triangle as the transpose of the
+   upper one at the end gives the oracle's result, even with the lower
+   triangle poisoned at the start: no step reads a stale tile below the
+   diagonal.
 """
 import numpy as np
 import pytest
@@ -154,3 +162,89 @@ def test_pre_update_identity_needs_the_closure():
             differs = True
             break
     assert differs
+
+
+# ---------------------------------------------------------------- symmetric schedule
+
+def smooth_blocked_symmetric(U0, L0, B, panel_mirror=True):
+    """The blocked schedule of symmetric mode on integer matrices, tile by
+    tile: phase 1 closes tile (K,K) (the oracle on the tile: the closure of
+    its middle atoms), phase 2 the upper-side panel tiles with their
+    transposes, phase 3 the tiles with I <= J, then the lower triangle as the
+    transpose of the upper one.  Every tile below the diagonal is first
+    overwritten with values that would change any result they reached.
+    `panel_mirror`: phase 2 stores the transposes (a test drops them)."""
+    n = U0.shape[0]
+    nb = (n + B - 1) // B
+    U, L = U0.astype(np.int64), L0.astype(np.int64)
+    sl = [slice(t * B, min(n, (t + 1) * B)) for t in range(nb)]
+    for I in range(nb):
+        for J in range(I):
+            U[sl[I], sl[J]] = 0
+            L[sl[I], sl[J]] = 1 << 29
+
+    def tile(I, J):
+        return U[sl[I], sl[J]].copy(), L[sl[I], sl[J]].copy()
+
+    def put(I, J, X, mirror=False):
+        U[sl[I], sl[J]], L[sl[I], sl[J]] = X
+        if mirror:
+            U[sl[J], sl[I]], L[sl[J], sl[I]] = X[0].T, X[1].T
+
+    for K in range(nb):
+        du, dl = tile(K, K)
+        D = tuple(a.astype(np.int64) for a in oracle.smooth(du.astype(np.int32),
+                                                            dl.astype(np.int32)))
+        put(K, K, D)
+        for j in range(nb):
+            if j > K:
+                X = tile(K, j)
+                put(K, j, plus(X, product(D, X)), mirror=panel_mirror)
+            elif j < K:
+                X = tile(j, K)
+                put(j, K, plus(X, product(X, D)), mirror=panel_mirror)
+        for I in range(nb):
+            for J in range(I, nb):
+                if K not in (I, J):
+                    put(I, J, plus(tile(I, J), product(tile(I, K), tile(K, J))))
+    for I in range(nb):
+        for J in range(I + 1, nb):
+            put(I, J, tile(I, J), mirror=True)
+    return U, L
+
+
+@pytest.mark.parametrize("n,B", [(12, 4), (13, 4), (17, 5), (9, 3), (7, 8)])
+@pytest.mark.parametrize("seed", range(3))
+def test_symmetric_schedule_equals_the_oracle(n, B, seed):
+    Uq, Lq = W.random_bounds(n, 4900 + 10 * n + seed, p_known=0.4, p_bad=0.05)
+    Uo, Lo = oracle.smooth(Uq, Lq)
+    Us, Ls = smooth_blocked_symmetric(Uq, Lq, B)
+    assert np.array_equal(Us, Uo) and np.array_equal(Ls, Lo)
+
+
+def test_symmetric_schedule_needs_the_panels_on_both_sides():
+    """Without phase 2's transposed stores, phase 3 reads poisoned panel
+    tiles below the diagonal: the poison reaches the result, so the test
+    above would see a stale read."""
+    Uq, Lq = W.random_bounds(12, 4990, p_known=0.4, p_bad=0.05)
+    Uo, Lo = oracle.smooth(Uq, Lq)
+    Us, Ls = smooth_blocked_symmetric(Uq, Lq, 4, panel_mirror=False)
+    assert not (np.array_equal(Us, Uo) and np.array_equal(Ls, Lo))
+
+
+def test_column_panel_is_the_transposed_row_panel_in_fp32():
+    """Off the grid too: with symmetric operands the column-panel product
+    (X D) and the row-panel product (D X^T) form the same fp32 sums, so one is
+    the other's transpose to the bit."""
+    rng = np.random.default_rng(4995)
+    s, r = 8, 11
+    Du = rng.random((s, s)).astype(np.float32) * 40
+    Du = np.minimum(Du, Du.T)
+    Dl = (Du * rng.random((s, s)).astype(np.float32) * 0.5).astype(np.float32)
+    Dl = np.maximum(Dl, Dl.T)
+    Xu = rng.random((r, s)).astype(np.float32) * 40
+    Xl = (Xu * rng.random((r, s)).astype(np.float32) * 0.5).astype(np.float32)
+    col = product((Xu, Xl), (Du, Dl))
+    row = product((Du, Dl), (Xu.T.copy(), Xl.T.copy()))
+    assert col[0].dtype == np.float32
+    assert np.array_equal(col[0], row[0].T) and np.array_equal(col[1], row[1].T)
