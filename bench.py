@@ -62,7 +62,7 @@ def tile_size(n, flags=0, batch=1, upper=False):
     upper: bs_smooth_upper, U alone)."""
     if flags & (1 << 5):
         return 64
-    if flags & (1 << 6):
+    if flags & ((1 << 6) | (1 << 12)):     # BS_TILE_128, BS_PAIRED_ROUNDS
         return 128
     nb = (n + 127) // 128
     return 128 if (nb - 1) ** 2 * batch >= (768 if upper else 9000) else 64
@@ -96,14 +96,6 @@ def perk_bytes(n, paired=True):
     return 16.0 * float(n) ** 2 * passes
 
 
-def phase3_algorithmic_bytes(cells, fb):
-    """DRAM bytes phase 3 must move for `cells` cell updates on fb-wide
-    tiles: each output tile of U and L (8 fb^2 bytes, fp32) read and written
-    once per block round, which applies fb middle atoms to its fb^2 cells --
-    16 / fb bytes per cell update."""
-    return 16.0 / fb * float(cells)
-
-
 def mix_ceiling_cells_per_clk(probe_instr_per_clk=None):
     """Cell updates per clock per SM the phase-3 instruction mix allows: a
     cell update is 3 adds (FP32 pipe) and 3 comparisons (ALU pipe), issued as
@@ -133,6 +125,75 @@ def merged_lookahead(n, fb, batch, sms, sym=False):
         return False
     rest = 0.5 * (nb - 2) * (nb - 1) if sym else float(nb - 2) ** 2
     return rest * batch < 0.5 * sms
+
+
+PAIRS_FROM = 48   # block rows from which 128-wide tiles take block rounds in pairs
+
+
+def pair_schedule_runs(n, fb, flags=0, sym=False):
+    """The library's rule for taking block rounds in pairs (128-wide tiles,
+    general inputs, look-ahead on; forced by BS_PAIRED_ROUNDS)."""
+    nb = (n + fb - 1) // fb
+    if fb != 128 or sym or nb < 3 or flags & (1 << 7):
+        return False
+    return bool(flags & (1 << 12)) or nb >= PAIRS_FROM
+
+
+def main_stream_phase3(n, fb, flags=0, batch=1, sms=152, pairs=None):
+    """Phase-3 launches of one blocked smoothing on the caller's stream
+    (general inputs, look-ahead on): (cell updates, tile cells passed over).
+    A pass over an r x c tile reads and writes it once, whatever the middle
+    atoms it applies, so 16 bytes per tile cell (U and L, fp32) are the
+    algorithmic DRAM traffic of a pass.
+      pairs: per pair (K, K+1) the tiles outside block-rows and -columns
+             K .. K+3 take both rounds in one pass, then block-row and
+             -column K outside K+1 .. K+3 take round K+1; an odd last round
+             runs whole;
+      merged (64-wide tiles, few rest tiles): every round but tile (K+1,K+1);
+      otherwise: every round but block-row and -column K+1, the last whole.
+    `pairs`: take the pair schedule or not (default: the library's rule)."""
+    nb = (n + fb - 1) // fb
+    size = [min(fb, n - K * fb) for K in range(nb)]
+    cells = passes = 0
+
+    def add(tiles, rounds):
+        nonlocal cells, passes
+        k = sum(size[r] for r in rounds)
+        for (i, j) in tiles:
+            cells += size[i] * size[j] * k
+            passes += size[i] * size[j]
+
+    def others(*excl):
+        return [x for x in range(nb) if x not in excl]
+
+    if nb < 2:
+        return 0, 0
+    if pair_schedule_runs(n, fb, flags) if pairs is None else pairs:
+        K = 0
+        while K + 1 < nb:
+            block = set(range(K, min(K + 4, nb)))
+            add([(i, j) for i in range(nb) for j in range(nb)
+                 if i not in block and j not in block], (K, K + 1))
+            add([(K, j) for j in range(nb) if not (K + 1 <= j <= K + 3)]
+                + [(i, K) for i in range(nb) if not (K <= i <= K + 3)], (K + 1,))
+            K += 2
+        if K == nb - 1:
+            add([(i, j) for i in others(K) for j in others(K)], (K,))
+    else:
+        merged = merged_lookahead(n, fb, batch, sms)
+        serial = nb < 3 or flags & (1 << 7)
+        for K in range(nb):
+            if serial or K == nb - 1:
+                skip = ()
+            elif merged:
+                skip = ((K + 1, K + 1),)
+            else:
+                skip = None
+            if skip is None:
+                add([(i, j) for i in others(K, K + 1) for j in others(K, K + 1)], (K,))
+            else:
+                add([(i, j) for i in others(K) for j in others(K) if (i, j) not in skip], (K,))
+    return cells * batch, passes * batch
 
 
 def next_cells(n, fb):
@@ -175,10 +236,11 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(cells):
-    """DRAM bytes of phase-3 launches covering `cells` cell updates, from the
-    committed ncu summary (bytes per cell update x cells), if the summary was
-    taken on the current kernel source; else None."""
+def committed_traffic(pass_cells):
+    """DRAM bytes of phase-3 launches that pass over `pass_cells` tile cells
+    (a pass reads and writes its tile once, whatever the rounds it applies),
+    from the committed ncu summary (bytes per tile cell passed x cells), if
+    the summary was taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "phase3_traffic.json")
     if not os.path.exists(p):
         return None
@@ -186,10 +248,10 @@ def committed_traffic(cells):
         d = json.load(f)
     if d.get("kernel_hash") != kernel_hash():
         return None
-    per_cell_k = d.get("dram_bytes_per_cell_k")
-    if per_cell_k is None:
+    per_pass_cell = d.get("dram_bytes_per_pass_cell")
+    if per_pass_cell is None:
         return None
-    return per_cell_k * float(cells)
+    return per_pass_cell * float(pass_cells)
 
 
 # ------------------------------------------------------------------ clocks
@@ -584,14 +646,12 @@ def main():
     p3 = prof["phase3"]
     fb = tile_size(n, flags)
     p3_cells_step = phase_cells(n, fb)[2]
-    main_cells_step = p3_cells_step - (next_cells(n, fb) if prof["phase3_next"]["launches"] else 0)
-    if merged_lookahead(n, fb, 1, sms):
-        main_cells_step -= diag_cells(n, fb)
+    main_cells_step, main_pass_cells = main_stream_phase3(n, fb, flags, 1, sms)
     p3_ops_step = main_cells_step * OPS_PER_CELL
     p3_s_step = p3["ms"] * 1e-3 / args.steps
     p3_achieved = p3_ops_step / p3_s_step if p3["launches"] else None
-    traffic = committed_traffic(main_cells_step)
-    algo_bytes = phase3_algorithmic_bytes(main_cells_step, fb)
+    traffic = committed_traffic(main_pass_cells)
+    algo_bytes = 16.0 * main_pass_cells
     clocks = clk.summary()
     probes = {} if args.no_probe else {
         name: round(bsm.bs_probe_alu(name), 2) for name in bsm.PROBES}
@@ -615,11 +675,15 @@ def main():
             "frac": (p3_achieved / alu_peak_ops) if p3_achieved else None,
             "traffic": traffic,
             "traffic_basis": "DRAM bytes of the same launches in one smoothing step (ncu bytes "
-                             "per cell update, profiles/phase3_traffic.json, x their cell updates)",
+                             "per tile cell passed over, profiles/phase3_traffic.json, x the "
+                             "tile cells those launches pass over)",
             "algorithmic_bytes": algo_bytes,
             "traffic_over_algorithmic": (traffic / algo_bytes) if traffic else None,
-            "algorithmic_bytes_basis": "16 / tile width bytes per cell update: each output tile "
-                                       "of U and L read and written once per block round",
+            "algorithmic_bytes_basis": "16 bytes per tile cell per pass: each output tile of U "
+                                       "and L read and written once per pass, a pass applying "
+                                       "one block round, or two where rounds go in pairs",
+            "schedule": "block rounds in pairs" if pair_schedule_runs(n, fb, flags)
+                        else "one block round per pass",
             "frac_of_instruction_mix_ceiling": (p3_achieved / OPS_PER_CELL / mix_peak_cells)
                                                if p3_achieved else None,
             "instruction_mix_ceiling_cells_per_clk_per_sm": mix_cells,
@@ -632,7 +696,7 @@ def main():
             "ms_per_step": p3_s_step * 1e3,
             "launches_per_step": p3["launches"] / args.steps,
             "achieved_basis": "6 ops x cell updates of the step's phase-3 launches on the caller's "
-                              "stream (all but the next block row and column of each round) / "
+                              "stream (all but the tiles the look-ahead stream takes) / "
                               "their summed device time, each launch timed with CUDA events on "
                               "that stream; the look-ahead stream's kernels share the GPU with "
                               "them meanwhile, so this understates the kernel alone",

@@ -48,6 +48,7 @@ BS_NO_LOOKAHEAD = 1 << 7
 BS_SYMMETRIC = 1 << 8
 BS_PERK_PAIRED = 1 << 10
 BS_ONE_LAUNCH = 1 << 11
+BS_PAIRED_ROUNDS = 1 << 12
 
 PHASES = ("round", "phase1", "phase2", "phase3", "phase3_next", "one_launch")
 

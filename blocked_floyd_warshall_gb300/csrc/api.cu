@@ -19,6 +19,7 @@ struct SideCtx {
     cudaEvent_t main_done[2] = {nullptr, nullptr};   // on the caller's stream, by round parity
     cudaEvent_t side_done = nullptr;                 // on the side stream
     cudaEvent_t next_done = nullptr;                 // on the side stream, after NEXT(K)
+    cudaEvent_t near_done = nullptr;                 // on the side stream, after NEAR2(K)
 };
 
 struct DeviceState {
@@ -96,10 +97,11 @@ cudaError_t acquire_side(DeviceState* d, SideCtx* out) {
     int lo = 0, hi = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, hi);
-    for (cudaEvent_t* ev : {&c.main_done[0], &c.main_done[1], &c.side_done, &c.next_done})
+    for (cudaEvent_t* ev :
+         {&c.main_done[0], &c.main_done[1], &c.side_done, &c.next_done, &c.near_done})
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {
-        for (cudaEvent_t ev : {c.main_done[0], c.main_done[1], c.side_done, c.next_done})
+        for (cudaEvent_t ev : {c.main_done[0], c.main_done[1], c.side_done, c.next_done, c.near_done})
             if (ev) cudaEventDestroy(ev);
         if (c.side) cudaStreamDestroy(c.side);
         return e;
@@ -127,7 +129,7 @@ void release_side(DeviceState* d, const SideCtx& c) {
 // 17.7 ms; n = 3000, 529 tiles: 3.3 against 2.6 ms).
 int choose_tile(int n, int batch, int mode, bool bounds) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
-    if (mode & BS_TILE_128) return bs::FB_LARGE;
+    if (mode & (BS_TILE_128 | BS_PAIRED_ROUNDS)) return bs::FB_LARGE;
     const double nb = (double)((n + bs::FB_LARGE - 1) / bs::FB_LARGE);
     const double from = bounds ? 9000.0 : 768.0;
     return (nb - 1) * (nb - 1) * batch >= from ? bs::FB_LARGE : bs::FB_SMALL;
@@ -156,8 +158,75 @@ int choose_tile(int n, int batch, int mode, bool bounds) {
 // round K, and phase 3 of round K+1 for phase 2 of round K+1.  With
 // symmetric inputs a last launch on `s` writes the lower triangle as the
 // transpose of the upper one.
+// Block rounds in pairs (K, K+1), K even: 128-wide tiles, general inputs.
+// The bulk of the tiles -- outside block-rows and -columns K .. K+3 -- takes
+// both rounds in one pass (P3_REST2, on `s`), so each is loaded and stored
+// once per pair instead of once per round (n = 16384 without look-ahead:
+// 777.9 -> 750.6 ms, same bits).  The side stream carries, per pair, what the
+// next steps need first:
+//   NEXT(K): block-row and -column K+1 take round K; phases 1 and 2 of K+1
+//            -> event P (the pair's panels are final);
+//   NEAR2(K): block-rows and -columns K+2, K+3 outside K, K+1 take both
+//            rounds -> event N;
+//   CORNER2: tiles (K+2,K), (K+3,K), (K,K+2), (K,K+3) take round K+1;
+//   phases 1 and 2 of K+2; NEXT(K+2); phases 1 and 2 of K+3 -> event P;
+// and `s`, after P: REST2(K); after N: PREV2, the rest of block-row and
+// -column K outside K+1 .. K+3 takes round K+1 -> event M.  The side stream
+// waits for M before NEAR2 of the next pair, whose tiles REST2(K) and PREV2
+// update.  Side by side the two streams touch disjoint tiles: REST2(K)
+// writes tiles outside block-rows and -columns K .. K+3 and reads rows and
+// columns K, K+1 there; the side stream writes tiles of block-rows and
+// -columns K+1 .. K+3 only and reads rows and columns K .. K+3.  PREV2
+// rewrites tiles of block-row and -column K that REST2(K) and NEAR2(K) read
+// as panels of round K, hence its two waits.  An odd last round runs alone
+// at the end (P3_ALL).
+cudaError_t run_pairs(bool is_int, const bs::Mats& m, cudaStream_t s, int nb, SideCtx& c) {
+    using namespace bs;
+    // phases 1 and 2 of round 0 are on `s`
+    cudaError_t e = cudaEventRecord(c.main_done[0], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c.side, c.main_done[0], 0);
+    if (e == cudaSuccess) e = launch_phase3(is_int, m, 0, P3_NEXT, c.side);
+    if (e == cudaSuccess) e = launch_phase1(is_int, m, 1, false, c.side);
+    if (e == cudaSuccess) e = launch_phase2(is_int, m, 1, c.side);
+    if (e == cudaSuccess) e = cudaEventRecord(c.next_done, c.side);
+    int K = 0;
+    for (; K + 1 < nb && e == cudaSuccess; K += 2) {
+        e = cudaStreamWaitEvent(s, c.next_done, 0);
+        if (e == cudaSuccess) e = launch_phase3(is_int, m, K, P3_REST2, s);
+        if (e == cudaSuccess && K > 0) e = cudaStreamWaitEvent(c.side, c.main_done[0], 0);
+        if (e == cudaSuccess) e = launch_phase3(is_int, m, K, P3_NEAR2, c.side);
+        if (e == cudaSuccess) e = cudaEventRecord(c.near_done, c.side);
+        if (e == cudaSuccess) e = launch_phase3(is_int, m, K + 1, P3_CORNER2, c.side);
+        if (e == cudaSuccess && K + 2 < nb) e = launch_phase1(is_int, m, K + 2, false, c.side);
+        if (e == cudaSuccess && K + 2 < nb) e = launch_phase2(is_int, m, K + 2, c.side);
+        if (e == cudaSuccess && K + 3 < nb) {
+            e = launch_phase3(is_int, m, K + 2, P3_NEXT, c.side);
+            if (e == cudaSuccess) e = launch_phase1(is_int, m, K + 3, false, c.side);
+            if (e == cudaSuccess) e = launch_phase2(is_int, m, K + 3, c.side);
+            if (e == cudaSuccess) e = cudaEventRecord(c.next_done, c.side);
+        }
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c.near_done, 0);
+        if (e == cudaSuccess) e = launch_phase3(is_int, m, K + 1, P3_PREV2, s);
+        if (e == cudaSuccess) e = cudaEventRecord(c.main_done[0], s);
+    }
+    // always join the side stream back, on success or failure
+    cudaError_t r = cudaEventRecord(c.side_done, c.side);
+    if (r == cudaSuccess) r = cudaStreamWaitEvent(s, c.side_done, 0);
+    if (e == cudaSuccess) e = r;
+    if (e == cudaSuccess && K == nb - 1) e = launch_phase3(is_int, m, K, P3_ALL, s);
+    return e;
+}
+
+// Block rows from which 128-wide tiles take block rounds in pairs.  Measured
+// (ms, single rounds against pairs): n = 16384 759.6 / 734.9, n = 12288
+// 324.8 / 314.5, n = 8192 on 128-wide tiles 98.5 / 95.2; upper bound alone
+// n = 16384 247.1 / 241.6, n = 8192 32.0 / 31.5, n = 4096 (32 block rows)
+// 4.4-4.8 / 5.5: with few rows the side stream's chain per pair (two serial
+// phase-1 closures among the rest) outlasts the pair's bulk.
+constexpr int PAIRS_FROM = 48;
+
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
-                        DeviceState* d) {
+                        bool force_pairs, DeviceState* d) {
     const int nb = (m.n + m.fb - 1) / m.fb;
     cudaError_t e = bs::launch_phase1(is_int, m, 0, false, s);
     if (e == cudaSuccess) e = bs::launch_phase2(is_int, m, 0, s);
@@ -174,6 +243,11 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
     SideCtx c;
     e = acquire_side(d, &c);
     if (e != cudaSuccess) return e;
+    if (m.fb == bs::FB_LARGE && !m.sym && (force_pairs || nb >= PAIRS_FROM)) {
+        e = run_pairs(is_int, m, s, nb, c);
+        release_side(d, c);
+        return e;
+    }
     // With fewer rest-of-round tiles than SMs, REST(K) would take the SMs
     // the moment it is ready and phase 1 of round K+1, on the critical path,
     // would wait for its CTAs to finish; REST(K) then waits for NEXT(K)
@@ -265,11 +339,14 @@ bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
                      long long bstride, int batch, int mode, bs::Mats* m) {
     const int known = BS_DTYPE_MASK | BS_PERK | BS_RULE_LITERAL | BS_VALIDATE | BS_TILE_64 |
                       BS_TILE_128 | BS_NO_LOOKAHEAD | BS_SYMMETRIC | BS_PERK_PAIRED |
-                      BS_ONE_LAUNCH;
+                      BS_ONE_LAUNCH | BS_PAIRED_ROUNDS;
     if (mode & ~known) return BS_ERR_ARG;
     if ((mode & BS_TILE_64) && (mode & BS_TILE_128)) return BS_ERR_ARG;
     if ((mode & BS_PERK_PAIRED) && !(mode & BS_PERK)) return BS_ERR_ARG;
     if ((mode & BS_ONE_LAUNCH) && (mode & (BS_PERK | BS_TILE_128 | BS_NO_LOOKAHEAD)))
+        return BS_ERR_ARG;
+    if ((mode & BS_PAIRED_ROUNDS) && (mode & (BS_PERK | BS_ONE_LAUNCH | BS_TILE_64 |
+                                              BS_NO_LOOKAHEAD | BS_SYMMETRIC)))
         return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
     if (n < 0 || batch < 0) return BS_ERR_ARG;
@@ -345,7 +422,8 @@ bs_status smooth(void* U, void* L, bool bounds, int n, int ld, long long bstride
     } else if (mode & BS_ONE_LAUNCH) {
         e = bs::launch_fused(is_int, m, s);
     } else {
-        e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0, d);
+        e = run_blocked(is_int, m, s, (mode & BS_NO_LOOKAHEAD) == 0,
+                        (mode & BS_PAIRED_ROUNDS) != 0, d);
     }
     return cuda_status(e);
 }

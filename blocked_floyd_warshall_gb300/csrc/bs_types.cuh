@@ -31,7 +31,11 @@ struct Mats {
 // profile categories (the index of bs_profile's arrays)
 enum Phase { PH_ROUND = 0, PH_ONE = 1, PH_TWO = 2, PH_THREE = 3, PH_NEXT = 4, PH_FUSED = 5 };
 
-// Which tiles a phase-3 launch covers (see p3_tile in phase3.cu).
-enum { P3_ALL = 0, P3_NEXT = 1, P3_REST = 2, P3_PANELS = 3, P3_ALL_OFF = 4 };
+// Which tiles a phase-3 launch covers (see p3_tile in p3_tile.cuh).  The
+// last four belong to the schedule that takes block rounds in pairs.
+enum {
+    P3_ALL = 0, P3_NEXT = 1, P3_REST = 2, P3_PANELS = 3, P3_ALL_OFF = 4,
+    P3_REST2 = 5, P3_NEAR2 = 6, P3_PREV2 = 7, P3_CORNER2 = 8
+};
 
 }  // namespace bs

@@ -155,6 +155,15 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
 //   P3_ALL_OFF: P3_ALL without tile (K+1,K+1), whose update phase 1 of round
 //               K+1 takes over;
 //   P3_PANELS : phase 2, the row panel (K,J) then the column panel (I,K).
+// Block rounds in pairs (K, K+1), general inputs only (see run_blocked):
+//   P3_REST2  : tiles outside block-rows and -columns K .. K+3, rounds K and
+//               K+1 in one pass;
+//   P3_NEAR2  : tiles in block-rows or -columns K+2, K+3, outside K and K+1,
+//               rounds K and K+1 in one pass;
+//   P3_PREV2  : (launched with K = the pair's second round) tiles in block-row
+//               or -column K-1 outside K .. K+2, round K;
+//   P3_CORNER2: (the same) tiles (K+1,K-1), (K+2,K-1), (K-1,K+1), (K-1,K+2),
+//               round K.
 // With symmetric inputs only tiles with I <= J are computed: (nb-1)nb/2,
 // nb-1, (nb-2)(nb-1)/2 and (nb-1)nb/2 - 1 tiles.  Phase 2 computes, for each
 // block column j != K, the panel tile on the upper side -- (K,j) for j > K,
@@ -165,6 +174,46 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
 // (p3_mirror_block).  With symmetric U and L the column panel tile (j,K) is
 // the transpose of the row panel tile (K,j), to the bit (the same sums, min
 // and max), so either side can be computed.
+
+// The tile sets of the pair schedule (general inputs; see the list above).
+__host__ __device__ inline int p3_pair_w(int nb, int K) { return min(4, nb - K); }
+__host__ __device__ inline int p3_pair_h(int nb, int K) { return max(0, min(2, nb - K - 2)); }
+__host__ __device__ inline int p3_pair_e(int nb, int Kb) { return min(3, nb - 1 - Kb); }
+
+__device__ __forceinline__ void p3_tile_pair(int part, int t, int nb, int K, int& I, int& J) {
+    if (part == P3_REST2) {
+        const int w = p3_pair_w(nb, K), m = nb - w;
+        const int ti = t / m, tj = t % m;
+        I = ti + (ti >= K ? w : 0);
+        J = tj + (tj >= K ? w : 0);
+    } else if (part == P3_NEAR2) {
+        const int h = p3_pair_h(nb, K);
+        if (t < h * (nb - 2)) {
+            const int j = t % (nb - 2);
+            I = K + 2 + t / (nb - 2);
+            J = j + (j >= K ? 2 : 0);
+        } else {
+            const int u = t - h * (nb - 2), m = nb - 2 - h;
+            const int i = u % m;
+            J = K + 2 + u / m;
+            I = i + (i >= K ? 2 + h : 0);
+        }
+    } else if (part == P3_PREV2) {
+        const int Kb = K - 1, e = p3_pair_e(nb, Kb);
+        if (t < nb - e) {
+            I = Kb;
+            J = t + (t >= Kb + 1 ? e : 0);
+        } else {
+            const int u = t - (nb - e);
+            I = u + (u >= Kb ? 1 + e : 0);
+            J = Kb;
+        }
+    } else {   // P3_CORNER2
+        const int Kb = K - 1, h = p3_pair_h(nb, Kb);
+        I = t < h ? Kb + 2 + t : Kb;
+        J = t < h ? Kb : Kb + 2 + (t - h);
+    }
+}
 
 // t -> (a, b), a <= b, enumerating the upper triangle column by column.
 __device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
@@ -235,6 +284,13 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
 // Tiles a phase-3 launch covers (see p3_tile).
 __host__ __device__ inline int p3_tiles(bool sym, int part, int nb, int K) {
     if (nb < 2) return 0;
+    if (part == P3_REST2) return K + 1 < nb ? (nb - p3_pair_w(nb, K)) * (nb - p3_pair_w(nb, K)) : 0;
+    if (part == P3_NEAR2) {
+        const int h = p3_pair_h(nb, K);
+        return K + 1 < nb ? h * (2 * nb - 4 - h) : 0;
+    }
+    if (part == P3_PREV2) return K >= 1 ? 2 * nb - 1 - 2 * p3_pair_e(nb, K - 1) : 0;
+    if (part == P3_CORNER2) return K >= 1 ? 2 * p3_pair_h(nb, K - 1) : 0;
     if (part == P3_PANELS) return sym ? nb - 1 : 2 * (nb - 1);
     if (sym)
         return part == P3_ALL ? (nb - 1) * nb / 2
@@ -255,7 +311,8 @@ __host__ __device__ inline int p3_tiles(bool sym, int part, int nb, int K) {
 // transposed too), after a block barrier that ends every read of `sm`.
 template <class T, bool HAS_L, int FB, bool WIDE>
 __device__ __forceinline__ void p3_update_tile(T* __restrict__ U, T* __restrict__ L, int n, int ld,
-                                               int I, int J, int K, bool vec, bool mirror, T* sm) {
+                                               int I, int J, int K, bool vec, bool mirror, T* sm,
+                                               int K2 = -1) {
     using S = P3S<FB, WIDE>;
     using E = El<T>;
     using SM = P3Smem<T, HAS_L, FB>;
@@ -270,14 +327,28 @@ __device__ __forceinline__ void p3_update_tile(T* __restrict__ U, T* __restrict_
     load_tile<S>(u, U + (size_t)oi * ld + oj, ld, mi, mj, vec, E::upad());
     if (HAS_L) load_tile<S>(l, L + (size_t)oi * ld + oj, ld, mi, mj, vec, E::lpad());
 
-    const int nchunks = (mk + BK - 1) / BK;
-    p3_stage<T, HAS_L, FB, S::NT>(sm, U, L, ld, oi, oj, ok, mi, mj, mk, 0, vec);
+    // K2 >= 0: block round K2 too, in the same pass (its panels final, the
+    // tile's own values after round K are never needed: min and max are
+    // exact, so folding both rounds' products in changes no bit)
+    // (the pair schedule runs on 128-wide tiles only)
+    constexpr bool PAIRS = FB == FB_LARGE;
+    const int ok2 = PAIRS ? K2 * FB : 0, mk2 = PAIRS && K2 >= 0 ? min(FB, n - ok2) : 0;
+    const int n1 = (mk + BK - 1) / BK;
+    const int nchunks = n1 + (PAIRS ? (mk2 + BK - 1) / BK : 0);
+    auto stage = [&](T* dst, int c) {
+        if constexpr (PAIRS) {
+            if (c >= n1) {
+                p3_stage<T, HAS_L, FB, S::NT>(dst, U, L, ld, oi, oj, ok2, mi, mj, mk2, c - n1, vec);
+                return;
+            }
+        }
+        p3_stage<T, HAS_L, FB, S::NT>(dst, U, L, ld, oi, oj, ok, mi, mj, mk, c, vec);
+    };
+    stage(sm, 0);
     cp_async_commit();
     const int r0 = S::row0(), cq = S::cq();
     for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks)
-            p3_stage<T, HAS_L, FB, S::NT>(sm + ((c + 1) & 1) * SM::STAGE, U, L, ld, oi, oj, ok,
-                                          mi, mj, mk, c + 1, vec);
+        if (c + 1 < nchunks) stage(sm + ((c + 1) & 1) * SM::STAGE, c + 1);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();

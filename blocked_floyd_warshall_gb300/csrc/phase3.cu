@@ -19,9 +19,11 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     if (HAS_L) L += off;
     const int nb = (n + FB - 1) / FB;
     int I, J;
-    p3_tile(part, sym, blockIdx.x, nb, K, I, J);
+    if (FB == FB_LARGE && part >= P3_REST2) p3_tile_pair(part, blockIdx.x, nb, K, I, J);
+    else p3_tile(part, sym, blockIdx.x, nb, K, I, J);
+    const bool two = part == P3_REST2 || part == P3_NEAR2;   // rounds K and K+1
     p3_update_tile<T, HAS_L, FB, WIDE>(U, L, n, ld, I, J, K, vec, sym && part == P3_PANELS,
-                                       reinterpret_cast<T*>(smem_raw));
+                                       reinterpret_cast<T*>(smem_raw), two ? K + 1 : -1);
 }
 
 // ---------------------------------------------------------------- strips
@@ -293,7 +295,9 @@ static cudaError_t phase3_t(const Mats& m, int K, int part, cudaStream_t s) {
     return for_batch_chunks(m, [&](int b0, int nbz) {
         T* U = static_cast<T*>(m.U) + (size_t)b0 * m.bstride;
         T* L = HAS_L ? static_cast<T*>(m.L) + (size_t)b0 * m.bstride : nullptr;
-        const Phase ph = part == P3_PANELS ? PH_TWO : part == P3_NEXT ? PH_NEXT : PH_THREE;
+        const Phase ph = part == P3_PANELS ? PH_TWO
+                         : part == P3_NEXT || part == P3_NEAR2 || part == P3_CORNER2 ? PH_NEXT
+                                                                                   : PH_THREE;
         before_launch(s, ph);
         const cudaError_t e = launch_prio(k_phase3<T, HAS_L, FB, WIDE>, dim3(tiles, 1, nbz),
                                           dim3(P3S<FB, WIDE>::NT), P3Smem<T, HAS_L, FB>::BYTES, s,
@@ -331,6 +335,7 @@ static cudaError_t strip_t(const Mats& m, int K, int part, cudaStream_t s) {
 template <class T, bool HAS_L>
 static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
     if (m.fb == FB_LARGE) return phase3_t<T, HAS_L, FB_LARGE, false>(m, K, part, s);
+    if (part >= P3_REST2) return cudaErrorInvalidValue;   // the pair schedule: 128-wide tiles
     const int nb = (m.n + FB_SMALL - 1) / FB_SMALL;
     const double ctas = (double)p3_tiles(m.sym, part, nb, K) * m.batch;
     if (2.0 * ctas <= m.sms) return strip_t<T, HAS_L, 4>(m, K, part, s);
@@ -339,6 +344,7 @@ static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
 }
 
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s) {
+    if (m.sym && part >= P3_REST2) return cudaErrorInvalidValue;   // general inputs only
     if (is_int) return m.L ? phase3_fb<int, true>(m, K, part, s) : phase3_fb<int, false>(m, K, part, s);
     return m.L ? phase3_fb<float, true>(m, K, part, s) : phase3_fb<float, false>(m, K, part, s);
 }

@@ -88,13 +88,81 @@ def test_per_round_bytes(n):
     assert bench.perk_bytes(n, paired=False) == 16 * n * n * n
 
 
-def test_phase3_algorithmic_bytes():
-    """One read and one write of every output tile of U and L per block round:
-    a 128-wide tile holds 128^2 cells x 8 bytes (fp32 U and L) and takes
-    128^3 cell updates per block round, 2 x 8 x 128^2 bytes -- 1/8 byte each."""
-    cells_one_tile_round = 128 ** 3
-    assert bench.phase3_algorithmic_bytes(cells_one_tile_round, 128) == 2 * 8 * 128 ** 2
-    assert bench.phase3_algorithmic_bytes(64 ** 3, 64) == 2 * 8 * 64 ** 2
+def brute_pair_side_cells(n, fb):
+    """Cell updates of the look-ahead stream's phase-3 launches when block
+    rounds go in pairs, from the sets' definitions: per pair (K, K+1) block
+    row and column K+1 outside row and column K take round K; block rows and
+    columns K+2, K+3 outside K, K+1 take rounds K and K+1; tiles (K+2, K),
+    (K+3, K), (K, K+2), (K, K+3) take round K+1; then (NEXT of the next pair)
+    block row and column K+3 outside K+2 take round K+2 -- that is NEXT(K+2),
+    counted with the next pair's K."""
+    nb = (n + fb - 1) // fb
+    size = [min(fb, n - K * fb) for K in range(nb)]
+    cells = 0
+    K = 0
+    while K + 1 < nb:
+        for I in range(nb):
+            for J in range(nb):
+                if I != K and J != K and (I == K + 1 or J == K + 1):
+                    cells += size[I] * size[J] * size[K]
+                if (I not in (K, K + 1) and J not in (K, K + 1)
+                        and (I in (K + 2, K + 3) or J in (K + 2, K + 3))):
+                    cells += size[I] * size[J] * (size[K] + size[K + 1])
+                if (I, J) in ((K + 2, K), (K + 3, K), (K, K + 2), (K, K + 3)):
+                    cells += size[I] * size[J] * size[K + 1]
+        K += 2
+    return cells
+
+
+@pytest.mark.parametrize("n,fb", [(9, 3), (12, 4), (13, 3), (17, 2), (25, 3), (30, 4)])
+def test_pair_schedule_main_and_side_cells_cover_phase3(n, fb):
+    """With block rounds in pairs the caller's-stream launches and the
+    look-ahead stream's together apply every phase-3 cell update once (phase-2
+    panels aside)."""
+    main, passes = bench.main_stream_phase3(n, fb, pairs=True)
+    assert main + brute_pair_side_cells(n, fb) == bench.phase_cells(n, fb)[2]
+    if n % fb == 0:
+        assert passes * fb <= main          # every pass applies one round or two
+
+
+def test_pair_schedule_halves_the_passes_at_16384():
+    """At n = 16384 nearly every caller's-stream pass applies two rounds: the
+    tile cells passed over are about half the cell updates / 128."""
+    main, passes = bench.main_stream_phase3(16384, 128)
+    assert 0.5 < passes * 128 / main < 0.53
+
+
+@pytest.mark.parametrize("n,fb", [(9, 4), (12, 4), (13, 8), (300, 64), (1000, 64)])
+def test_single_round_main_stream_cells(n, fb):
+    """One block round per pass: the caller's stream runs all of phase 3 but
+    the next block row and column of each round (the merged form of small
+    matrices: all but tile (K+1, K+1)); each pass applies fb middle atoms."""
+    p3 = bench.phase_cells(n, fb)[2]
+    main, passes = bench.main_stream_phase3(n, fb)
+    nb = (n + fb - 1) // fb
+    if nb < 3:
+        assert main == p3
+    elif bench.merged_lookahead(n, fb, 1, 152):
+        assert main == p3 - bench.diag_cells(n, fb)
+    else:
+        assert main == p3 - bench.next_cells(n, fb)
+    serial, _ = bench.main_stream_phase3(n, fb, flags=1 << 7)
+    assert serial == p3
+    if n % fb == 0:
+        assert passes * fb == main
+
+
+def test_pair_schedule_rule():
+    """128-wide tiles, general inputs, look-ahead: pairs from 48 block rows on
+    (n = 6017), or forced by BS_PAIRED_ROUNDS."""
+    assert bench.pair_schedule_runs(16384, 128)
+    assert bench.pair_schedule_runs(6017, 128)
+    assert not bench.pair_schedule_runs(6016, 128)
+    assert bench.pair_schedule_runs(300, 128, flags=1 << 12)
+    assert not bench.pair_schedule_runs(16384, 64)
+    assert not bench.pair_schedule_runs(16384, 128, sym=True)
+    assert not bench.pair_schedule_runs(16384, 128, flags=1 << 7)
+    assert bench.tile_size(300, flags=1 << 12) == 128
 
 
 def test_instruction_mix_ceiling():
@@ -113,6 +181,6 @@ def test_committed_phase3_capture_is_current():
         d = json.load(f)
     assert d["kernel_hash"] == bench.kernel_hash(), (
         "profiles/phase3_traffic.json is stale: re-take the phase-3 DRAM capture")
-    per_cell = d["dram_bytes_per_cell_k"]
-    assert per_cell == pytest.approx(
-        (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["cells_per_launch"])
+    per_pass_cell = d["dram_bytes_per_pass_cell"]
+    assert per_pass_cell == pytest.approx(
+        (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["tile_cells_per_launch"])

@@ -49,6 +49,7 @@ SCHEDULES = {
     "sym": bsm.BS_SYMMETRIC,
     "one": bsm.BS_ONE_LAUNCH,
     "one_sym": bsm.BS_ONE_LAUNCH | bsm.BS_SYMMETRIC,
+    "pairs": bsm.BS_PAIRED_ROUNDS,
 }
 # every algorithm: the blocked schedules and both per-round forms
 ALGOS = dict(SCHEDULES, perk=bsm.BS_PERK, perk2=bsm.BS_PERK | bsm.BS_PERK_PAIRED)
@@ -109,7 +110,7 @@ def test_symmetric_upper_only(n, algo):
 
 @pytest.mark.parametrize("n", [997, 1001, 1003])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "sym", "t128", "one"])
+@pytest.mark.parametrize("sched", ["auto", "sym", "t128", "one", "pairs"])
 def test_blocked_tails_near_1000(n, dtype, sched):
     """Sizes around the n = 1000 chain with ragged last tiles (37, 41, 43 rows
     of 64; 101, 105, 107 of 128), a padded leading dimension n + 5 with
@@ -123,7 +124,7 @@ def test_blocked_tails_near_1000(n, dtype, sched):
 
 
 @pytest.mark.parametrize("n", [129, 300])
-@pytest.mark.parametrize("sched", ["t64", "t128"])
+@pytest.mark.parametrize("sched", ["t64", "t128", "pairs"])
 def test_blocked_asymmetric(n, sched):
     Uq, Lq = W.random_bounds(n, 3000 + n, p_known=0.3, p_bad=0.02, symmetric=False)
     Uo, Lo = oracle.smooth(Uq, Lq)
@@ -133,7 +134,7 @@ def test_blocked_asymmetric(n, sched):
 
 @pytest.mark.parametrize("n,ld,offset", [(130, 140, 0), (130, 133, 0), (257, 260, 1),
                                          (97, 101, 3), (200, 200, 1)])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs"])
 def test_leading_dimension_and_misalignment(n, ld, offset, algo):
     """ld > n keeps the padding untouched; ld % 4 != 0 or a base not 16-byte
     aligned takes the scalar-IO instantiation with identical results."""
@@ -146,9 +147,9 @@ def test_leading_dimension_and_misalignment(n, ld, offset, algo):
     assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
 
 
-@pytest.mark.parametrize("n", [1, 5, 128, 129, 300])
+@pytest.mark.parametrize("n", [1, 5, 128, 129, 300, 513])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs"])
 def test_upper_only(n, dtype, algo):
     Uq, _ = W.random_bounds(n, 5000 + n, p_known=0.25)
     U0 = W.to_f32(Uq) if dtype == "f32" else Uq
@@ -207,7 +208,7 @@ def off_grid(n, seed, p_bad, symmetric=True):
 
 
 @pytest.mark.parametrize("n,p_bad", [(300, 0.0), (300, 0.02), (700, 0.01)])
-@pytest.mark.parametrize("sched", ["t64", "t128", "sym"])
+@pytest.mark.parametrize("sched", ["t64", "t128", "sym", "pairs"])
 def test_fp32_off_grid_within_tolerance(n, p_bad, sched):
     """Off the 1/1024 grid fp32 sums round, so the schedule changes the last
     bits.  Against the fp64 oracle on the same fp32 inputs:
@@ -241,7 +242,7 @@ def gamma(m):
 
 @pytest.mark.parametrize("n,p_bad,seed", [(300, 0.0, 1), (300, 0.02, 2), (700, 0.01, 3),
                                           (517, 0.005, 4)])
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "sym", "perk", "perk2"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "sym", "perk", "perk2", "pairs"])
 def test_fp32_off_grid_per_cell_bound(n, p_bad, seed, sched):
     """Off the 1/1024 grid, every fp32 cell against the fp64 oracle, with a
     bound from the cell's own path (oracle provenance: edges h and summed
@@ -304,7 +305,7 @@ def edge_cases():
 
 
 @pytest.mark.parametrize("case", sorted(edge_cases()))
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs"])
 def test_edge_cases(case, algo):
     Uq, Lq = edge_cases()[case]
     flags = ALGOS[algo]
@@ -318,7 +319,7 @@ def test_edge_cases(case, algo):
         np.testing.assert_array_equal(Uo, Uq.astype(Uo.dtype) / (1 if Uo.dtype == np.int32 else 1024))
 
 
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs"])
 def test_infinite_upper_bounds(algo):
     """fp32 U may be +inf for unknown pairs; inf + x = inf never wins."""
     Uq, Lq = W.random_bounds(200, 9500, p_known=0.1, p_bad=0.01)
@@ -394,7 +395,7 @@ def globule4096():
     return m, Uo, Lo
 
 
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial", "sym"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial", "sym", "pairs"])
 def test_globule_4096_int32_blocked(globule4096, sched):
     m, Uo, Lo = globule4096
     Ug, Lg, ok = gpu_bounds(m["U"], m["L"], SCHEDULES[sched])
@@ -416,7 +417,7 @@ def test_globule_4096_fp32_blocked_and_per_round(globule4096):
         assert bsm.bs_check_feasible(dev(Ug), dev(Lg)) == expect_flags
 
 
-@pytest.mark.parametrize("sched", ["auto", "t128", "sym", "one", "one_sym"])
+@pytest.mark.parametrize("sched", ["auto", "t128", "sym", "one", "one_sym", "pairs"])
 def test_batched_chains(sched):
     """Batch of 256 molecules n=512 in one call; every 32nd molecule against the
     oracle, all molecules against a per-molecule GPU call."""
@@ -694,7 +695,7 @@ def test_symmetric_flag_checks():
 
 
 @pytest.mark.parametrize("sched,n", [("t64", 300), ("t128", 300), ("sym", 300), ("perk", 300),
-                                     ("auto", 1000), ("one", 300)])
+                                     ("auto", 1000), ("one", 300), ("pairs", 1000)])
 def test_cuda_graph_capture_and_replay(sched, n):
     """A smoothing captured into a CUDA graph (look-ahead fork and join
     included) replays to the same result, twice, on fresh inputs.  n = 1000
@@ -819,6 +820,15 @@ def test_profile_records_every_launch():
     # rounds 0, 1: phase 3 split into the rest (caller's stream) and the next
     # block row and column (look-ahead stream)
     assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 3, 2, 0]
+    assert p["phase3"]["ms"] > 0 and p["phase3_next"]["ms"] > 0
+    # block rounds in pairs: on the caller's stream the pair's bulk (no tile at
+    # nb = 3), the rest of block row and column 0 and the odd last round
+    # whole; on the look-ahead stream the next block row and column, the near
+    # ones and the corner tiles
+    bsm.bs_profile_begin()
+    bsm.bs_smooth_bounds(U, L, flags=bsm.BS_PAIRED_ROUNDS)
+    p = bsm.bs_profile_end()
+    assert [p[k]["launches"] for k in bsm.PHASES] == [0, 3, 3, 2, 3, 0]
     assert p["phase3"]["ms"] > 0 and p["phase3_next"]["ms"] > 0
     # 64-wide tiles, few rest tiles: phase 3 of each round but the last is
     # one launch on the caller's stream, beside phase 1 of the next round

@@ -248,3 +248,172 @@ def test_column_panel_is_the_transposed_row_panel_in_fp32():
     row = product((Du, Dl), (Xu.T.copy(), Xl.T.copy()))
     assert col[0].dtype == np.float32
     assert np.array_equal(col[0], row[0].T) and np.array_equal(col[1], row[1].T)
+
+
+# ---------------------------------------------------------------- block rounds in pairs
+
+def pair_schedule(nb):
+    """The launches of the pair schedule (128-wide tiles, general inputs), in
+    the library's host order, as (stream, kind, K, tiles, rounds, waits):
+    stream "s" (the caller's) or "side"; kind "p1", "p2" or "p3"; waits: the
+    names of events the launch waits for first.  Events are ("rec", name)
+    entries.  The sets are written from their definitions (block-rows and
+    -columns), not from the device code's index maps."""
+    def rng(*excl):
+        return [x for x in range(nb) if x not in excl]
+
+    def tiles_next(K):
+        return {(K + 1, j) for j in rng(K)} | {(i, K + 1) for i in rng(K, K + 1)}
+
+    def tiles_panels(K):
+        return {(K, j) for j in rng(K)} | {(i, K) for i in rng(K)}
+
+    def near(K):
+        rows = {K + 2, K + 3} & set(range(nb))
+        return {(i, j) for i in rng(K, K + 1) for j in rng(K, K + 1) if i in rows or j in rows}
+
+    out = []
+    add = out.append
+    add(("s", "p1", 0, {(0, 0)}, (0,)))
+    add(("s", "p2", 0, tiles_panels(0), (0,)))
+    add(("rec", "s", "M"))
+    add(("wait", "side", "M"))
+    add(("side", "p3", 0, tiles_next(0), (0,)))
+    add(("side", "p1", 1, {(1, 1)}, (1,)))
+    add(("side", "p2", 1, tiles_panels(1), (1,)))
+    add(("rec", "side", "P"))
+    K = 0
+    while K + 1 < nb:
+        add(("wait", "s", "P"))
+        add(("s", "p3", K, {(i, j) for i in range(nb) for j in range(nb)
+                            if not (K <= i < K + 4) and not (K <= j < K + 4)}, (K, K + 1)))
+        if K > 0:
+            add(("wait", "side", "M"))
+        add(("side", "p3", K, near(K), (K, K + 1)))
+        add(("rec", "side", "N"))
+        add(("side", "p3", K + 1, {(K + 2, K), (K + 3, K), (K, K + 2), (K, K + 3)}
+             & {(i, j) for i in range(nb) for j in range(nb)}, (K + 1,)))
+        if K + 2 < nb:
+            add(("side", "p1", K + 2, {(K + 2, K + 2)}, (K + 2,)))
+            add(("side", "p2", K + 2, tiles_panels(K + 2), (K + 2,)))
+        if K + 3 < nb:
+            add(("side", "p3", K + 2, tiles_next(K + 2), (K + 2,)))
+            add(("side", "p1", K + 3, {(K + 3, K + 3)}, (K + 3,)))
+            add(("side", "p2", K + 3, tiles_panels(K + 3), (K + 3,)))
+            add(("rec", "side", "P"))
+        add(("wait", "s", "N"))
+        add(("s", "p3", K + 1, {(K, j) for j in range(nb) if not (K + 1 <= j <= K + 3)}
+             | {(i, K) for i in range(nb) if not (K <= i <= K + 3)}, (K + 1,)))
+        add(("rec", "s", "M"))
+        K += 2
+    add(("rec", "side", "J"))
+    add(("wait", "s", "J"))
+    if K == nb - 1:
+        add(("s", "p3", K, {(i, j) for i in rng(K) for j in rng(K)}, (K,)))
+    return out
+
+
+def launches_with_order(entries):
+    """The launches and, for each, the set of launches that happen before it
+    (stream order and event waits)."""
+    launches, before = [], []
+    last = {"s": None, "side": None}       # last launch on each stream
+    pending = {"s": set(), "side": set()}  # happens-before set a stream's next launch inherits
+    events = {}
+    for e in entries:
+        if e[0] == "rec":
+            events[e[2]] = set(pending[e[1]])
+        elif e[0] == "wait":
+            pending[e[1]] |= events[e[2]]
+        else:
+            idx = len(launches)
+            launches.append(e)
+            hb = set(pending[e[0]])
+            before.append(hb)
+            pending[e[0]] = hb | {idx}
+    return launches, before
+
+
+def reads_writes(launch):
+    _, kind, K, tiles, rounds = launch
+    writes = set(tiles)
+    reads = set(tiles)
+    for (i, j) in tiles:
+        for k in rounds:
+            reads |= {(i, k), (k, j)}
+    if kind == "p2":
+        reads.add((K, K))
+    return reads, writes
+
+
+@pytest.mark.parametrize("nb", list(range(3, 14)))
+def test_pair_schedule_has_no_race(nb):
+    """Launches that may run side by side (neither ordered before the other by
+    its stream or an event) touch disjoint tiles: no write meets a read or a
+    write of the other."""
+    launches, before = launches_with_order(pair_schedule(nb))
+    rw = [reads_writes(x) for x in launches]
+    for b in range(len(launches)):
+        for a in range(b):
+            if a in before[b]:
+                continue
+            (ra, wa), (rb, wb) = rw[a], rw[b]
+            assert not (wa & (rb | wb)) and not (wb & ra), (nb, launches[a][1:3], launches[b][1:3])
+
+
+@pytest.mark.parametrize("nb", list(range(3, 14)))
+def test_pair_schedule_updates_every_tile_with_every_round(nb):
+    """Each tile takes every block round exactly once, in increasing order,
+    across the launches in any order the dependencies allow (checked along
+    the host order, which is one of them)."""
+    launches, _ = launches_with_order(pair_schedule(nb))
+    done = {(i, j): [] for i in range(nb) for j in range(nb)}
+    for _, kind, K, tiles, rounds in launches:
+        for t in tiles:
+            done[t].extend(rounds)
+    for t, r in done.items():
+        assert r == list(range(nb)), (nb, t, r)
+
+
+def smooth_pair_schedule(U0, L0, B):
+    """Run the pair schedule's launches in host order on integer matrices: a
+    phase-3 launch reads, for each tile, its operands of every round it
+    applies before writing (one pass), then writes the tile."""
+    n = U0.shape[0]
+    nb = (n + B - 1) // B
+    U, L = U0.astype(np.int64), L0.astype(np.int64)
+    sl = [slice(t * B, min(n, (t + 1) * B)) for t in range(nb)]
+
+    def tile(I, J):
+        return U[sl[I], sl[J]].copy(), L[sl[I], sl[J]].copy()
+
+    launches, _ = launches_with_order(pair_schedule(nb))
+    for _, kind, K, tiles, rounds in launches:
+        if kind == "p1":
+            du, dl = tile(K, K)
+            U[sl[K], sl[K]], L[sl[K], sl[K]] = (a.astype(np.int64) for a in oracle.smooth(
+                du.astype(np.int32), dl.astype(np.int32)))
+            continue
+        new = {}
+        for (I, J) in tiles:
+            X = tile(I, J)
+            if kind == "p2":
+                D = tile(K, K)
+                X = plus(X, product(D, X)) if I == K else plus(X, product(X, D))
+            else:
+                for k in rounds:
+                    X = plus(X, product(tile(I, k), tile(k, J)))
+            new[(I, J)] = X
+        for (I, J), X in new.items():
+            U[sl[I], sl[J]], L[sl[I], sl[J]] = X
+    return U, L
+
+
+@pytest.mark.parametrize("n,B", [(12, 4), (13, 3), (17, 2), (25, 3), (9, 3), (21, 2)])
+@pytest.mark.parametrize("seed", range(2))
+def test_pair_schedule_equals_the_oracle(n, B, seed):
+    Uq, Lq = W.random_bounds(n, 5100 + 10 * n + seed, p_known=0.4, p_bad=0.05,
+                             symmetric=bool(seed))
+    Uo, Lo = oracle.smooth(Uq, Lq)
+    Us, Ls = smooth_pair_schedule(Uq, Lq, B)
+    assert np.array_equal(Us, Uo) and np.array_equal(Ls, Lo)
