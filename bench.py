@@ -65,6 +65,8 @@ def tile_size(n, flags=0, batch=1, upper=False):
     if flags & ((1 << 6) | (1 << 12)):     # BS_TILE_128, BS_PAIRED_ROUNDS
         return 128
     nb = (n + 127) // 128
+    if not upper and not flags & (1 << 8) and nb >= PAIRS_FROM:   # general inputs, in pairs
+        return 128
     return 128 if (nb - 1) ** 2 * batch >= (768 if upper else 9000) else 64
 
 

@@ -115,9 +115,23 @@ void release_side(DeviceState* d, const SideCtx& c) {
     d->free_side.push_back(c);
 }
 
-// Tile size for the blocked schedule: 64 x 64 unless a block round's phase 3
-// at 128 holds at least 9000 tiles over the batch (single matrices from
-// n = 12161 on), then 128 x 128; fp32 and int32 alike.  Measured on the
+// Block rows from which 128-wide tiles take block rounds in pairs.  Measured
+// (ms, single rounds against pairs): n = 16384 759.6 / 734.9, n = 12288
+// 324.8 / 314.5, n = 8192 on 128-wide tiles 98.5 / 95.2; upper bound alone
+// n = 16384 247.1 / 241.6, n = 8192 32.0 / 31.5, n = 4096 (32 block rows)
+// 4.4-4.8 / 5.5: with few rows the side stream's chain per pair (two serial
+// phase-1 closures among the rest) outlasts the pair's bulk.
+constexpr int PAIRS_FROM = 48;
+
+// Tile size for the blocked schedule: 128 x 128 from PAIRS_FROM block rows
+// of 128 for general inputs (single matrices from n = 6017 on; symmetric
+// inputs keep one round per pass) or once a block round's phase 3
+// at 128 holds at least 9000 tiles over the batch, else 64 x 64; fp32 and
+// int32 alike.  With 48 rows or more the 128-wide schedule takes block
+// rounds in pairs and wins (ms, 64 against 128 in pairs: fp32 n = 6144
+// 41.5 / 41.0, n = 8192 96.8 / 95.2, n = 10240 188.3 / 186.8; int32
+// n = 6144 43.9 / 42.6, n = 8192 102.6 / 99.1; at n = 5120, 40 rows, one
+// round per pass, 24.5 / 25.7).  Before pairs, measured on the
 // GB300 (ms, 64 against 128): fp32 n = 4096 12.92 / 13.22, n = 6000 39.6 /
 // 41.1, n = 8192 97.1 / 98.6, n = 10000 178.8 / 185.7, n = 12288 324.7 /
 // 324.6, n = 16384 766.8 / 758.7; 64 molecules of n = 1024 12.24 / 12.40;
@@ -131,6 +145,7 @@ int choose_tile(int n, int batch, int mode, bool bounds) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
     if (mode & (BS_TILE_128 | BS_PAIRED_ROUNDS)) return bs::FB_LARGE;
     const double nb = (double)((n + bs::FB_LARGE - 1) / bs::FB_LARGE);
+    if (bounds && !(mode & BS_SYMMETRIC) && nb >= PAIRS_FROM) return bs::FB_LARGE;   // in pairs
     const double from = bounds ? 9000.0 : 768.0;
     return (nb - 1) * (nb - 1) * batch >= from ? bs::FB_LARGE : bs::FB_SMALL;
 }
@@ -217,13 +232,6 @@ cudaError_t run_pairs(bool is_int, const bs::Mats& m, cudaStream_t s, int nb, Si
     return e;
 }
 
-// Block rows from which 128-wide tiles take block rounds in pairs.  Measured
-// (ms, single rounds against pairs): n = 16384 759.6 / 734.9, n = 12288
-// 324.8 / 314.5, n = 8192 on 128-wide tiles 98.5 / 95.2; upper bound alone
-// n = 16384 247.1 / 241.6, n = 8192 32.0 / 31.5, n = 4096 (32 block rows)
-// 4.4-4.8 / 5.5: with few rows the side stream's chain per pair (two serial
-// phase-1 closures among the rest) outlasts the pair's bulk.
-constexpr int PAIRS_FROM = 48;
 
 cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool lookahead,
                         bool force_pairs, DeviceState* d) {

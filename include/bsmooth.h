@@ -94,7 +94,9 @@ enum {
     BS_RULE_LITERAL = 1 << 3, /* printed rule; BS_PERK only, else BS_ERR_ARG */
     BS_VALIDATE = 1 << 4,     /* check the preconditions first (synchronises) */
     /* Blocked-mode schedule knobs; every setting gives identical results. */
-    BS_TILE_64 = 1 << 5,      /* force 64 x 64 tiles (default: 128 once a block
+    BS_TILE_64 = 1 << 5,      /* force 64 x 64 tiles (default: 128 from 48
+                                 block rows of 128 with general inputs
+                                 (block rounds in pairs), or once a block
                                  round's phase 3 holds at least 9000 tiles of
                                  128 over the batch, 768 for the upper bound
                                  alone, else 64) */

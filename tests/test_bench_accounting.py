@@ -66,13 +66,18 @@ def test_merged_lookahead_rule():
 
 
 def test_tile_rule_matches_documented_thresholds():
-    """64-wide tiles unless a 128-wide phase 3 holds >= 9000 tiles over the
-    batch, fp32 and int32 alike (768 for the upper bound alone)."""
+    """128-wide tiles from 48 block rows of 128 (where block rounds go in
+    pairs) or once a 128-wide phase 3 holds >= 9000 tiles over the batch,
+    else 64; fp32 and int32 alike (768 tiles for the upper bound alone)."""
     assert bench.tile_size(4096) == 64
-    assert bench.tile_size(10000) == 64
+    assert bench.tile_size(6016) == 64 and bench.tile_size(6017) == 128   # 47, 48 rows
+    assert bench.tile_size(10000) == 128
     assert bench.tile_size(16384) == 128
-    assert bench.tile_size(12160) == 64 and bench.tile_size(12161) == 128   # 94^2, 95^2 tiles
     assert bench.tile_size(4096, flags=1) == 64 and bench.tile_size(16384, flags=1) == 128
+    assert bench.tile_size(6017, flags=1) == 128
+    assert bench.tile_size(10000, flags=1 << 8) == 64          # symmetric: 78^2 < 9000
+    assert bench.tile_size(3000, batch=18) == 128              # 23^2 x 18 = 9522
+    assert bench.tile_size(3000, batch=17) == 64               # 23^2 x 17 = 8993
     assert bench.tile_size(512, batch=256) == 64               # 9 x 256 = 2304
     assert bench.tile_size(4096, upper=True) == 128            # U alone: 961 >= 768
     assert bench.tile_size(3000, upper=True) == 64             # 23^2 = 529
