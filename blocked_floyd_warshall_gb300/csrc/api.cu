@@ -173,7 +173,7 @@ int choose_tile(int n, int batch, int mode, bool bounds) {
 // round K, and phase 3 of round K+1 for phase 2 of round K+1.  With
 // symmetric inputs a last launch on `s` writes the lower triangle as the
 // transpose of the upper one.
-// Block rounds in pairs (K, K+1), K even: 128-wide tiles, general inputs.
+// Block rounds in pairs (K, K+1), K even: 128-wide tiles.
 // The bulk of the tiles -- outside block-rows and -columns K .. K+3 -- takes
 // both rounds in one pass (P3_REST2, on `s`), so each is loaded and stored
 // once per pair instead of once per round (n = 16384 without look-ahead:
@@ -194,7 +194,9 @@ int choose_tile(int n, int batch, int mode, bool bounds) {
 // -columns K+1 .. K+3 only and reads rows and columns K .. K+3.  PREV2
 // rewrites tiles of block-row and -column K that REST2(K) and NEAR2(K) read
 // as panels of round K, hence its two waits.  An odd last round runs alone
-// at the end (P3_ALL).
+// at the end (P3_ALL).  With symmetric inputs every set keeps its tiles on
+// and above the diagonal (the panels are stored on both sides as always)
+// and the lower triangle is written at the end.
 cudaError_t run_pairs(bool is_int, const bs::Mats& m, cudaStream_t s, int nb, SideCtx& c) {
     using namespace bs;
     // phases 1 and 2 of round 0 are on `s`
@@ -229,6 +231,7 @@ cudaError_t run_pairs(bool is_int, const bs::Mats& m, cudaStream_t s, int nb, Si
     if (r == cudaSuccess) r = cudaStreamWaitEvent(s, c.side_done, 0);
     if (e == cudaSuccess) e = r;
     if (e == cudaSuccess && K == nb - 1) e = launch_phase3(is_int, m, K, P3_ALL, s);
+    if (e == cudaSuccess && m.sym) e = launch_mirror(is_int, m, s);
     return e;
 }
 
@@ -251,7 +254,7 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
     SideCtx c;
     e = acquire_side(d, &c);
     if (e != cudaSuccess) return e;
-    if (m.fb == bs::FB_LARGE && !m.sym && (force_pairs || nb >= PAIRS_FROM)) {
+    if (m.fb == bs::FB_LARGE && (force_pairs || nb >= PAIRS_FROM)) {
         e = run_pairs(is_int, m, s, nb, c);
         release_side(d, c);
         return e;
@@ -353,8 +356,8 @@ bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
     if ((mode & BS_PERK_PAIRED) && !(mode & BS_PERK)) return BS_ERR_ARG;
     if ((mode & BS_ONE_LAUNCH) && (mode & (BS_PERK | BS_TILE_128 | BS_NO_LOOKAHEAD)))
         return BS_ERR_ARG;
-    if ((mode & BS_PAIRED_ROUNDS) && (mode & (BS_PERK | BS_ONE_LAUNCH | BS_TILE_64 |
-                                              BS_NO_LOOKAHEAD | BS_SYMMETRIC)))
+    if ((mode & BS_PAIRED_ROUNDS) &&
+        (mode & (BS_PERK | BS_ONE_LAUNCH | BS_TILE_64 | BS_NO_LOOKAHEAD)))
         return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
     if (n < 0 || batch < 0) return BS_ERR_ARG;

@@ -175,20 +175,57 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
 // the transpose of the row panel tile (K,j), to the bit (the same sums, min
 // and max), so either side can be computed.
 
-// The tile sets of the pair schedule (general inputs; see the list above).
+// t -> (a, b), a <= b, enumerating the upper triangle column by column.
+__device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
+    int c = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+    while (c * (c + 1) / 2 > t) --c;
+    while ((c + 1) * (c + 2) / 2 <= t) ++c;
+    b = c;
+    a = t - c * (c + 1) / 2;
+}
+
+// The tile sets of the pair schedule (see the list above); with symmetric
+// inputs the tiles on and above the diagonal of each set (CORNER2: (K-1,K+1)
+// and (K-1,K+2); PREV2: block row K-1 from the diagonal on, without
+// K .. K+2, and block column K-1 above the diagonal).
 __host__ __device__ inline int p3_pair_w(int nb, int K) { return min(4, nb - K); }
 __host__ __device__ inline int p3_pair_h(int nb, int K) { return max(0, min(2, nb - K - 2)); }
 __host__ __device__ inline int p3_pair_e(int nb, int Kb) { return min(3, nb - 1 - Kb); }
+// symmetric NEAR2: the near block rows' tiles from the diagonal on
+__host__ __device__ inline int p3_pair_near_rows(int nb, int K) {
+    const int h = p3_pair_h(nb, K), a = nb - K - 2;
+    return h == 2 ? 2 * a - 1 : h == 1 ? a : 0;
+}
 
-__device__ __forceinline__ void p3_tile_pair(int part, int t, int nb, int K, int& I, int& J) {
+__device__ __forceinline__ void p3_tile_pair(int part, bool sym, int t, int nb, int K, int& I,
+                                             int& J) {
     if (part == P3_REST2) {
         const int w = p3_pair_w(nb, K), m = nb - w;
-        const int ti = t / m, tj = t % m;
-        I = ti + (ti >= K ? w : 0);
-        J = tj + (tj >= K ? w : 0);
+        int a, b;
+        if (sym) {
+            p3_tri(t, a, b);
+        } else {
+            a = t / m;
+            b = t % m;
+        }
+        I = a + (a >= K ? w : 0);
+        J = b + (b >= K ? w : 0);
     } else if (part == P3_NEAR2) {
         const int h = p3_pair_h(nb, K);
-        if (t < h * (nb - 2)) {
+        if (sym) {
+            const int a = nb - K - 2, rows = p3_pair_near_rows(nb, K);
+            if (t < a) {
+                I = K + 2;
+                J = K + 2 + t;
+            } else if (t < rows) {
+                I = K + 3;
+                J = K + 3 + (t - a);
+            } else {
+                const int u = t - rows;
+                I = u % K;
+                J = K + 2 + u / K;
+            }
+        } else if (t < h * (nb - 2)) {
             const int j = t % (nb - 2);
             I = K + 2 + t / (nb - 2);
             J = j + (j >= K ? 2 : 0);
@@ -200,7 +237,11 @@ __device__ __forceinline__ void p3_tile_pair(int part, int t, int nb, int K, int
         }
     } else if (part == P3_PREV2) {
         const int Kb = K - 1, e = p3_pair_e(nb, Kb);
-        if (t < nb - e) {
+        if (sym) {
+            const int r = nb - Kb - e;
+            I = t < r ? Kb : t - r;
+            J = t < r ? (t == 0 ? Kb : Kb + e + t) : Kb;
+        } else if (t < nb - e) {
             I = Kb;
             J = t + (t >= Kb + 1 ? e : 0);
         } else {
@@ -210,18 +251,9 @@ __device__ __forceinline__ void p3_tile_pair(int part, int t, int nb, int K, int
         }
     } else {   // P3_CORNER2
         const int Kb = K - 1, h = p3_pair_h(nb, Kb);
-        I = t < h ? Kb + 2 + t : Kb;
-        J = t < h ? Kb : Kb + 2 + (t - h);
+        I = t < h && !sym ? Kb + 2 + t : Kb;
+        J = t < h && !sym ? Kb : Kb + 2 + (sym ? t : t - h);
     }
-}
-
-// t -> (a, b), a <= b, enumerating the upper triangle column by column.
-__device__ __forceinline__ void p3_tri(int t, int& a, int& b) {
-    int c = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
-    while (c * (c + 1) / 2 > t) --c;
-    while ((c + 1) * (c + 2) / 2 <= t) ++c;
-    b = c;
-    a = t - c * (c + 1) / 2;
 }
 
 __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K, int& I,
@@ -284,13 +316,21 @@ __device__ __forceinline__ void p3_tile(int part, bool sym, int t, int nb, int K
 // Tiles a phase-3 launch covers (see p3_tile).
 __host__ __device__ inline int p3_tiles(bool sym, int part, int nb, int K) {
     if (nb < 2) return 0;
-    if (part == P3_REST2) return K + 1 < nb ? (nb - p3_pair_w(nb, K)) * (nb - p3_pair_w(nb, K)) : 0;
+    if (part == P3_REST2) {
+        const int m = nb - p3_pair_w(nb, K);
+        return K + 1 < nb ? (sym ? m * (m + 1) / 2 : m * m) : 0;
+    }
     if (part == P3_NEAR2) {
         const int h = p3_pair_h(nb, K);
-        return K + 1 < nb ? h * (2 * nb - 4 - h) : 0;
+        if (K + 1 >= nb) return 0;
+        return sym ? p3_pair_near_rows(nb, K) + h * K : h * (2 * nb - 4 - h);
     }
-    if (part == P3_PREV2) return K >= 1 ? 2 * nb - 1 - 2 * p3_pair_e(nb, K - 1) : 0;
-    if (part == P3_CORNER2) return K >= 1 ? 2 * p3_pair_h(nb, K - 1) : 0;
+    if (part == P3_PREV2) {
+        if (K < 1) return 0;
+        const int e = p3_pair_e(nb, K - 1);
+        return sym ? nb - e : 2 * nb - 1 - 2 * e;
+    }
+    if (part == P3_CORNER2) return K >= 1 ? (sym ? 1 : 2) * p3_pair_h(nb, K - 1) : 0;
     if (part == P3_PANELS) return sym ? nb - 1 : 2 * (nb - 1);
     if (sym)
         return part == P3_ALL ? (nb - 1) * nb / 2

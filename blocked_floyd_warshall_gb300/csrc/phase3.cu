@@ -19,7 +19,7 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     if (HAS_L) L += off;
     const int nb = (n + FB - 1) / FB;
     int I, J;
-    if (FB == FB_LARGE && part >= P3_REST2) p3_tile_pair(part, blockIdx.x, nb, K, I, J);
+    if (FB == FB_LARGE && part >= P3_REST2) p3_tile_pair(part, sym, blockIdx.x, nb, K, I, J);
     else p3_tile(part, sym, blockIdx.x, nb, K, I, J);
     const bool two = part == P3_REST2 || part == P3_NEAR2;   // rounds K and K+1
     p3_update_tile<T, HAS_L, FB, WIDE>(U, L, n, ld, I, J, K, vec, sym && part == P3_PANELS,
@@ -344,7 +344,6 @@ static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
 }
 
 cudaError_t launch_phase3(bool is_int, const Mats& m, int K, int part, cudaStream_t s) {
-    if (m.sym && part >= P3_REST2) return cudaErrorInvalidValue;   // general inputs only
     if (is_int) return m.L ? phase3_fb<int, true>(m, K, part, s) : phase3_fb<int, false>(m, K, part, s);
     return m.L ? phase3_fb<float, true>(m, K, part, s) : phase3_fb<float, false>(m, K, part, s);
 }

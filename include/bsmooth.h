@@ -120,10 +120,9 @@ enum {
                                  taken in pairs whatever the size (the bulk
                                  tiles update both rounds of a pair in one
                                  pass; by default from 48 block rows on, with
-                                 general inputs and 128-wide tiles); same
-                                 results.  With BS_PERK, BS_ONE_LAUNCH,
-                                 BS_TILE_64, BS_NO_LOOKAHEAD or BS_SYMMETRIC:
-                                 BS_ERR_ARG */
+                                 128-wide tiles); same results.  With
+                                 BS_PERK, BS_ONE_LAUNCH, BS_TILE_64 or
+                                 BS_NO_LOOKAHEAD: BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the
                                  diagonal are computed (the panels of each block

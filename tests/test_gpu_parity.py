@@ -50,6 +50,7 @@ SCHEDULES = {
     "one": bsm.BS_ONE_LAUNCH,
     "one_sym": bsm.BS_ONE_LAUNCH | bsm.BS_SYMMETRIC,
     "pairs": bsm.BS_PAIRED_ROUNDS,
+    "pairs_sym": bsm.BS_PAIRED_ROUNDS | bsm.BS_SYMMETRIC,
 }
 # every algorithm: the blocked schedules and both per-round forms
 ALGOS = dict(SCHEDULES, perk=bsm.BS_PERK, perk2=bsm.BS_PERK | bsm.BS_PERK_PAIRED)
@@ -88,7 +89,8 @@ def test_blocked_matches_oracle(n, dtype, sched):
 
 @pytest.mark.parametrize("n", [1, 2, 5, 63, 64, 65, 127, 129, 257, 300, 513])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "t64_serial", "t128_serial", "one"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "t64_serial", "t128_serial", "one",
+                                   "pairs"])
 def test_symmetric_mode_matches_oracle(n, dtype, sched):
     """Half the tiles computed and mirrored: bit-identical to the oracle."""
     Uq, Lq = W.random_bounds(n, 2500 + n, p_known=0.2, p_bad=0.02)
@@ -99,8 +101,8 @@ def test_symmetric_mode_matches_oracle(n, dtype, sched):
     assert same_bits(Ug, Uo) and same_bits(Lg, Lo)
 
 
-@pytest.mark.parametrize("n", [65, 300])
-@pytest.mark.parametrize("algo", ["t64", "t128", "one"])
+@pytest.mark.parametrize("n", [65, 300, 513])
+@pytest.mark.parametrize("algo", ["t64", "t128", "one", "pairs"])
 def test_symmetric_upper_only(n, algo):
     Uq, _ = W.random_bounds(n, 5500 + n, p_known=0.25)
     Uo = oracle.smooth_upper(Uq)
@@ -110,7 +112,7 @@ def test_symmetric_upper_only(n, algo):
 
 @pytest.mark.parametrize("n", [997, 1001, 1003])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "sym", "t128", "one", "pairs"])
+@pytest.mark.parametrize("sched", ["auto", "sym", "t128", "one", "pairs", "pairs_sym"])
 def test_blocked_tails_near_1000(n, dtype, sched):
     """Sizes around the n = 1000 chain with ragged last tiles (37, 41, 43 rows
     of 64; 101, 105, 107 of 128), a padded leading dimension n + 5 with
@@ -208,7 +210,7 @@ def off_grid(n, seed, p_bad, symmetric=True):
 
 
 @pytest.mark.parametrize("n,p_bad", [(300, 0.0), (300, 0.02), (700, 0.01)])
-@pytest.mark.parametrize("sched", ["t64", "t128", "sym", "pairs"])
+@pytest.mark.parametrize("sched", ["t64", "t128", "sym", "pairs", "pairs_sym"])
 def test_fp32_off_grid_within_tolerance(n, p_bad, sched):
     """Off the 1/1024 grid fp32 sums round, so the schedule changes the last
     bits.  Against the fp64 oracle on the same fp32 inputs:
@@ -242,7 +244,8 @@ def gamma(m):
 
 @pytest.mark.parametrize("n,p_bad,seed", [(300, 0.0, 1), (300, 0.02, 2), (700, 0.01, 3),
                                           (517, 0.005, 4)])
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "sym", "perk", "perk2", "pairs"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128", "sym", "perk", "perk2", "pairs",
+                                   "pairs_sym"])
 def test_fp32_off_grid_per_cell_bound(n, p_bad, seed, sched):
     """Off the 1/1024 grid, every fp32 cell against the fp64 oracle, with a
     bound from the cell's own path (oracle provenance: edges h and summed
@@ -395,7 +398,7 @@ def globule4096():
     return m, Uo, Lo
 
 
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial", "sym", "pairs"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial", "sym", "pairs", "pairs_sym"])
 def test_globule_4096_int32_blocked(globule4096, sched):
     m, Uo, Lo = globule4096
     Ug, Lg, ok = gpu_bounds(m["U"], m["L"], SCHEDULES[sched])
@@ -417,7 +420,7 @@ def test_globule_4096_fp32_blocked_and_per_round(globule4096):
         assert bsm.bs_check_feasible(dev(Ug), dev(Lg)) == expect_flags
 
 
-@pytest.mark.parametrize("sched", ["auto", "t128", "sym", "one", "one_sym", "pairs"])
+@pytest.mark.parametrize("sched", ["auto", "t128", "sym", "one", "one_sym", "pairs", "pairs_sym"])
 def test_batched_chains(sched):
     """Batch of 256 molecules n=512 in one call; every 32nd molecule against the
     oracle, all molecules against a per-molecule GPU call."""

@@ -252,13 +252,15 @@ def test_column_panel_is_the_transposed_row_panel_in_fp32():
 
 # ---------------------------------------------------------------- block rounds in pairs
 
-def pair_schedule(nb):
-    """The launches of the pair schedule (128-wide tiles, general inputs), in
+def pair_schedule(nb, sym=False):
+    """The launches of the pair schedule (128-wide tiles), in
     the library's host order, as (stream, kind, K, tiles, rounds, waits):
     stream "s" (the caller's) or "side"; kind "p1", "p2" or "p3"; waits: the
     names of events the launch waits for first.  Events are ("rec", name)
     entries.  The sets are written from their definitions (block-rows and
-    -columns), not from the device code's index maps."""
+    -columns), not from the device code's index maps.  sym: every phase-3
+    set keeps its tiles on and above the diagonal, the panels are written on
+    both sides, and a last launch ("mirror") writes the lower triangle."""
     def rng(*excl):
         return [x for x in range(nb) if x not in excl]
 
@@ -273,7 +275,11 @@ def pair_schedule(nb):
         return {(i, j) for i in rng(K, K + 1) for j in rng(K, K + 1) if i in rows or j in rows}
 
     out = []
-    add = out.append
+
+    def add(e):
+        if sym and len(e) == 5 and e[1] == "p3":
+            e = e[:3] + ({(i, j) for (i, j) in e[3] if i <= j},) + e[4:]
+        out.append(e)
     add(("s", "p1", 0, {(0, 0)}, (0,)))
     add(("s", "p2", 0, tiles_panels(0), (0,)))
     add(("rec", "s", "M"))
@@ -310,6 +316,8 @@ def pair_schedule(nb):
     add(("wait", "s", "J"))
     if K == nb - 1:
         add(("s", "p3", K, {(i, j) for i in rng(K) for j in rng(K)}, (K,)))
+    if sym:
+        add(("s", "mirror", -1, {(i, j) for i in range(nb) for j in range(i)}, ()))
     return out
 
 
@@ -337,6 +345,8 @@ def launches_with_order(entries):
 def reads_writes(launch):
     _, kind, K, tiles, rounds = launch
     writes = set(tiles)
+    if kind == "mirror":
+        return {(j, i) for (i, j) in tiles}, writes
     reads = set(tiles)
     for (i, j) in tiles:
         for k in rounds:
@@ -347,11 +357,12 @@ def reads_writes(launch):
 
 
 @pytest.mark.parametrize("nb", list(range(3, 14)))
-def test_pair_schedule_has_no_race(nb):
+@pytest.mark.parametrize("sym", [False, True])
+def test_pair_schedule_has_no_race(nb, sym):
     """Launches that may run side by side (neither ordered before the other by
     its stream or an event) touch disjoint tiles: no write meets a read or a
     write of the other."""
-    launches, before = launches_with_order(pair_schedule(nb))
+    launches, before = launches_with_order(pair_schedule(nb, sym))
     rw = [reads_writes(x) for x in launches]
     for b in range(len(launches)):
         for a in range(b):
@@ -362,33 +373,49 @@ def test_pair_schedule_has_no_race(nb):
 
 
 @pytest.mark.parametrize("nb", list(range(3, 14)))
-def test_pair_schedule_updates_every_tile_with_every_round(nb):
-    """Each tile takes every block round exactly once, in increasing order,
-    across the launches in any order the dependencies allow (checked along
-    the host order, which is one of them)."""
-    launches, _ = launches_with_order(pair_schedule(nb))
+@pytest.mark.parametrize("sym", [False, True])
+def test_pair_schedule_updates_every_tile_with_every_round(nb, sym):
+    """Each tile (with symmetric inputs: each tile on or above the diagonal)
+    takes every block round exactly once, in increasing order, across the
+    launches in any order the dependencies allow (checked along the host
+    order, which is one of them)."""
+    launches, _ = launches_with_order(pair_schedule(nb, sym))
     done = {(i, j): [] for i in range(nb) for j in range(nb)}
     for _, kind, K, tiles, rounds in launches:
-        for t in tiles:
-            done[t].extend(rounds)
-    for t, r in done.items():
-        assert r == list(range(nb)), (nb, t, r)
+        for (i, j) in tiles:
+            if kind != "mirror" and (not sym or i <= j):
+                done[(i, j)].extend(rounds)
+    for (i, j), r in done.items():
+        if not sym or i <= j:
+            assert r == list(range(nb)), (nb, (i, j), r)
 
 
-def smooth_pair_schedule(U0, L0, B):
+def smooth_pair_schedule(U0, L0, B, sym=False):
     """Run the pair schedule's launches in host order on integer matrices: a
     phase-3 launch reads, for each tile, its operands of every round it
-    applies before writing (one pass), then writes the tile."""
+    applies before writing (one pass), then writes the tile.  sym: the tiles
+    below the diagonal are poisoned first (values that would change any
+    result they reached), as nothing may read them before they are
+    written."""
     n = U0.shape[0]
     nb = (n + B - 1) // B
     U, L = U0.astype(np.int64), L0.astype(np.int64)
     sl = [slice(t * B, min(n, (t + 1) * B)) for t in range(nb)]
+    if sym:
+        for I in range(nb):
+            for J in range(I):
+                U[sl[I], sl[J]] = 0
+                L[sl[I], sl[J]] = 1 << 29
 
     def tile(I, J):
         return U[sl[I], sl[J]].copy(), L[sl[I], sl[J]].copy()
 
-    launches, _ = launches_with_order(pair_schedule(nb))
+    launches, _ = launches_with_order(pair_schedule(nb, sym))
     for _, kind, K, tiles, rounds in launches:
+        if kind == "mirror":
+            for (I, J) in tiles:
+                U[sl[I], sl[J]], L[sl[I], sl[J]] = U[sl[J], sl[I]].T, L[sl[J], sl[I]].T
+            continue
         if kind == "p1":
             du, dl = tile(K, K)
             U[sl[K], sl[K]], L[sl[K], sl[K]] = (a.astype(np.int64) for a in oracle.smooth(
@@ -396,6 +423,8 @@ def smooth_pair_schedule(U0, L0, B):
             continue
         new = {}
         for (I, J) in tiles:
+            if kind == "p2" and sym and I > J:
+                continue        # the upper-side panel tile, stored on both sides
             X = tile(I, J)
             if kind == "p2":
                 D = tile(K, K)
@@ -404,6 +433,8 @@ def smooth_pair_schedule(U0, L0, B):
                 for k in rounds:
                     X = plus(X, product(tile(I, k), tile(k, J)))
             new[(I, J)] = X
+            if kind == "p2" and sym:
+                new[(J, I)] = (X[0].T, X[1].T)
         for (I, J), X in new.items():
             U[sl[I], sl[J]], L[sl[I], sl[J]] = X
     return U, L
@@ -416,4 +447,12 @@ def test_pair_schedule_equals_the_oracle(n, B, seed):
                              symmetric=bool(seed))
     Uo, Lo = oracle.smooth(Uq, Lq)
     Us, Ls = smooth_pair_schedule(Uq, Lq, B)
+    assert np.array_equal(Us, Uo) and np.array_equal(Ls, Lo)
+
+
+@pytest.mark.parametrize("n,B", [(12, 4), (13, 3), (17, 2), (25, 3), (9, 3), (21, 2)])
+def test_symmetric_pair_schedule_equals_the_oracle(n, B):
+    Uq, Lq = W.random_bounds(n, 5300 + n, p_known=0.4, p_bad=0.05)
+    Uo, Lo = oracle.smooth(Uq, Lq)
+    Us, Ls = smooth_pair_schedule(Uq, Lq, B, sym=True)
     assert np.array_equal(Us, Uo) and np.array_equal(Ls, Lo)
