@@ -62,7 +62,7 @@ def tile_size(n, flags=0, batch=1, upper=False):
     upper: bs_smooth_upper, U alone)."""
     if flags & (1 << 5):
         return 64
-    if flags & ((1 << 6) | (1 << 12)):     # BS_TILE_128, BS_PAIRED_ROUNDS
+    if flags & ((1 << 6) | (1 << 12)):     # BS_TILE_128, BS_PAIRED_ROUNDS (without BS_TILE_64)
         return 128
     nb = (n + 127) // 128
     if not upper and not flags & (1 << 8) and nb >= PAIRS_FROM:   # general inputs, in pairs
@@ -129,16 +129,24 @@ def merged_lookahead(n, fb, batch, sms, sym=False):
     return rest * batch < 0.5 * sms
 
 
-PAIRS_FROM = 48   # block rows from which 128-wide tiles take block rounds in pairs
+PAIRS_FROM = 48        # block rows from which 128-wide tiles take block rounds in pairs
+PAIRS_TILES_64 = 2500  # bulk tiles of a pair (over the batch) from which 64-wide tiles do
 
 
-def pair_schedule_runs(n, fb, flags=0, sym=False):
-    """The library's rule for taking block rounds in pairs (128-wide tiles,
-    general inputs, look-ahead on; forced by BS_PAIRED_ROUNDS)."""
+def pair_schedule_runs(n, fb, flags=0, sym=False, batch=1):
+    """The library's rule for taking block rounds in pairs (look-ahead on;
+    forced by BS_PAIRED_ROUNDS): 128-wide tiles from 48 block rows, 64-wide
+    ones once a pair's bulk holds 2500 tiles over the batch."""
     nb = (n + fb - 1) // fb
-    if fb != 128 or sym or nb < 3 or flags & (1 << 7):
+    if nb < 3 or flags & (1 << 7):
         return False
-    return bool(flags & (1 << 12)) or nb >= PAIRS_FROM
+    if flags & (1 << 12):
+        return True
+    if fb == 128:
+        return nb >= PAIRS_FROM
+    r = nb - 4
+    rest2 = 0 if r <= 0 else (r * (r + 1) // 2 if sym else r * r)
+    return rest2 * batch >= PAIRS_TILES_64
 
 
 def main_stream_phase3(n, fb, flags=0, batch=1, sms=152, pairs=None):
@@ -170,7 +178,7 @@ def main_stream_phase3(n, fb, flags=0, batch=1, sms=152, pairs=None):
 
     if nb < 2:
         return 0, 0
-    if pair_schedule_runs(n, fb, flags) if pairs is None else pairs:
+    if pair_schedule_runs(n, fb, flags, batch=batch) if pairs is None else pairs:
         K = 0
         while K + 1 < nb:
             block = set(range(K, min(K + 4, nb)))
@@ -684,7 +692,7 @@ def main():
             "algorithmic_bytes_basis": "16 bytes per tile cell per pass: each output tile of U "
                                        "and L read and written once per pass, a pass applying "
                                        "one block round, or two where rounds go in pairs",
-            "schedule": "block rounds in pairs" if pair_schedule_runs(n, fb, flags)
+            "schedule": "block rounds in pairs" if pair_schedule_runs(n, fb, flags, batch=1)
                         else "one block round per pass",
             "frac_of_instruction_mix_ceiling": (p3_achieved / OPS_PER_CELL / mix_peak_cells)
                                                if p3_achieved else None,

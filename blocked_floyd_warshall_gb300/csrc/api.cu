@@ -122,6 +122,21 @@ void release_side(DeviceState* d, const SideCtx& c) {
 // 4.4-4.8 / 5.5: with few rows the side stream's chain per pair (two serial
 // phase-1 closures among the rest) outlasts the pair's bulk.
 constexpr int PAIRS_FROM = 48;
+// 64-wide tiles take block rounds in pairs once a pair's bulk (REST2) holds
+// at least this many tiles over the batch.  Measured (ms, one round per pass
+// against pairs): n = 4096 (3600 tiles) 12.88 / 12.45, n = 6000 39.5 / 37.7,
+// int32 n = 4096 13.65 / 13.26, 256 x n = 512 (4096) 6.22 / 6.01, symmetric
+// 256 x n = 512 (2560) 3.76 / 3.69, symmetric n = 8192 (7750) 50.6 / 47.9;
+// n = 3000 (1849) 5.56 / 5.54, symmetric n = 4096 (1830) 7.15 / 7.57,
+// n = 2048 (784) 2.14 / 2.47, n = 1000 0.59 / 0.86.
+constexpr double PAIRS_TILES_64 = 2500.0;
+
+bool pairs_pay(const bs::Mats& m, int nb) {
+    if (m.fb == bs::FB_LARGE) return nb >= PAIRS_FROM;
+    const double r = nb - 4.0;
+    const double rest2 = r <= 0 ? 0.0 : m.sym ? r * (r + 1) / 2 : r * r;
+    return rest2 * m.batch >= PAIRS_TILES_64;
+}
 
 // Tile size for the blocked schedule: 128 x 128 from PAIRS_FROM block rows
 // of 128 for general inputs (single matrices from n = 6017 on; symmetric
@@ -143,7 +158,7 @@ constexpr int PAIRS_FROM = 48;
 // 17.7 ms; n = 3000, 529 tiles: 3.3 against 2.6 ms).
 int choose_tile(int n, int batch, int mode, bool bounds) {
     if (mode & BS_TILE_64) return bs::FB_SMALL;
-    if (mode & (BS_TILE_128 | BS_PAIRED_ROUNDS)) return bs::FB_LARGE;
+    if (mode & (BS_TILE_128 | BS_PAIRED_ROUNDS)) return bs::FB_LARGE;   // pairs: 128 unless 64 is asked
     const double nb = (double)((n + bs::FB_LARGE - 1) / bs::FB_LARGE);
     if (bounds && !(mode & BS_SYMMETRIC) && nb >= PAIRS_FROM) return bs::FB_LARGE;   // in pairs
     const double from = bounds ? 9000.0 : 768.0;
@@ -173,7 +188,7 @@ int choose_tile(int n, int batch, int mode, bool bounds) {
 // round K, and phase 3 of round K+1 for phase 2 of round K+1.  With
 // symmetric inputs a last launch on `s` writes the lower triangle as the
 // transpose of the upper one.
-// Block rounds in pairs (K, K+1), K even: 128-wide tiles.
+// Block rounds in pairs (K, K+1), K even (see pairs_pay for when).
 // The bulk of the tiles -- outside block-rows and -columns K .. K+3 -- takes
 // both rounds in one pass (P3_REST2, on `s`), so each is loaded and stored
 // once per pair instead of once per round (n = 16384 without look-ahead:
@@ -254,7 +269,7 @@ cudaError_t run_blocked(bool is_int, const bs::Mats& m, cudaStream_t s, bool loo
     SideCtx c;
     e = acquire_side(d, &c);
     if (e != cudaSuccess) return e;
-    if (m.fb == bs::FB_LARGE && (force_pairs || nb >= PAIRS_FROM)) {
+    if (force_pairs || pairs_pay(m, nb)) {
         e = run_pairs(is_int, m, s, nb, c);
         release_side(d, c);
         return e;
@@ -356,8 +371,7 @@ bs_status check_args(const void* U, const void* L, bool bounds, int n, int ld,
     if ((mode & BS_PERK_PAIRED) && !(mode & BS_PERK)) return BS_ERR_ARG;
     if ((mode & BS_ONE_LAUNCH) && (mode & (BS_PERK | BS_TILE_128 | BS_NO_LOOKAHEAD)))
         return BS_ERR_ARG;
-    if ((mode & BS_PAIRED_ROUNDS) &&
-        (mode & (BS_PERK | BS_ONE_LAUNCH | BS_TILE_64 | BS_NO_LOOKAHEAD)))
+    if ((mode & BS_PAIRED_ROUNDS) && (mode & (BS_PERK | BS_ONE_LAUNCH | BS_NO_LOOKAHEAD)))
         return BS_ERR_ARG;
     if ((mode & BS_DTYPE_MASK) > BS_INT32_Q10) return BS_ERR_ARG;
     if (n < 0 || batch < 0) return BS_ERR_ARG;

@@ -370,8 +370,8 @@ __device__ __forceinline__ void p3_update_tile(T* __restrict__ U, T* __restrict_
     // K2 >= 0: block round K2 too, in the same pass (its panels final, the
     // tile's own values after round K are never needed: min and max are
     // exact, so folding both rounds' products in changes no bit)
-    // (the pair schedule runs on 128-wide tiles only)
-    constexpr bool PAIRS = FB == FB_LARGE;
+    // (the pair schedule runs the 8 x 8 and 8 x 4 forms, not the wide one)
+    constexpr bool PAIRS = !WIDE;
     const int ok2 = PAIRS ? K2 * FB : 0, mk2 = PAIRS && K2 >= 0 ? min(FB, n - ok2) : 0;
     const int n1 = (mk + BK - 1) / BK;
     const int nchunks = n1 + (PAIRS ? (mk2 + BK - 1) / BK : 0);

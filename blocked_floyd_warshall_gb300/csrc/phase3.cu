@@ -19,7 +19,7 @@ k_phase3(T* __restrict__ U, T* __restrict__ L, int n, int ld, long long bstride,
     if (HAS_L) L += off;
     const int nb = (n + FB - 1) / FB;
     int I, J;
-    if (FB == FB_LARGE && part >= P3_REST2) p3_tile_pair(part, sym, blockIdx.x, nb, K, I, J);
+    if (!WIDE && part >= P3_REST2) p3_tile_pair(part, sym, blockIdx.x, nb, K, I, J);
     else p3_tile(part, sym, blockIdx.x, nb, K, I, J);
     const bool two = part == P3_REST2 || part == P3_NEAR2;   // rounds K and K+1
     p3_update_tile<T, HAS_L, FB, WIDE>(U, L, n, ld, I, J, K, vec, sym && part == P3_PANELS,
@@ -335,7 +335,8 @@ static cudaError_t strip_t(const Mats& m, int K, int part, cudaStream_t s) {
 template <class T, bool HAS_L>
 static cudaError_t phase3_fb(const Mats& m, int K, int part, cudaStream_t s) {
     if (m.fb == FB_LARGE) return phase3_t<T, HAS_L, FB_LARGE, false>(m, K, part, s);
-    if (part >= P3_REST2) return cudaErrorInvalidValue;   // the pair schedule: 128-wide tiles
+    // the pair schedule's sets: always the 8 x 4 form (the only 64-wide form with their maps)
+    if (part >= P3_REST2) return phase3_t<T, HAS_L, FB_SMALL, false>(m, K, part, s);
     const int nb = (m.n + FB_SMALL - 1) / FB_SMALL;
     const double ctas = (double)p3_tiles(m.sym, part, nb, K) * m.batch;
     if (2.0 * ctas <= m.sms) return strip_t<T, HAS_L, 4>(m, K, part, s);

@@ -116,12 +116,14 @@ enum {
                                  barriers only; same results.  Meant for
                                  batches of small molecules.  With BS_PERK,
                                  BS_TILE_128 or BS_NO_LOOKAHEAD: BS_ERR_ARG */
-    BS_PAIRED_ROUNDS = 1 << 12, /* blocked mode: 128 x 128 tiles, block rounds
-                                 taken in pairs whatever the size (the bulk
-                                 tiles update both rounds of a pair in one
-                                 pass; by default from 48 block rows on, with
-                                 128-wide tiles); same results.  With
-                                 BS_PERK, BS_ONE_LAUNCH, BS_TILE_64 or
+    BS_PAIRED_ROUNDS = 1 << 12, /* blocked mode: block rounds taken in pairs
+                                 whatever the size (the bulk tiles update
+                                 both rounds of a pair in one pass), on
+                                 128 x 128 tiles unless BS_TILE_64 is given;
+                                 by default pairs run from 48 block rows of
+                                 128, and on 64-wide tiles once a pair's bulk
+                                 holds 2500 tiles over the batch; same
+                                 results.  With BS_PERK, BS_ONE_LAUNCH or
                                  BS_NO_LOOKAHEAD: BS_ERR_ARG */
     BS_SYMMETRIC = 1 << 8     /* blocked mode, symmetric U and L (both triangles
                                  stored, section 6): only tiles on and above the

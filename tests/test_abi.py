@@ -94,7 +94,6 @@ def no_gpu():
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_ONE_LAUNCH | bsm.BS_NO_LOOKAHEAD), bsm.BS_ERR_ARG),
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_PAIRED_ROUNDS | bsm.BS_PERK), bsm.BS_ERR_ARG),
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_PAIRED_ROUNDS | bsm.BS_ONE_LAUNCH), bsm.BS_ERR_ARG),
-    ((FAKE, FAKE2, 8, 8, None, bsm.BS_PAIRED_ROUNDS | bsm.BS_TILE_64), bsm.BS_ERR_ARG),
     ((FAKE, FAKE2, 8, 8, None, bsm.BS_PAIRED_ROUNDS | bsm.BS_NO_LOOKAHEAD), bsm.BS_ERR_ARG),
     ((None, FAKE2, 8, 8, None, 0), bsm.BS_ERR_ARG),                       # null U
     ((FAKE, None, 8, 8, None, 0), bsm.BS_ERR_ARG),                        # null L

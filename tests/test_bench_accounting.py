@@ -158,16 +158,26 @@ def test_single_round_main_stream_cells(n, fb):
 
 
 def test_pair_schedule_rule():
-    """128-wide tiles, general inputs, look-ahead: pairs from 48 block rows on
-    (n = 6017), or forced by BS_PAIRED_ROUNDS."""
+    """Look-ahead on: 128-wide tiles take block rounds in pairs from 48 block
+    rows (n = 6017), 64-wide ones once a pair's bulk ((nb - 4)^2 tiles, or
+    (nb - 4)(nb - 3) / 2 with symmetric inputs) holds 2500 tiles over the
+    batch; BS_PAIRED_ROUNDS forces them."""
     assert bench.pair_schedule_runs(16384, 128)
     assert bench.pair_schedule_runs(6017, 128)
     assert not bench.pair_schedule_runs(6016, 128)
+    assert bench.pair_schedule_runs(16384, 128, sym=True)
     assert bench.pair_schedule_runs(300, 128, flags=1 << 12)
-    assert not bench.pair_schedule_runs(16384, 64)
-    assert not bench.pair_schedule_runs(16384, 128, sym=True)
     assert not bench.pair_schedule_runs(16384, 128, flags=1 << 7)
+    assert bench.pair_schedule_runs(4096, 64)                        # 60^2 = 3600
+    assert not bench.pair_schedule_runs(3000, 64)                    # 43^2 = 1849
+    assert bench.pair_schedule_runs(3456, 64)                        # 50^2 = 2500
+    assert not bench.pair_schedule_runs(3392, 64)                    # 49^2 = 2401
+    assert bench.pair_schedule_runs(512, 64, batch=256)              # 16 x 256 = 4096
+    assert not bench.pair_schedule_runs(4096, 64, sym=True)          # 60 x 61 / 2 = 1830
+    assert bench.pair_schedule_runs(8192, 64, sym=True)              # 124 x 125 / 2 = 7750
+    assert bench.pair_schedule_runs(300, 64, flags=1 << 12)
     assert bench.tile_size(300, flags=1 << 12) == 128
+    assert bench.tile_size(300, flags=(1 << 12) | (1 << 5)) == 64
 
 
 def test_instruction_mix_ceiling():

@@ -51,6 +51,7 @@ SCHEDULES = {
     "one_sym": bsm.BS_ONE_LAUNCH | bsm.BS_SYMMETRIC,
     "pairs": bsm.BS_PAIRED_ROUNDS,
     "pairs_sym": bsm.BS_PAIRED_ROUNDS | bsm.BS_SYMMETRIC,
+    "pairs64": bsm.BS_PAIRED_ROUNDS | bsm.BS_TILE_64,
 }
 # every algorithm: the blocked schedules and both per-round forms
 ALGOS = dict(SCHEDULES, perk=bsm.BS_PERK, perk2=bsm.BS_PERK | bsm.BS_PERK_PAIRED)
@@ -90,7 +91,7 @@ def test_blocked_matches_oracle(n, dtype, sched):
 @pytest.mark.parametrize("n", [1, 2, 5, 63, 64, 65, 127, 129, 257, 300, 513])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
 @pytest.mark.parametrize("sched", ["auto", "t64", "t128", "t64_serial", "t128_serial", "one",
-                                   "pairs"])
+                                   "pairs", "pairs64"])
 def test_symmetric_mode_matches_oracle(n, dtype, sched):
     """Half the tiles computed and mirrored: bit-identical to the oracle."""
     Uq, Lq = W.random_bounds(n, 2500 + n, p_known=0.2, p_bad=0.02)
@@ -102,7 +103,7 @@ def test_symmetric_mode_matches_oracle(n, dtype, sched):
 
 
 @pytest.mark.parametrize("n", [65, 300, 513])
-@pytest.mark.parametrize("algo", ["t64", "t128", "one", "pairs"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "one", "pairs", "pairs64"])
 def test_symmetric_upper_only(n, algo):
     Uq, _ = W.random_bounds(n, 5500 + n, p_known=0.25)
     Uo = oracle.smooth_upper(Uq)
@@ -112,7 +113,7 @@ def test_symmetric_upper_only(n, algo):
 
 @pytest.mark.parametrize("n", [997, 1001, 1003])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "sym", "t128", "one", "pairs", "pairs_sym"])
+@pytest.mark.parametrize("sched", ["auto", "sym", "t128", "one", "pairs", "pairs_sym", "pairs64"])
 def test_blocked_tails_near_1000(n, dtype, sched):
     """Sizes around the n = 1000 chain with ragged last tiles (37, 41, 43 rows
     of 64; 101, 105, 107 of 128), a padded leading dimension n + 5 with
@@ -126,7 +127,7 @@ def test_blocked_tails_near_1000(n, dtype, sched):
 
 
 @pytest.mark.parametrize("n", [129, 300])
-@pytest.mark.parametrize("sched", ["t64", "t128", "pairs"])
+@pytest.mark.parametrize("sched", ["t64", "t128", "pairs", "pairs64"])
 def test_blocked_asymmetric(n, sched):
     Uq, Lq = W.random_bounds(n, 3000 + n, p_known=0.3, p_bad=0.02, symmetric=False)
     Uo, Lo = oracle.smooth(Uq, Lq)
@@ -136,7 +137,7 @@ def test_blocked_asymmetric(n, sched):
 
 @pytest.mark.parametrize("n,ld,offset", [(130, 140, 0), (130, 133, 0), (257, 260, 1),
                                          (97, 101, 3), (200, 200, 1)])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs", "pairs64"])
 def test_leading_dimension_and_misalignment(n, ld, offset, algo):
     """ld > n keeps the padding untouched; ld % 4 != 0 or a base not 16-byte
     aligned takes the scalar-IO instantiation with identical results."""
@@ -151,7 +152,7 @@ def test_leading_dimension_and_misalignment(n, ld, offset, algo):
 
 @pytest.mark.parametrize("n", [1, 5, 128, 129, 300, 513])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs", "pairs64"])
 def test_upper_only(n, dtype, algo):
     Uq, _ = W.random_bounds(n, 5000 + n, p_known=0.25)
     U0 = W.to_f32(Uq) if dtype == "f32" else Uq
@@ -210,7 +211,7 @@ def off_grid(n, seed, p_bad, symmetric=True):
 
 
 @pytest.mark.parametrize("n,p_bad", [(300, 0.0), (300, 0.02), (700, 0.01)])
-@pytest.mark.parametrize("sched", ["t64", "t128", "sym", "pairs", "pairs_sym"])
+@pytest.mark.parametrize("sched", ["t64", "t128", "sym", "pairs", "pairs_sym", "pairs64"])
 def test_fp32_off_grid_within_tolerance(n, p_bad, sched):
     """Off the 1/1024 grid fp32 sums round, so the schedule changes the last
     bits.  Against the fp64 oracle on the same fp32 inputs:
@@ -308,7 +309,7 @@ def edge_cases():
 
 
 @pytest.mark.parametrize("case", sorted(edge_cases()))
-@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs"])
+@pytest.mark.parametrize("algo", ["t64", "t128", "perk", "perk2", "one", "pairs", "pairs64"])
 def test_edge_cases(case, algo):
     Uq, Lq = edge_cases()[case]
     flags = ALGOS[algo]
@@ -398,7 +399,8 @@ def globule4096():
     return m, Uo, Lo
 
 
-@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial", "sym", "pairs", "pairs_sym"])
+@pytest.mark.parametrize("sched", ["auto", "t64", "t128_serial", "sym", "pairs", "pairs_sym",
+                                   "pairs64"])
 def test_globule_4096_int32_blocked(globule4096, sched):
     m, Uo, Lo = globule4096
     Ug, Lg, ok = gpu_bounds(m["U"], m["L"], SCHEDULES[sched])
@@ -420,7 +422,8 @@ def test_globule_4096_fp32_blocked_and_per_round(globule4096):
         assert bsm.bs_check_feasible(dev(Ug), dev(Lg)) == expect_flags
 
 
-@pytest.mark.parametrize("sched", ["auto", "t128", "sym", "one", "one_sym", "pairs", "pairs_sym"])
+@pytest.mark.parametrize("sched", ["auto", "t128", "sym", "one", "one_sym", "pairs", "pairs_sym",
+                                   "pairs64"])
 def test_batched_chains(sched):
     """Batch of 256 molecules n=512 in one call; every 32nd molecule against the
     oracle, all molecules against a per-molecule GPU call."""
@@ -441,7 +444,7 @@ def test_batched_chains(sched):
 
 @pytest.mark.parametrize("n,B", [(200, 3), (300, 4), (257, 12), (130, 40)])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
-@pytest.mark.parametrize("sched", ["auto", "sym", "one"])
+@pytest.mark.parametrize("sched", ["auto", "sym", "one", "pairs64"])
 def test_batched_small_molecules(n, B, dtype, sched):
     """Small batches of small molecules: the launches take the strip forms
     (four or two CTAs per tile) or the 256-thread form depending on the
