@@ -151,7 +151,8 @@ def pair_schedule_runs(n, fb, flags=0, sym=False, batch=1):
 
 def main_stream_phase3(n, fb, flags=0, batch=1, sms=152, pairs=None):
     """Phase-3 launches of one blocked smoothing on the caller's stream
-    (general inputs, look-ahead on): (cell updates, tile cells passed over).
+    (general inputs, look-ahead on; the roofline's schedule): (cell updates,
+    tile cells passed over).
     A pass over an r x c tile reads and writes it once, whatever the middle
     atoms it applies, so 16 bytes per tile cell (U and L, fp32) are the
     algorithmic DRAM traffic of a pass.
@@ -234,15 +235,41 @@ def load_peaks():
 KERNEL_SOURCES = ("phase3.cu", "p3_tile.cuh", "pairops.cuh", "bs_tile.cuh", "bs_types.cuh")
 
 
+def code_only(text):
+    """C++ source without its comments, whitespace runs collapsed: what the
+    compiler sees, so that the kernel hash ignores edits to comments."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_hash():
     """Hash of the phase-3 kernel's code (its source file, the device helpers
     and the types it includes; not the host-side declarations of the other
-    kernels): ties a committed ncu traffic figure to the code."""
+    kernels), comments left out: ties a committed ncu traffic figure to the
+    code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blocked_floyd_warshall_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update((f + "\n" + code_only(fh.read())).encode())
     return h.hexdigest()[:16]
 
 

@@ -155,7 +155,7 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
 //   P3_ALL_OFF: P3_ALL without tile (K+1,K+1), whose update phase 1 of round
 //               K+1 takes over;
 //   P3_PANELS : phase 2, the row panel (K,J) then the column panel (I,K).
-// Block rounds in pairs (K, K+1), general inputs only (see run_blocked):
+// Block rounds in pairs (K, K+1) (see run_pairs; symmetric forms below):
 //   P3_REST2  : tiles outside block-rows and -columns K .. K+3, rounds K and
 //               K+1 in one pass;
 //   P3_NEAR2  : tiles in block-rows or -columns K+2, K+3, outside K and K+1,
@@ -164,9 +164,9 @@ __device__ __forceinline__ void p3_stage(T* stage, const T* U, const T* L, size_
 //               or -column K-1 outside K .. K+2, round K;
 //   P3_CORNER2: (the same) tiles (K+1,K-1), (K+2,K-1), (K-1,K+1), (K-1,K+2),
 //               round K.
-// With symmetric inputs only tiles with I <= J are computed: (nb-1)nb/2,
-// nb-1, (nb-2)(nb-1)/2 and (nb-1)nb/2 - 1 tiles.  Phase 2 computes, for each
-// block column j != K, the panel tile on the upper side -- (K,j) for j > K,
+// With symmetric inputs only tiles with I <= J are computed (the first four
+// sets: (nb-1)nb/2, nb-1, (nb-2)(nb-1)/2 and (nb-1)nb/2 - 1 tiles).  Phase 2
+// computes, for each block column j != K, the panel tile on the upper side -- (K,j) for j > K,
 // the column panel tile (j,K) for j < K -- and stores it also transposed, so
 // that both panels are whole for phase 3.  Phase-3 tiles are stored once:
 // no later step reads a tile below the diagonal but a panel, and the lower

@@ -199,3 +199,14 @@ def test_committed_phase3_capture_is_current():
     per_pass_cell = d["dram_bytes_per_pass_cell"]
     assert per_pass_cell == pytest.approx(
         (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["tile_cells_per_launch"])
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The hash that ties the committed capture to the kernel sees code, not
+    comments or layout: a changed comment keeps it, changed code does not."""
+    a = "int f(int x) { return x + 1; }  // add one\n"
+    b = "/* the successor */ int f(int x) {\n    return x + 1;\n}\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert bench.code_only('s = "// kept";') == 's = "// kept";'
