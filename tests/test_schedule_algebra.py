@@ -410,14 +410,25 @@ def smooth_pair_schedule(U0, L0, B, sym=False):
     def tile(I, J):
         return U[sl[I], sl[J]].copy(), L[sl[I], sl[J]].copy()
 
-    launches, _ = launches_with_order(pair_schedule(nb, sym))
+    return run_schedule(U, L, sl, pair_schedule(nb, sym), sym)
+
+
+def run_schedule(U, L, sl, entries, sym=False):
+    """Execute a launch list (see pair_schedule) in host order on the tiles of
+    U and L (int64, in place; sl: the block slices)."""
+    def tile(I, J):
+        return U[sl[I], sl[J]].copy(), L[sl[I], sl[J]].copy()
+
+    launches, _ = launches_with_order(entries)
     for _, kind, K, tiles, rounds in launches:
         if kind == "mirror":
             for (I, J) in tiles:
                 U[sl[I], sl[J]], L[sl[I], sl[J]] = U[sl[J], sl[I]].T, L[sl[J], sl[I]].T
             continue
-        if kind == "p1":
+        if kind in ("p1", "p1pre"):
             du, dl = tile(K, K)
+            if kind == "p1pre":     # round K-1's product first, then the closure
+                du, dl = plus((du, dl), product(tile(K, K - 1), tile(K - 1, K)))
             U[sl[K], sl[K]], L[sl[K], sl[K]] = (a.astype(np.int64) for a in oracle.smooth(
                 du.astype(np.int32), dl.astype(np.int32)))
             continue
@@ -456,3 +467,123 @@ def test_symmetric_pair_schedule_equals_the_oracle(n, B):
     Uo, Lo = oracle.smooth(Uq, Lq)
     Us, Ls = smooth_pair_schedule(Uq, Lq, B, sym=True)
     assert np.array_equal(Us, Uo) and np.array_equal(Ls, Lo)
+
+
+
+# ---------------------------------------------------------------- one block round per pass
+
+def single_round_schedule(nb, mode, drop_side_wait=False):
+    """The launch list of the look-ahead schedule with one block round per
+    pass, as the library enqueues it (mode "loose": the rest of round K starts
+    after phase 2 of round K; "tight": after the next block row and column;
+    "merged": small 64-wide matrices, phase 3 of round K but tile (K+1,K+1)
+    on the caller's stream beside phase 1 of K+1, which applies round K to
+    that tile first).  drop_side_wait: a planted mistake, the side stream no
+    longer waits for the rest of the previous round."""
+    def rng(*excl):
+        return [x for x in range(nb) if x not in excl]
+
+    def panels(K):
+        return {(K, j) for j in rng(K)} | {(i, K) for i in rng(K)}
+
+    def nxt(K):
+        return {(K + 1, j) for j in rng(K)} | {(i, K + 1) for i in rng(K, K + 1)}
+
+    def rest(K):
+        return {(i, j) for i in rng(K, K + 1) for j in rng(K, K + 1)}
+
+    out = []
+    add = out.append
+    add(("s", "p1", 0, {(0, 0)}, (0,)))
+    add(("s", "p2", 0, panels(0), (0,)))
+    add(("rec", "s", "M1"))                 # stands for the rest of round -1
+    forked = False
+    for K in range(nb - 1):
+        m_cur, m_prev = "M%d" % (K & 1), "M%d" % ((K + 1) & 1)
+        if mode == "merged":
+            if forked:
+                add(("wait", "s", "SD"))
+            forked = False
+            add(("s", "p3", K, {(i, j) for i in rng(K) for j in rng(K)} - {(K + 1, K + 1)}, (K,)))
+            add(("rec", "s", m_cur))
+            add(("wait", "side", m_prev))
+            forked = True
+            add(("side", "p1pre", K + 1, {(K + 1, K + 1)}, (K, K + 1)))
+            add(("wait", "side", m_cur))
+            add(("side", "p2", K + 1, panels(K + 1), (K + 1,)))
+            add(("rec", "side", "SD"))
+            continue
+        if mode == "loose":
+            if forked:
+                add(("wait", "s", "SD"))
+            forked = False
+            add(("s", "p3", K, rest(K), (K,)))
+            add(("rec", "s", m_cur))
+        if not drop_side_wait:
+            add(("wait", "side", m_prev))
+        forked = True
+        add(("side", "p3", K, nxt(K), (K,)))
+        if mode == "tight":
+            add(("rec", "side", "ND"))
+        add(("side", "p1", K + 1, {(K + 1, K + 1)}, (K + 1,)))
+        add(("side", "p2", K + 1, panels(K + 1), (K + 1,)))
+        add(("rec", "side", "SD"))
+        if mode == "tight":
+            add(("wait", "s", "ND"))
+            add(("s", "p3", K, rest(K), (K,)))
+            add(("rec", "s", m_cur))
+    if forked:
+        add(("wait", "s", "SD"))
+    add(("s", "p3", nb - 1, {(i, j) for i in rng(nb - 1) for j in rng(nb - 1)}, (nb - 1,)))
+    return out
+
+
+@pytest.mark.parametrize("nb", list(range(3, 13)))
+@pytest.mark.parametrize("mode", ["loose", "tight", "merged"])
+def test_single_round_schedule_has_no_race(nb, mode):
+    """The look-ahead schedules of one round per pass: what the two streams
+    may run side by side touches disjoint tiles."""
+    launches, before = launches_with_order(single_round_schedule(nb, mode))
+    rw = [reads_writes(x) for x in launches]
+    for b in range(len(launches)):
+        for a in range(b):
+            if a in before[b]:
+                continue
+            (ra, wa), (rb, wb) = rw[a], rw[b]
+            assert not (wa & (rb | wb)) and not (wb & ra), (nb, mode, launches[a][1:3],
+                                                             launches[b][1:3])
+
+
+@pytest.mark.parametrize("nb", list(range(3, 13)))
+@pytest.mark.parametrize("mode", ["loose", "tight", "merged"])
+def test_single_round_schedule_updates_every_tile_with_every_round(nb, mode):
+    launches, _ = launches_with_order(single_round_schedule(nb, mode))
+    done = {(i, j): [] for i in range(nb) for j in range(nb)}
+    for _, kind, K, tiles, rounds in launches:
+        for t in tiles:
+            done[t].extend(rounds)
+    for t, r in done.items():
+        assert r == list(range(nb)), (nb, mode, t, r)
+
+
+@pytest.mark.parametrize("n,B", [(12, 4), (13, 3), (17, 2), (9, 3)])
+@pytest.mark.parametrize("mode", ["loose", "tight", "merged"])
+def test_single_round_schedule_equals_the_oracle(n, B, mode):
+    Uq, Lq = W.random_bounds(n, 5400 + n, p_known=0.4, p_bad=0.05, symmetric=False)
+    Uo, Lo = oracle.smooth(Uq, Lq)
+    nb = (n + B - 1) // B
+    U, L = Uq.astype(np.int64), Lq.astype(np.int64)
+    sl = [slice(t * B, min(n, (t + 1) * B)) for t in range(nb)]
+    Us, Ls = run_schedule(U, L, sl, single_round_schedule(nb, mode))
+    assert np.array_equal(Us, Uo) and np.array_equal(Ls, Lo)
+
+
+def test_race_check_catches_a_missing_wait():
+    """Without the side stream's wait for the rest of the previous round,
+    NEXT(K) rewrites panels that REST(K-1) may still be reading: the checker
+    flags it."""
+    launches, before = launches_with_order(single_round_schedule(6, "loose", drop_side_wait=True))
+    rw = [reads_writes(x) for x in launches]
+    races = [(a, b) for b in range(len(launches)) for a in range(b) if a not in before[b]
+             and ((rw[a][1] & (rw[b][0] | rw[b][1])) or (rw[b][1] & rw[a][0]))]
+    assert races
