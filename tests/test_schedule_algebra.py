@@ -19,6 +19,12 @@ with the oracle.
    upper one at the end gives the oracle's result, even with the lower
    triangle poisoned at the start: no step reads a stale tile below the
    diagonal.
+4. Launch lists and barrier phases.  The library's schedules -- block rounds
+   in pairs, one round per pass (loose, tight, merged look-ahead) and the
+   one-launch form's cluster-barrier phases -- written as lists of launches
+   with their streams and events: whatever may run side by side touches
+   disjoint tiles, every tile takes every round once and in order, and
+   running them gives the oracle's result.
 """
 import numpy as np
 import pytest
@@ -587,3 +593,85 @@ def test_race_check_catches_a_missing_wait():
     races = [(a, b) for b in range(len(launches)) for a in range(b) if a not in before[b]
              and ((rw[a][1] & (rw[b][0] | rw[b][1])) or (rw[b][1] & rw[a][0]))]
     assert races
+
+
+# ---------------------------------------------------------------- the one-launch form
+
+def one_launch_phases(nb, sym=False):
+    """The one-launch form (one thread-block cluster per molecule) as phases
+    between its cluster barriers; each phase lists the units its CTAs run side
+    by side, one per tile (kind, K, tiles, rounds): closure of tile (0,0);
+    then per block round K the panels, then every other tile of round K beside
+    rank 0's update and closure of tile (K+1,K+1) (the whole round when K is
+    the last); with symmetric inputs the tiles on and above the diagonal, the
+    panels stored on both sides and the lower triangle written at the end."""
+    def keep(t):
+        return not sym or t[0] <= t[1]
+
+    phases = [[("p1", 0, {(0, 0)}, (0,))]]
+    for K in range(nb):
+        panels = []
+        for j in range(nb):
+            if j == K:
+                continue
+            if sym:
+                t = (K, j) if j > K else (j, K)
+                panels.append(("p2", K, {t, (t[1], t[0])}, (K,)))
+            else:
+                panels += [("p2", K, {(K, j)}, (K,)), ("p2", K, {(j, K)}, (K,))]
+        phases.append(panels)
+        rest = [("p3", K, {(i, j)}, (K,)) for i in range(nb) for j in range(nb)
+                if i != K and j != K and keep((i, j))]
+        if K + 1 < nb:
+            rest = [u for u in rest if (K + 1, K + 1) not in u[2]]
+            rest.append(("p1pre", K + 1, {(K + 1, K + 1)}, (K, K + 1)))
+        phases.append(rest)
+    if sym:
+        phases.append([("mirror", -1, {(i, j)}, ()) for i in range(nb) for j in range(i)])
+    return phases
+
+
+@pytest.mark.parametrize("nb", list(range(2, 10)))
+@pytest.mark.parametrize("sym", [False, True])
+def test_one_launch_phases_have_no_race(nb, sym):
+    """Between two cluster barriers the CTAs' units touch disjoint tiles (a
+    symmetric panel unit writes its tile and the transpose)."""
+    for units in one_launch_phases(nb, sym):
+        rw = []
+        for kind, K, tiles, rounds in units:
+            if kind == "p2":
+                reads = set(tiles) | {(K, K)}
+            else:
+                reads, _ = reads_writes(("", kind, K, tiles, rounds))
+            rw.append((reads, set(tiles)))
+        for b in range(len(rw)):
+            for a in range(b):
+                (ra, wa), (rb, wb) = rw[a], rw[b]
+                assert not (wa & (rb | wb)) and not (wb & ra), (nb, sym, units[a], units[b])
+
+
+@pytest.mark.parametrize("n,B", [(12, 4), (13, 3), (9, 3), (8, 8)])
+@pytest.mark.parametrize("sym", [False, True])
+def test_one_launch_phases_equal_the_oracle(n, B, sym):
+    Uq, Lq = W.random_bounds(n, 5500 + n, p_known=0.4, p_bad=0.05, symmetric=sym)
+    Uo, Lo = oracle.smooth(Uq, Lq)
+    nb = (n + B - 1) // B
+    U, L = Uq.astype(np.int64), Lq.astype(np.int64)
+    sl = [slice(t * B, min(n, (t + 1) * B)) for t in range(nb)]
+    if sym:
+        for I in range(nb):
+            for J in range(I):
+                U[sl[I], sl[J]] = 0
+                L[sl[I], sl[J]] = 1 << 29
+    for units in one_launch_phases(nb, sym):
+        # every unit of a phase reads the state before the phase (they are
+        # disjoint, so the order inside a phase does not matter)
+        entries = []
+        for kind, K, tiles, rounds in units:
+            if kind == "p2" and sym:
+                t = min(tiles)        # the upper-side tile; the unit mirrors it
+                entries.append(("s", "p2", K, {t, (t[1], t[0])}, rounds))
+            else:
+                entries.append(("s", kind, K, tiles, rounds))
+        U, L = run_schedule(U, L, sl, entries, sym)
+    assert np.array_equal(U, Uo) and np.array_equal(L, Lo)
