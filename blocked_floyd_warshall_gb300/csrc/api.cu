@@ -127,8 +127,10 @@ constexpr int PAIRS_FROM = 48;
 // against pairs): n = 4096 (3600 tiles) 12.88 / 12.45, n = 6000 39.5 / 37.7,
 // int32 n = 4096 13.65 / 13.26, 256 x n = 512 (4096) 6.22 / 6.01, symmetric
 // 256 x n = 512 (2560) 3.76 / 3.69, symmetric n = 8192 (7750) 50.6 / 47.9;
-// n = 3000 (1849) 5.56 / 5.54, symmetric n = 4096 (1830) 7.15 / 7.57,
-// n = 2048 (784) 2.14 / 2.47, n = 1000 0.59 / 0.86.
+// n = 3584 (2704) 8.79 / 8.53, symmetric n = 5120 (2926) 12.96 / 12.58,
+// symmetric n = 6144 (4278) 21.97 / 21.10; at the threshold n = 3456 (2500)
+// 7.90 / 7.90; below it n = 3000 (1849) 5.56 / 5.54, symmetric n = 4096
+// (1830) 7.15 / 7.57, n = 2048 (784) 2.14 / 2.47, n = 1000 0.59 / 0.86.
 constexpr double PAIRS_TILES_64 = 2500.0;
 
 bool pairs_pay(const bs::Mats& m, int nb) {
