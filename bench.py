@@ -795,6 +795,7 @@ SCHEDULE_FLAGS = {"auto": 0, "t64": 1 << 5, "t128": 1 << 6,
                   "t64_serial": (1 << 5) | (1 << 7), "t128_serial": (1 << 6) | (1 << 7),
                   "perk": 1 << 2, "perk2": (1 << 2) | (1 << 10), "sym": 1 << 8,
                   "one": 1 << 11, "one_sym": (1 << 11) | (1 << 8),   # one launch per call
+                  "pairs": 1 << 12, "pairs64": (1 << 12) | (1 << 5),   # block rounds in pairs, forced
                   "graph": 0,   # "graph": the auto schedule captured once, replayed
                   "upper": 0}   # "upper": bs_smooth_upper, U alone
 ALL_SCHEDULES = ("auto", "t64", "t128", "t64_serial", "t128_serial", "sym")
@@ -804,9 +805,9 @@ SWEEP = (
     (1, "f32", ALL_SCHEDULES + ("graph", "one"), "chain n=1000"),
     (("random", 2048), "f32", ALL_SCHEDULES + ("graph", "one"), "random bounds n=2048"),
     (("random", 3000), "f32", ("auto", "t64", "t128", "t128_serial"), "random bounds n=3000"),
-    (2, "f32", ALL_SCHEDULES + ("perk", "perk2", "upper"), "globule n=4096"),
+    (2, "f32", ALL_SCHEDULES + ("pairs", "pairs64", "perk", "perk2", "upper"), "globule n=4096"),
     (2, "i32", ("auto",), "globule n=4096"),
-    (3, "f32", ALL_SCHEDULES + ("one", "one_sym"), "256 chains n=512, batched"),
+    (3, "f32", ALL_SCHEDULES + ("pairs64", "one", "one_sym"), "256 chains n=512, batched"),
     (4, "f32", ("auto", "t128_serial", "sym", "upper"), "globule n=16384"),
 )
 
