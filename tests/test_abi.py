@@ -52,6 +52,33 @@ def test_python_binding_has_the_c_names():
         assert hasattr(bsm, name), name
 
 
+def header_constants():
+    """BS_NAME = value pairs of the header's enums (values: integers and
+    shifts of integers)."""
+    out = {}
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"\b(BS_[A-Z0-9_]+)\s*=\s*(\d+(?:\s*<<\s*\d+)?)", text):
+            a, _, b = m.group(2).partition("<<")
+            out[m.group(1)] = int(a) << int(b) if b else int(a)
+    return out
+
+
+def test_binding_constants_match_the_header():
+    consts = header_constants()
+    for name in ("BS_OK", "BS_ERR_ARG", "BS_INT32_Q10", "BS_PERK", "BS_TILE_64", "BS_TILE_128",
+                 "BS_SYMMETRIC", "BS_PERK_PAIRED", "BS_ONE_LAUNCH", "BS_PAIRED_ROUNDS"):
+        assert name in consts, name
+    for name, value in consts.items():
+        if hasattr(bsm, name):
+            assert getattr(bsm, name) == value, name
+    bits = [v for k, v in consts.items()
+            if k in ("BS_PERK", "BS_RULE_LITERAL", "BS_VALIDATE", "BS_TILE_64", "BS_TILE_128",
+                     "BS_NO_LOOKAHEAD", "BS_SYMMETRIC", "BS_PERK_PAIRED", "BS_ONE_LAUNCH",
+                     "BS_PAIRED_ROUNDS")]
+    assert len(set(bits)) == len(bits) and all(b & (b - 1) == 0 for b in bits)   # distinct bits
+
+
 def test_strerror_and_counters(lib):
     for st in range(7):
         assert isinstance(bsm.bs_strerror(st), str) and bsm.bs_strerror(st)
