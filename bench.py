@@ -291,6 +291,22 @@ def committed_traffic(pass_cells):
     return per_pass_cell * float(pass_cells)
 
 
+def committed_capture_rate(alu_peak_ops):
+    """The committed capture's launch alone: 6-op rate of its cell updates
+    over its ncu duration (one launch, cold caches, nothing beside it) as a
+    fraction of the ALU peak, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "phase3_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash() or not d.get("gpu_time_ns"):
+        return None
+    ops = OPS_PER_CELL * float(d["cells_per_launch"])
+    return {"frac": ops / (d["gpu_time_ns"] * 1e-9) / alu_peak_ops,
+            "basis": "profiles/phase3_traffic.json: %s, alone under ncu" % d.get("workload", "")}
+
+
 # ------------------------------------------------------------------ clocks
 
 
@@ -716,6 +732,7 @@ def main():
                              "tile cells those launches pass over)",
             "algorithmic_bytes": algo_bytes,
             "traffic_over_algorithmic": (traffic / algo_bytes) if traffic else None,
+            "frac_alone_committed_capture": committed_capture_rate(alu_peak_ops),
             "algorithmic_bytes_basis": "16 bytes per tile cell per pass: each output tile of U "
                                        "and L read and written once per pass, a pass applying "
                                        "one block round, or two where rounds go in pairs",

@@ -210,3 +210,15 @@ def test_kernel_hash_ignores_comments_only():
     assert bench.code_only(a) == bench.code_only(b)
     assert bench.code_only(a) != bench.code_only(c)
     assert bench.code_only('s = "// kept";') == 's = "// kept";'
+
+
+def test_committed_capture_rate():
+    """The capture's own launch alone: its cell updates x 6 over its duration
+    against the ALU peak; at most the peak itself."""
+    peak = 152 * 128 * 2070e6
+    r = bench.committed_capture_rate(peak)
+    with open(os.path.join(bench.ROOT, "profiles", "phase3_traffic.json")) as f:
+        d = json.load(f)
+    assert r is not None
+    assert r["frac"] == pytest.approx(6 * d["cells_per_launch"] / (d["gpu_time_ns"] * 1e-9) / peak)
+    assert 0.5 < r["frac"] < 1.0
