@@ -110,6 +110,8 @@ def library() -> ctypes.CDLL:
         lib.bs_launch_count.restype = ll
         lib.bs_one_launch_cluster.argtypes = []
         lib.bs_one_launch_cluster.restype = i
+        lib.bs_schedule_info.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.bs_schedule_info.restype = i
         _lib = lib
         return lib
 
@@ -257,6 +259,16 @@ def bs_one_launch_cluster() -> int:
     """CTAs per cluster of BS_ONE_LAUNCH on the current device (0 before the
     first smoothing call on it)."""
     return int(library().bs_one_launch_cluster())
+
+
+def bs_schedule_info(n: int, batch: int = 1, mode: int = 0, bounds: bool = True) -> tuple:
+    """(tile width, block rounds in pairs) a blocked call would take; host
+    logic only, no GPU needed."""
+    tile, pairs = ctypes.c_int(0), ctypes.c_int(0)
+    _check(library().bs_schedule_info(int(n), int(batch), int(mode), int(bool(bounds)),
+                                      ctypes.byref(tile), ctypes.byref(pairs)),
+           "bs_schedule_info")
+    return tile.value, bool(pairs.value)
 
 
 def bs_profile_begin() -> None:

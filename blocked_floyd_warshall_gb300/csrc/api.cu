@@ -553,6 +553,27 @@ long long bs_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 int bs_one_launch_cluster(void) { return bs::fused_cluster_size(); }
 
+bs_status bs_schedule_info(int n, int batch, int mode, int bounds, int* tile, int* pairs) {
+    if (!tile || !pairs) return BS_ERR_ARG;
+    // the argument rules of a smoothing call on a contiguous layout; the two
+    // addresses are placeholders that check_args never dereferences
+    const int ld = n > 0 ? n : 1;
+    const long long span = n > 0 ? (long long)(n - 1) * ld + n : 1;
+    bs::Mats m;
+    bs_status st = check_args(reinterpret_cast<const void*>(256), reinterpret_cast<const void*>(512),
+                              bounds != 0, n, ld, span, batch, mode, &m);
+    if (st != BS_OK) return st;
+    const bool perk = (mode & BS_PERK) != 0;
+    if ((bounds && (mode & BS_RULE_LITERAL) && !perk) || (perk && (mode & BS_SYMMETRIC)))
+        return BS_ERR_ARG;
+    const int nb = n > 0 ? (n + m.fb - 1) / m.fb : 0;
+    *tile = perk ? 0 : m.fb;
+    // run_blocked: look-ahead from three block rows, then the pair rule
+    *pairs = !perk && !(mode & BS_ONE_LAUNCH) && !(mode & BS_NO_LOOKAHEAD) && nb >= 3 &&
+             ((mode & BS_PAIRED_ROUNDS) || pairs_pay(m, nb));
+    return BS_OK;
+}
+
 bs_status bs_profile_begin(void) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     for (auto& r : g_prof) {

@@ -210,6 +210,15 @@ long long bs_launch_count(void);
  * clusters of 4 or 8. */
 int bs_one_launch_cluster(void);
 
+/* The schedule a blocked smoothing call would take, without running it (host
+ * logic only: no GPU, stream or memory involved).  bounds: nonzero for
+ * bs_smooth_bounds(_batched), zero for bs_smooth_upper; n, batch and mode as
+ * in those calls (a contiguous layout is assumed).  *tile: 64 or 128, the tile
+ * width (0 with BS_PERK); *pairs: 1 if the bulk tiles take block rounds in
+ * pairs, else 0.  Mode bits the smoothing calls would reject give
+ * BS_ERR_ARG, as do null outputs. */
+bs_status bs_schedule_info(int n, int batch, int mode, int bounds, int *tile, int *pairs);
+
 /* Per-phase device time.  After bs_profile_begin(), every smoothing call
  * records a CUDA event pair around each of its kernel launches, on the stream
  * the kernel runs on (the caller's, or the library's look-ahead stream).

@@ -222,3 +222,31 @@ def test_committed_capture_rate():
     assert r is not None
     assert r["frac"] == pytest.approx(6 * d["cells_per_launch"] / (d["gpu_time_ns"] * 1e-9) / peak)
     assert 0.5 < r["frac"] < 1.0
+
+
+def test_bench_rules_match_the_library():
+    """bench.py's copies of the tile and pair rules give what the library
+    itself would run (bs_schedule_info, host logic only)."""
+    import blocked_floyd_warshall_gb300 as bsm
+    bsm.build()
+    sizes = [1, 2, 63, 64, 65, 128, 129, 256, 300, 385, 513, 1000, 2048, 3000, 3392, 3456, 3584,
+             4096, 5120, 6016, 6017, 6144, 8192, 10000, 12160, 12161, 16384, 20000]
+    modes = [0, bsm.BS_TILE_64, bsm.BS_TILE_128, bsm.BS_SYMMETRIC, bsm.BS_PAIRED_ROUNDS,
+             bsm.BS_PAIRED_ROUNDS | bsm.BS_TILE_64, bsm.BS_NO_LOOKAHEAD,
+             bsm.BS_SYMMETRIC | bsm.BS_TILE_128]
+    checked = 0
+    for n in sizes:
+        for batch in (1, 3, 64, 256):
+            if n * n * batch > 2 ** 31:
+                continue
+            for mode in modes:
+                for bounds in (True, False):
+                    tile, pairs = bsm.bs_schedule_info(n, batch, mode, bounds)
+                    want_tile = bench.tile_size(n, flags=mode, batch=batch, upper=not bounds)
+                    assert tile == want_tile, (n, batch, mode, bounds, tile, want_tile)
+                    want_pairs = bench.pair_schedule_runs(n, tile, flags=mode,
+                                                          sym=bool(mode & bsm.BS_SYMMETRIC),
+                                                          batch=batch)
+                    assert pairs == want_pairs, (n, batch, mode, bounds, pairs, want_pairs)
+                    checked += 1
+    assert checked > 1000
